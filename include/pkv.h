@@ -1,0 +1,301 @@
+/*
+ * pkv.h -- C ABI of libpkv: paged KV-cache decode attention for GB300 (sm_103a).
+ *
+ * What the library computes (sources cited by page title and section):
+ *
+ *  - A flat pool of fixed-size physical KV blocks (16 tokens by default) and
+ *    a per-sequence block table mapping logical block i (tokens 16i..16i+15)
+ *    to a physical block ("The 8GB VRAM Breakthrough", §3 "How
+ *    Logical-to-Physical Block Tables Work").  The pool is a stack of free
+ *    block ids plus one reference count per block ("A Ideia de 60 Anos Que
+ *    Domou a Memória da GPU", section "o código: a diferença entre reservar e
+ *    mapear"); blocks are taken on demand when the current one is full (same
+ *    page, section "a ideia roubada").
+ *  - Prefix sharing by reference counts and copy-on-write of a *partially
+ *    filled* shared block on the first divergent write ("The 8GB VRAM
+ *    Breakthrough", §3 "Copy-on-Write (CoW) Prefix Sharing").
+ *  - The KV-append write of each new token ("The 8GB VRAM Breakthrough", §1:
+ *    every generated token writes one new KV vector back).
+ *  - Single-query grouped-query attention through the block tables ("The 8GB
+ *    VRAM Breakthrough", §3: the kernel gathers the scattered physical blocks
+ *    for QK^T and the softmax-weighted sum of V).  Paging does not change the
+ *    result ("PagedAttention aplica memória virtual ao cache KV de LLMs",
+ *    section "Compartilhamento e compromissos"): the output is plain
+ *    softmax(scale * q K^T) V over the sequence's tokens in logical order.
+ *  - An INT4-asymmetric / FP8-E4M3 cache with the first n_sink tokens kept in
+ *    16-bit, dequantised in registers inside the attention kernel ("The 8GB
+ *    VRAM Breakthrough", §4 "The Hybrid Solution: Sink-FP16 + Group-Wise
+ *    Asymmetric INT4 / FP8" and §5 "On-the-Fly Register Dequantization").
+ *
+ * Conventions (all entry points):
+ *  - Every function returns an int status: PKV_OK (0) or a negative PKV_ERR_*.
+ *    No exception or C++ object crosses the ABI; results go to out-params.
+ *  - Host handles (pkv_pool*) are created and owned by the library; release
+ *    them with pkv_pool_destroy.  Host calls on one pool are not thread-safe.
+ *  - ALL device memory is owned by the caller (pools, tables, workspaces,
+ *    outputs).  The library never allocates or frees device memory.
+ *  - Device entry points are asynchronous on the caller's cudaStream_t,
+ *    passed as void* (NULL = legacy default stream).  A failed launch returns
+ *    PKV_ERR_CUDA.  Arguments are validated on the host before any launch
+ *    (PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED / PKV_ERR_MISALIGNED /
+ *    PKV_ERR_WORKSPACE); data-dependent indices (table entries, slots, context
+ *    lengths) are checked on the device: an out-of-range index is skipped (it
+ *    is never dereferenced) and a bit is set in a per-device status word that
+ *    pkv_device_status reads back.
+ *  - Device pointers must be 16-byte aligned.  16-bit data is IEEE fp16
+ *    (PKV_DTYPE_F16) or bfloat16 (PKV_DTYPE_BF16).
+ *  - Layouts are row-major (last index fastest):
+ *      q, out           [batch, num_q_heads, head_dim]          16-bit
+ *      k, v (new rows)  [num_tokens, num_kv_heads, head_dim]    16-bit
+ *      k_pool, v_pool   [num_blocks, num_kv_heads, block_size, head_dim]
+ *      block_tables     [batch, max_blocks] int32, entries past the context
+ *                       are not read (the host manager pads them with -1)
+ *      context_lens     [batch] int32, tokens per sequence INCLUDING the
+ *                       token appended in this decode step
+ *      slot_mapping     [num_tokens] int64, slot = block * block_size + offset;
+ *                       a negative slot skips that token
+ *  - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,   /* null pointer, bad size or shape            */
+    PKV_ERR_OUT_OF_BLOCKS = -2, /* pool cannot supply the blocks; no change   */
+    PKV_ERR_BAD_HANDLE = -3,    /* null pool handle                           */
+    PKV_ERR_BAD_SEQ = -4,       /* unknown sequence id                        */
+    PKV_ERR_DOUBLE_FREE = -5,   /* refcount of a free block would go below 0  */
+    PKV_ERR_CUDA = -6,          /* a CUDA runtime call or launch failed       */
+    PKV_ERR_DEVICE_BOUNDS = -7, /* device status word had an index error      */
+    PKV_ERR_UNSUPPORTED = -8,   /* valid but not implemented shape / mode     */
+    PKV_ERR_WORKSPACE = -9,     /* workspace missing or too small             */
+    PKV_ERR_MISALIGNED = -10    /* a device pointer is not 16-byte aligned    */
+};
+
+enum { PKV_DTYPE_F16 = 0, PKV_DTYPE_BF16 = 1 };
+enum { PKV_QMODE_INT4_ASYM = 1, PKV_QMODE_FP8_E4M3 = 2 };
+
+/* Device status bits (see pkv_device_status). */
+enum {
+    PKV_STATUS_BAD_BLOCK = 1,   /* block-table entry outside [0, num_blocks)     */
+    PKV_STATUS_BAD_SLOT = 2,    /* slot outside [0, num_blocks * block_size)     */
+    PKV_STATUS_BAD_CONTEXT = 4, /* context_len < 0 or > max_blocks * block_size  */
+    PKV_STATUS_BAD_PAIR = 8,    /* copy pair outside [0, num_blocks)             */
+    PKV_STATUS_BAD_SINK = 16    /* sink row / position outside its buffer        */
+};
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* pkv_status_string(int status);
+
+/* Library ABI version (monotonic integer). */
+int pkv_version(void);
+
+/* ====================================================== host block manager
+ * Physical block pool with a LIFO free stack and one reference count per
+ * block, plus sequences with block tables ("A Ideia de 60 Anos...", section
+ * "o código"; "The 8GB VRAM Breakthrough", §3).
+ */
+typedef struct pkv_pool pkv_pool;
+
+/* Create a pool of num_blocks blocks of block_size tokens.  free_order
+ * (host, nullable, num_blocks entries, a permutation of 0..num_blocks-1)
+ * fixes the allocation order: successive allocations from a fresh pool
+ * return free_order[0], free_order[1], ...; NULL means 0, 1, 2, ....
+ * Errors: INVALID_ARG (sizes <= 0, not a permutation). */
+int pkv_pool_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order,
+                    pkv_pool** out);
+int pkv_pool_destroy(pkv_pool* pool);
+int pkv_pool_num_free(const pkv_pool* pool, int32_t* out);
+int pkv_pool_num_blocks(const pkv_pool* pool, int32_t* out);
+int pkv_pool_block_size(const pkv_pool* pool, int32_t* out);
+
+/* Pop a free block and set its count to 1.  OUT_OF_BLOCKS if none. */
+int pkv_block_alloc(pkv_pool* pool, int32_t* block);
+/* Add an owner to an allocated block.  DOUBLE_FREE if the block is free. */
+int pkv_block_incref(pkv_pool* pool, int32_t block);
+/* Drop an owner; at zero the block is pushed back on the free stack.
+ * DOUBLE_FREE if the count is already zero. */
+int pkv_block_decref(pkv_pool* pool, int32_t block);
+int pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* out);
+
+/* New empty sequence.  Ids are 0, 1, 2, ... in creation order (forks too). */
+int pkv_seq_create(pkv_pool* pool, int64_t* seq);
+/* Give back every block of the sequence in logical order.  BAD_SEQ. */
+int pkv_seq_free(pkv_pool* pool, int64_t seq);
+/* Child sharing all of the parent's blocks (each count + 1), same length. */
+int pkv_seq_fork(pkv_pool* pool, int64_t parent, int64_t* child);
+
+/* Reserve slots for n_tokens new tokens of seq (the copy-on-write append).
+ * If the tail block is partially filled and shared (count > 1) it is first
+ * replaced by a fresh block and one (src, dst) copy is reported; then a new
+ * block is taken each time the tail fills.
+ *   slots_out       host int64[n_tokens]: slot of each new token
+ *   copy_pairs_out  host int32[2] (nullable if the caller guarantees no CoW):
+ *                   {src, dst} of the block the caller must copy (K, V and any
+ *                   quantisation metadata) before writing the new tokens
+ *   n_copies        host int32: 0 or 1
+ * All-or-nothing: OUT_OF_BLOCKS leaves the pool and the sequence unchanged. */
+int pkv_seq_append(pkv_pool* pool, int64_t seq, int32_t n_tokens, int64_t* slots_out,
+                   int32_t* copy_pairs_out, int32_t* n_copies);
+
+/* One decode step for n sequences: appends n_tokens_each tokens to each of
+ * seqs[0..n-1] in order.  slots_out int64[n * n_tokens_each];
+ * copy_pairs_out int32[2 * n] (pairs in sequence order); n_copies total.
+ * All-or-nothing across the whole batch. */
+int pkv_seq_append_batch(pkv_pool* pool, const int64_t* seqs, int32_t n, int32_t n_tokens_each,
+                         int64_t* slots_out, int32_t* copy_pairs_out, int32_t* n_copies);
+
+int pkv_seq_len(const pkv_pool* pool, int64_t seq, int64_t* out);
+int pkv_seq_num_blocks(const pkv_pool* pool, int64_t seq, int32_t* out);
+/* Copy the sequence's table into out[0..capacity); INVALID_ARG if it does
+ * not fit. */
+int pkv_seq_block_table(const pkv_pool* pool, int64_t seq, int32_t* out, int32_t capacity);
+
+/* Build the decode inputs for seqs[0..n-1]: tables (host int32 [n, max_blocks],
+ * unused entries -1) and context_lens (host int32 [n]).  INVALID_ARG if a
+ * sequence has more than max_blocks blocks. */
+int pkv_build_block_tables(const pkv_pool* pool, const int64_t* seqs, int32_t n, int32_t* tables,
+                           int32_t max_blocks, int32_t* context_lens);
+
+/* Fault injection: after n more successful block allocations, every further
+ * allocation fails with OUT_OF_BLOCKS (appends stay all-or-nothing).
+ * n < 0 disables. */
+int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
+
+/* ================================================================ sizes */
+
+/* Bytes of the split-K workspace pkv_paged_attention_decode* needs for this
+ * shape: fp32 partial outputs [batch, num_q_heads, P, head_dim] and fp32
+ * (max, sum) pairs [batch, num_q_heads, P, 2], P = ceil(max_blocks *
+ * block_size / partition_size).  partition_size 0 selects the default (512);
+ * otherwise it must be a positive multiple of block_size.  Zero when a
+ * single partition covers max_blocks * block_size (single-pass decode). */
+int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                               int32_t max_blocks, int32_t block_size, int32_t partition_size,
+                               size_t* out);
+
+/* =============================================================== device */
+
+/* KV-append scatter: for every token t with slot_mapping[t] >= 0,
+ * k_pool[slot / block_size, h, slot % block_size, :] = k[t, h, :] (and the
+ * same for v), bit-exact.  head_dim % 8 == 0.  Slots beyond the pool set
+ * PKV_STATUS_BAD_SLOT and are skipped. */
+int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int32_t num_tokens,
+                  void* k_pool, void* v_pool, int32_t num_blocks, int32_t num_kv_heads,
+                  int32_t head_dim, int32_t block_size, int dtype, void* stream);
+
+/* Paged decode attention: out[b, h, :] = sum_t softmax_t(scale *
+ * <q[b, h], K_t>) V_t over the tokens t < context_lens[b] of sequence b,
+ * where K_t / V_t are read from k_pool / v_pool at block
+ * block_tables[b, t / block_size], offset t % block_size, KV head
+ * h / (num_q_heads / num_kv_heads).  fp32 accumulation; out has q's dtype;
+ * a sequence with context 0 gets zeros.
+ * The context is cut into partitions of partition_size tokens (0 = 512)
+ * processed by independent CTAs; when more than one partition can occur
+ * (max_blocks * block_size > partition_size) partial (max, sum, output)
+ * triples go to `workspace` (device, >= pkv_decode_workspace_bytes) and a
+ * second kernel merges them with a log-sum-exp rescale (flash-decoding
+ * split-K); otherwise the first kernel writes out directly.
+ * Supported: block_size 16, head_dim 64 or 128, 1 <= num_q_heads /
+ * num_kv_heads <= 8 (else UNSUPPORTED). */
+int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, const int32_t* context_lens,
+                               int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                               int32_t max_blocks, float scale, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t partition_size, int dtype,
+                               void* stream);
+
+/* The two phases of pkv_paged_attention_decode, for callers that time or
+ * overlap them.  _partials always writes the workspace (never out);
+ * _merge reads it and writes out.  Same arguments and requirements. */
+int pkv_paged_attention_decode_partials(const void* q, const void* k_pool, const void* v_pool,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                        int32_t max_blocks, float scale, void* workspace,
+                                        size_t workspace_bytes, int32_t partition_size, int dtype,
+                                        void* stream);
+int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
+                                     int32_t num_q_heads, int32_t head_dim, int32_t max_blocks,
+                                     int32_t block_size, int32_t partition_size,
+                                     const void* workspace, size_t workspace_bytes, void* out,
+                                     int dtype, void* stream);
+
+/* Quantised KV-append ("The 8GB VRAM Breakthrough", §4; §5 flowchart: fused
+ * quantiser on the write path).  For every token t with slot >= 0 and every
+ * KV head, K and V rows are quantised and written at the slot:
+ *   INT4_ASYM: per group of group_size elements (group_size divides head_dim;
+ *     supported: head_dim, 64, 32), binary32 steps in this order
+ *     s = fp16(binary32(max - min) / 15), s = 1 if max == min or s == 0;
+ *     z = fp16(binary32(-min) / s), -0 stored as +0;
+ *     q = clamp(rint(binary32(x / s) + z), 0, 15)
+ *     (fp16() rounds to nearest even, saturating at 65504); codes packed two
+ *     per byte, element 2i in the low nibble.
+ *     k_codes/v_codes u8 [num_blocks, Hkv, block_size, head_dim/2];
+ *     k_scale/k_zero/v_scale/v_zero fp16 [num_blocks, Hkv, block_size,
+ *     head_dim/group_size].  Dequantised value: (q - z) * s.
+ *   FP8_E4M3: one scale per (token, head): s = fp16(max|x| / 448), 1 if 0;
+ *     code = E4M3 (OCP e4m3fn) of binary32(x / s), nearest even, saturating
+ *     at +-448.  k_codes/v_codes u8 [num_blocks, Hkv, block_size, head_dim];
+ *     k_scale/v_scale fp16 [num_blocks, Hkv, block_size, 1]; zeros unused
+ *     (may be NULL).  group_size is ignored.
+ * Sinks: if positions[t] < n_sink, the 16-bit row is also copied to
+ * sink_k/sink_v[seq_idx[t], positions[t], h, :]; sink buffers are
+ * [sink_rows, n_sink, Hkv, head_dim] in dtype (nullable when n_sink == 0).
+ * positions / seq_idx: device int32 [num_tokens]. */
+int pkv_kv_append_quant(const void* k, const void* v, const int64_t* slot_mapping,
+                        const int32_t* positions, const int32_t* seq_idx, int32_t num_tokens,
+                        void* k_codes, void* k_scale, void* k_zero, void* v_codes,
+                        void* v_scale, void* v_zero, void* sink_k, void* sink_v, int32_t n_sink,
+                        int32_t sink_rows, int32_t num_blocks, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t block_size, int32_t group_size, int qmode,
+                        int dtype, void* stream);
+
+/* Decode attention over a quantised cache: as pkv_paged_attention_decode
+ * with K_t, V_t the dequantised values ((q - z) * s for INT4, e4m3 * s for
+ * FP8), except that positions t < n_sink read sink_k/sink_v[b, t, kv_head]
+ * (16-bit, row b of the sink buffers belongs to batch entry b).  q and out
+ * are 16-bit (dtype).  Supported: block_size 16, head_dim 128 or 64,
+ * group_size == head_dim for INT4, n_sink <= block_size, 1 <= G <= 8. */
+int pkv_paged_attention_decode_quant(const void* q, const void* k_codes, const void* k_scale,
+                                     const void* k_zero, const void* v_codes, const void* v_scale,
+                                     const void* v_zero, const void* sink_k, const void* sink_v,
+                                     int32_t n_sink, const int32_t* block_tables,
+                                     const int32_t* context_lens, int32_t batch,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t num_blocks, int32_t block_size, int32_t max_blocks,
+                                     int32_t group_size, float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, int32_t partition_size, int qmode,
+                                     int dtype, void* stream);
+
+/* Copy-on-write block copy ("The 8GB VRAM Breakthrough", §3; "A Ideia de 60
+ * Anos...", section "o bônus que paga o ingresso"): for each pair i,
+ * block pairs[2i+1] of every pool becomes a byte copy of block pairs[2i].
+ *   pools            host array of n_pools device pointers (1..8)
+ *   bytes_per_block  host int64[n_pools], each a multiple of 16
+ *   pairs            device int32 [n_pairs, 2] (src, dst)
+ * Pairs outside [0, num_blocks) set PKV_STATUS_BAD_PAIR and are skipped.
+ * Pairs must not chain (no dst used as another pair's src). */
+int pkv_copy_blocks(void* const* pools, const int64_t* bytes_per_block, int32_t n_pools,
+                    const int32_t* pairs, int32_t n_pairs, int32_t num_blocks, void* stream);
+
+/* Read and clear the current device's status word (synchronises `stream`).
+ * *status receives the PKV_STATUS_* bits seen since the last call; returns
+ * PKV_ERR_DEVICE_BOUNDS if any bit was set, PKV_OK otherwise. */
+int pkv_device_status(int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -9,7 +9,8 @@ the stored types), every step an IEEE binary32 operation, in this order:
 
 1. mn, mx = min and max of the group (exact in binary32 for 16-bit inputs);
 2. s = fp16(binary32(mx - mn) / 15); if mx == mn or s == 0 then s = 1;
-3. z = fp16(binary32(-mn) / s)            (a floating zero point, stored fp16);
+3. z = fp16(binary32(-mn) / s)            (a floating zero point, stored fp16;
+   a zero point of -0 is stored as +0, since min(-0, +0) may be either);
 4. q = clamp(rint_half_even(binary32(binary32(x / s) + z)), 0, 15);
    fp16() rounds to nearest even and saturates to +-65504.
 
@@ -70,6 +71,8 @@ def int4_quantize_group(x):
     if mx == mn or s16 == 0:
         s16 = np.float16(1.0)
     z16 = fp16_sat(np.float32(-mn) / np.float32(s16))
+    if z16 == 0:
+        z16 = np.float16(0.0)
     codes = np.empty(x.shape[0], dtype=np.uint8)
     s32 = np.float32(s16)
     z32 = np.float32(z16)
@@ -104,6 +107,7 @@ def int4_quantize_rows(X, group_size):
     s16[degenerate] = np.float16(1.0)
     s32 = s16.astype(np.float32)
     z16 = _fp16_sat_array((-mn) / s32)
+    z16[z16 == 0] = np.float16(0.0)
     z32 = z16.astype(np.float32)
     v = (Xg / s32[..., None]) + z32[..., None]
     q = np.clip(np.rint(v), 0.0, 15.0).astype(np.uint8)

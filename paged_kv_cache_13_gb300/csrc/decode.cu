@@ -1,0 +1,497 @@
+// Paged single-query GQA decode attention over a 16-bit (bf16 / fp16) cache.
+//
+// What it computes: for sequence b and query head h (KV head h / G),
+//   out[b, h] = sum_t softmax_t(scale * <q[b, h], K_t>) V_t,  t < ctx_b,
+// with K_t, V_t gathered through the block table ("The 8GB VRAM
+// Breakthrough", §3 "How Logical-to-Physical Block Tables Work": the kernel
+// reads the table on the fly and gathers the non-contiguous physical blocks
+// for QK^T and the softmax-weighted sum of V).
+//
+// Design (sm_103a):
+// * Work unit = (sequence, KV head, partition of `part_blocks` blocks).  One
+//   CTA of NW warps per unit; the warps take the partition's blocks
+//   round-robin, each keeping its own online-softmax state (running max m,
+//   sum l, accumulator o) for the G query heads of the KV head; the CTA merges
+//   the warps through shared memory at the end.  With more than one partition
+//   per sequence the CTA writes an fp32 (m, l, o) partial and a second kernel
+//   merges the partials with a log-sum-exp rescale (flash-decoding split-K).
+// * A block of one KV head is 16 tokens x D contiguous 16-bit values (4 KiB
+//   for D = 128).  Each lane issues 16-byte loads straight from global memory
+//   into registers, shaped so that the registers ARE the tensor-core fragments
+//   (no shared-memory staging, no shuffles of K or V):
+//     QK^T : S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]   (mma m16n8k16,
+//            tokens as M, the GQA group as N, head dim as K).  Lane (g, c)
+//            (g = lane / 4, c = lane % 4) loads K rows g and g+8 at
+//            [32i + 8c, +8): a 16-byte piece whose four 32-bit words are the
+//            A-fragment registers of two k-steps.  The k order inside a
+//            k-step is permuted, and Q's B fragment uses the same permutation.
+//     PV   : O^T[D x 8 heads] = V^T[D x 16 tok] . P^T[16 tok x 8]  (head dim
+//            as M, heads as N, tokens as K).  Lane (g, c) loads V rows
+//            2c, 2c+1, 8+2c, 9+2c at [64j + 8g, +8); one byte-permute per
+//            register pairs two tokens of the same column into the A fragment.
+//            P^T comes from the QK^T accumulator by one 8x8 movmatrix
+//            transpose per half-block.
+//   Heads beyond G in the N dimension carry zero queries and are ignored.
+// * Online softmax in base 2 (logits pre-multiplied by scale * log2 e);
+//   block max by three xor-shuffles across the 8 token lanes; the running sum
+//   stays a per-lane partial until the end.
+// * Tokens at or past ctx in the last block get logit -inf, and their V rows
+//   are zeroed in registers (an unwritten slot may hold NaN bit patterns).
+
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int BS = 16;  // tokens per block (the kernels are specialised to 16)
+constexpr int NW = 4;   // warps per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeArgs {
+    const void* q;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    int hq, hkv, G, num_blocks, max_blocks, part_blocks, max_parts;
+    float scale_log2;
+    void* out;
+    float* ws_o;   // [B, Hq, max_parts, D]
+    float* ws_ml;  // [B, Hq, max_parts, 2]
+    int* status;
+};
+
+// Element e (0 .. D/8-1) of lane group g in the PV fragment layout sits at
+// head-dim column 64 * (e / 8) + 8 * g + e % 8.
+template <int D>
+__device__ __forceinline__ int pv_col(int e, int g) {
+    return 64 * (e >> 3) + 8 * g + (e & 7);
+}
+
+template <typename T, int D, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) {
+    using H = Half16<T>;
+    constexpr int KC = D / 32;  // 16-byte K pieces per lane per row
+    constexpr int VC = D / 64;  // 16-byte V pieces per lane per row
+    constexpr int MT = D / 16;  // PV m-tiles
+
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+
+    int ctx = a.ctx_lens[b];
+    const int cap = a.max_blocks * BS;
+    if (ctx < 0 || ctx > cap) {
+        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int nblk = (ctx + BS - 1) / BS;
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    if (p >= (nparts > 0 ? nparts : 1)) return;
+    const int blk_begin = p * a.part_blocks;
+    const int blk_end = min(blk_begin + a.part_blocks, nblk);
+
+    // Q^T B-fragments: lane (g, c) holds query head g's columns [32i + 8c, +8).
+    uint4 qf[KC];
+    if (g < a.G) {
+        const T* qrow = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * a.G + g) * D;
+#pragma unroll
+        for (int i = 0; i < KC; ++i) qf[i] = *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * c);
+    } else {
+#pragma unroll
+        for (int i = 0; i < KC; ++i) qf[i] = make_uint4(0, 0, 0, 0);
+    }
+
+    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    float o[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    const T* kpool = static_cast<const T*>(a.k_pool);
+    const T* vpool = static_cast<const T*>(a.v_pool);
+    const int vrow0 = 2 * c, vrow1 = 2 * c + 1, vrow2 = 8 + 2 * c, vrow3 = 9 + 2 * c;
+
+    for (int lb = blk_begin + warp; lb < blk_end; lb += NW) {
+        const int phys = trow[lb];
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            continue;
+        }
+        const int64_t base = (static_cast<int64_t>(phys) * a.hkv + kvh) * (BS * D);
+        const T* kb = kpool + base;
+        const T* vb = vpool + base;
+
+        uint4 kr0[KC], kr1[KC], vr[4][VC];
+#pragma unroll
+        for (int i = 0; i < KC; ++i) {
+            kr0[i] = ldg_stream(kb + g * D + 32 * i + 8 * c);
+            kr1[i] = ldg_stream(kb + (g + 8) * D + 32 * i + 8 * c);
+        }
+#pragma unroll
+        for (int j = 0; j < VC; ++j) {
+            vr[0][j] = ldg_stream(vb + vrow0 * D + 64 * j + 8 * g);
+            vr[1][j] = ldg_stream(vb + vrow1 * D + 64 * j + 8 * g);
+            vr[2][j] = ldg_stream(vb + vrow2 * D + 64 * j + 8 * g);
+            vr[3][j] = ldg_stream(vb + vrow3 * D + 64 * j + 8 * g);
+        }
+
+        // ---- S^T = K Q^T: s[0]=S(t=g,h=2c) s[1]=S(g,2c+1) s[2]=S(g+8,2c) s[3]=S(g+8,2c+1)
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < KC; ++i) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                H::mma(s, word(kr0[i], 2 * e), word(kr1[i], 2 * e), word(kr0[i], 2 * e + 1),
+                       word(kr1[i], 2 * e + 1), word(qf[i], 2 * e), word(qf[i], 2 * e + 1));
+            }
+        }
+        const int tok0 = lb * BS + g;
+        const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
+        const float x0 = ok0 ? s[0] * a.scale_log2 : neg_inf();
+        const float x1 = ok0 ? s[1] * a.scale_log2 : neg_inf();
+        const float x2 = ok1 ? s[2] * a.scale_log2 : neg_inf();
+        const float x3 = ok1 ? s[3] * a.scale_log2 : neg_inf();
+
+        // ---- online softmax (base 2); heads 2c (x0, x2) and 2c+1 (x1, x3)
+        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+        const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+        const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        // P^T B-fragments: transpose the two 8x8 (token x head) halves.
+        const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+
+        if (lb * BS + BS > ctx) {  // last, partial block: zero masked V rows
+            const int t0 = lb * BS;
+#pragma unroll
+            for (int j = 0; j < VC; ++j) {
+                if (t0 + vrow0 >= ctx) vr[0][j] = make_uint4(0, 0, 0, 0);
+                if (t0 + vrow1 >= ctx) vr[1][j] = make_uint4(0, 0, 0, 0);
+                if (t0 + vrow2 >= ctx) vr[2][j] = make_uint4(0, 0, 0, 0);
+                if (t0 + vrow3 >= ctx) vr[3][j] = make_uint4(0, 0, 0, 0);
+            }
+        }
+
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            constexpr int HALF = D / 16;
+            const int elo = mt, ehi = mt + HALF;
+            const int jl = elo >> 3, wl = (elo & 7) >> 1, hl = elo & 1;
+            const int jh = ehi >> 3, wh = (ehi & 7) >> 1, hh = ehi & 1;
+            const uint32_t sl = hl ? 0x7632u : 0x5410u;
+            const uint32_t sh = hh ? 0x7632u : 0x5410u;
+            const uint32_t a0 = __byte_perm(word(vr[0][jl], wl), word(vr[1][jl], wl), sl);
+            const uint32_t a1 = __byte_perm(word(vr[0][jh], wh), word(vr[1][jh], wh), sh);
+            const uint32_t a2 = __byte_perm(word(vr[2][jl], wl), word(vr[3][jl], wl), sl);
+            const uint32_t a3 = __byte_perm(word(vr[2][jh], wh), word(vr[3][jh], wh), sh);
+            H::mma(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+    }
+
+    // finish the per-lane partial sums over the 8 token lanes
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+
+    // ---- merge the NW warps of the CTA
+    __shared__ float sm_ml[NW][8][2];
+    __shared__ float sm_o[NW][8][D];
+    if (g == 0) {
+        sm_ml[warp][2 * c][0] = m0;
+        sm_ml[warp][2 * c][1] = l0;
+        sm_ml[warp][2 * c + 1][0] = m1;
+        sm_ml[warp][2 * c + 1][1] = l1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int dl = pv_col<D>(mt, g), dh = pv_col<D>(mt + D / 16, g);
+        sm_o[warp][2 * c][dl] = o[mt][0];
+        sm_o[warp][2 * c + 1][dl] = o[mt][1];
+        sm_o[warp][2 * c][dh] = o[mt][2];
+        sm_o[warp][2 * c + 1][dh] = o[mt][3];
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < a.G * D; idx += NW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_ml[w][h][0]);
+        float acc = 0.f, L = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float sc = ex2(sm_ml[w][h][0] - M);
+                acc += sc * sm_o[w][h][d];
+                L += sc * sm_ml[w][h][1];
+            }
+        }
+        const int64_t qh = static_cast<int64_t>(b) * a.hq + kvh * a.G + h;
+        if constexpr (SPLIT) {
+            const int64_t row = qh * a.max_parts + p;
+            a.ws_o[row * D + d] = acc;
+            if (d == 0) {
+                a.ws_ml[2 * row] = M;
+                a.ws_ml[2 * row + 1] = L;
+            }
+        } else {
+            static_cast<T*>(a.out)[qh * D + d] = H::from_float(L > 0.f ? acc / L : 0.f);
+        }
+    }
+}
+
+// Merge the partition partials of one (sequence, query head): one thread per
+// head-dim column.
+template <typename T, int D>
+__global__ void __launch_bounds__(D) merge_kernel(const int32_t* __restrict__ ctx_lens, int hq,
+                                                 int max_blocks, int part_blocks, int max_parts,
+                                                 const float* __restrict__ ws_o,
+                                                 const float* __restrict__ ws_ml, T* __restrict__ out) {
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    int ctx = ctx_lens[b];
+    const int cap = max_blocks * BS;
+    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+    const int nblk = (ctx + BS - 1) / BS;
+    const int np = (nblk + part_blocks - 1) / part_blocks;
+    const int64_t row0 = (static_cast<int64_t>(b) * hq + h) * max_parts;
+    float M = neg_inf();
+    for (int p = 0; p < np; ++p) M = fmaxf(M, ws_ml[2 * (row0 + p)]);
+    float acc = 0.f, L = 0.f;
+    if (M != neg_inf()) {
+        for (int p = 0; p < np; ++p) {
+            const float sc = ex2(ws_ml[2 * (row0 + p)] - M);
+            acc += sc * ws_o[(row0 + p) * D + d];
+            L += sc * ws_ml[2 * (row0 + p) + 1];
+        }
+    }
+    out[(static_cast<int64_t>(b) * hq + h) * D + d] = Half16<T>::from_float(L > 0.f ? acc / L : 0.f);
+}
+
+struct Shape {
+    int batch, hq, hkv, D, num_blocks, block_size, max_blocks, part_blocks, max_parts;
+};
+
+int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_blocks,
+                int32_t block_size, int32_t max_blocks, int32_t partition_size, int dtype,
+                Shape* s) {
+    if (batch < 0 || hq <= 0 || hkv <= 0 || D <= 0 || num_blocks <= 0 || block_size <= 0 ||
+        max_blocks < 0 || partition_size < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_INVALID_ARG;
+    if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (block_size != BS || (D != 64 && D != 128) || hq / hkv > 8) return PKV_ERR_UNSUPPORTED;
+    if (batch > 65535 || hkv > 65535) return PKV_ERR_UNSUPPORTED;
+    if (partition_size == 0) partition_size = 512;
+    if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
+    s->batch = batch;
+    s->hq = hq;
+    s->hkv = hkv;
+    s->D = D;
+    s->num_blocks = num_blocks;
+    s->block_size = block_size;
+    s->max_blocks = max_blocks;
+    s->part_blocks = partition_size / block_size;
+    s->max_parts = (max_blocks + s->part_blocks - 1) / s->part_blocks;
+    if (s->max_parts < 1) s->max_parts = 1;
+    return PKV_OK;
+}
+
+size_t ws_bytes(const Shape& s) {
+    return static_cast<size_t>(s.batch) * s.hq * s.max_parts * (s.D + 2) * sizeof(float);
+}
+
+template <typename T, int D, bool SPLIT>
+void launch_partitions(const DecodeArgs& a, const Shape& s, cudaStream_t st) {
+    dim3 grid(SPLIT ? s.max_parts : 1, s.hkv, s.batch);
+    paged_decode_kernel<T, D, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+}
+
+template <bool SPLIT>
+int run_partitions(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
+    if (dtype == PKV_DTYPE_BF16) {
+        if (s.D == 128) launch_partitions<__nv_bfloat16, 128, SPLIT>(a, s, st);
+        else launch_partitions<__nv_bfloat16, 64, SPLIT>(a, s, st);
+    } else {
+        if (s.D == 128) launch_partitions<__half, 128, SPLIT>(a, s, st);
+        else launch_partitions<__half, 64, SPLIT>(a, s, st);
+    }
+    return launch_status();
+}
+
+int run_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, const float* ws_ml,
+              void* out, int dtype, cudaStream_t st) {
+    dim3 grid(s.hq, s.batch);
+    if (dtype == PKV_DTYPE_BF16) {
+        if (s.D == 128)
+            merge_kernel<__nv_bfloat16, 128><<<grid, 128, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__nv_bfloat16*>(out));
+        else
+            merge_kernel<__nv_bfloat16, 64><<<grid, 64, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__nv_bfloat16*>(out));
+    } else {
+        if (s.D == 128)
+            merge_kernel<__half, 128><<<grid, 128, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__half*>(out));
+        else
+            merge_kernel<__half, 64><<<grid, 64, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__half*>(out));
+    }
+    return launch_status();
+}
+
+int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_pool,
+              const int32_t* tables, const int32_t* ctx_lens, const Shape& s, float scale) {
+    if (!q || !k_pool || !v_pool || !tables || !ctx_lens) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(tables) & 3u) || (reinterpret_cast<uintptr_t>(ctx_lens) & 3u))
+        return PKV_ERR_MISALIGNED;
+    int* st = status_word();
+    if (!st) return PKV_ERR_CUDA;
+    a->q = q;
+    a->k_pool = k_pool;
+    a->v_pool = v_pool;
+    a->tables = tables;
+    a->ctx_lens = ctx_lens;
+    a->hq = s.hq;
+    a->hkv = s.hkv;
+    a->G = s.hq / s.hkv;
+    a->num_blocks = s.num_blocks;
+    a->max_blocks = s.max_blocks;
+    a->part_blocks = s.part_blocks;
+    a->max_parts = s.max_parts;
+    a->scale_log2 = scale * kLog2e;
+    a->out = nullptr;
+    a->ws_o = nullptr;
+    a->ws_ml = nullptr;
+    a->status = st;
+    return PKV_OK;
+}
+
+int set_workspace(DecodeArgs* a, const Shape& s, void* ws, size_t bytes) {
+    if (!ws || bytes < ws_bytes(s)) return PKV_ERR_WORKSPACE;
+    if (!aligned16(ws)) return PKV_ERR_MISALIGNED;
+    a->ws_o = static_cast<float*>(ws);
+    a->ws_ml = a->ws_o + static_cast<size_t>(s.batch) * s.hq * s.max_parts * s.D;
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
+                                          int32_t max_blocks, int32_t block_size,
+                                          int32_t partition_size, size_t* out) {
+    if (!out || batch < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks < 0 ||
+        block_size <= 0 || partition_size < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (partition_size == 0) partition_size = 512;
+    if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
+    const int64_t part_blocks = partition_size / block_size;
+    const int64_t parts = (max_blocks + part_blocks - 1) / part_blocks;
+    if (parts <= 1) {
+        *out = 0;
+        return PKV_OK;
+    }
+    *out = static_cast<size_t>(batch) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+    return PKV_OK;
+}
+
+extern "C" int pkv_paged_attention_decode_partials(
+    const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+    const int32_t* context_lens, int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+    int32_t head_dim, int32_t num_blocks, int32_t block_size, int32_t max_blocks, float scale,
+    void* workspace, size_t workspace_bytes, int32_t partition_size, int dtype, void* stream) {
+    pkv::Shape s;
+    int st = pkv::check_shape(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                              max_blocks, partition_size, dtype, &s);
+    if (st != PKV_OK) return st;
+    if (batch == 0 || max_blocks == 0) return PKV_OK;
+    pkv::DecodeArgs a;
+    if ((st = pkv::fill_args(&a, q, k_pool, v_pool, block_tables, context_lens, s, scale)) != PKV_OK)
+        return st;
+    if ((st = pkv::set_workspace(&a, s, workspace, workspace_bytes)) != PKV_OK) return st;
+    return pkv::run_partitions<true>(a, s, dtype, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
+                                                int32_t num_q_heads, int32_t head_dim,
+                                                int32_t max_blocks, int32_t block_size,
+                                                int32_t partition_size, const void* workspace,
+                                                size_t workspace_bytes, void* out, int dtype,
+                                                void* stream) {
+    // The merge never reads the pool, so only the partial-buffer shape matters.
+    if (batch < 0 || num_q_heads <= 0 || max_blocks < 0 || partition_size < 0 ||
+        (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16))
+        return PKV_ERR_INVALID_ARG;
+    if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) || batch > 65535 ||
+        num_q_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    const int32_t ps = partition_size == 0 ? 512 : partition_size;
+    if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
+    pkv::Shape s;
+    s.batch = batch;
+    s.hq = num_q_heads;
+    s.hkv = 1;
+    s.D = head_dim;
+    s.num_blocks = 1;
+    s.block_size = block_size;
+    s.max_blocks = max_blocks;
+    s.part_blocks = ps / block_size;
+    s.max_parts = (max_blocks + s.part_blocks - 1) / s.part_blocks;
+    if (s.max_parts < 1) s.max_parts = 1;
+    if (batch == 0) return PKV_OK;
+    if (!context_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(out)) return PKV_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < pkv::ws_bytes(s)) return PKV_ERR_WORKSPACE;
+    if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
+    const float* ws_o = static_cast<const float*>(workspace);
+    const float* ws_ml = ws_o + static_cast<size_t>(s.batch) * s.hq * s.max_parts * s.D;
+    return pkv::run_merge(context_lens, s, ws_o, ws_ml, out, dtype, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_pool,
+                                          const int32_t* block_tables, const int32_t* context_lens,
+                                          int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                          int32_t max_blocks, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t partition_size, int dtype, void* stream) {
+    pkv::Shape s;
+    int st = pkv::check_shape(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                              max_blocks, partition_size, dtype, &s);
+    if (st != PKV_OK) return st;
+    if (batch == 0) return PKV_OK;
+    if (!out) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(out)) return PKV_ERR_MISALIGNED;
+    pkv::DecodeArgs a;
+    if ((st = pkv::fill_args(&a, q, k_pool, v_pool, block_tables, context_lens, s, scale)) != PKV_OK)
+        return st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (s.max_parts <= 1) {
+        a.out = out;
+        a.part_blocks = s.max_blocks > 0 ? s.max_blocks : 1;
+        return pkv::run_partitions<false>(a, s, dtype, cs);
+    }
+    if ((st = pkv::set_workspace(&a, s, workspace, workspace_bytes)) != PKV_OK) return st;
+    if ((st = pkv::run_partitions<true>(a, s, dtype, cs)) != PKV_OK) return st;
+    return pkv::run_merge(context_lens, s, a.ws_o, a.ws_ml, out, dtype, cs);
+}

@@ -1,0 +1,574 @@
+// Paged decode attention over an INT4-asymmetric or FP8-E4M3 KV cache with
+// 16-bit attention sinks.
+//
+// What it computes: the decode attention of decode.cu with every cached
+// K/V value replaced by its dequantised value -- (q - z) * s for INT4, with
+// one fp16 (s, z) per (token, head) (group = head dim); e4m3(code) * s for
+// FP8, one fp16 s per (token, head) -- except the first n_sink positions of
+// each sequence, which read the 16-bit sink buffers ("The 8GB VRAM
+// Breakthrough", §4 "The Hybrid Solution: Sink-FP16 + Group-Wise Asymmetric
+// INT4 / FP8"; §5 "On-the-Fly Register Dequantization": packed codes and
+// (scale, zero) go straight to registers, no dequantised copy in memory).
+//
+// Design: the tensor-core layout of decode.cu (tokens as M for QK^T, head dim
+// as M for PV, the GQA group as N), with fragments built from the codes in
+// registers and the per-token scale / zero factored out of the products:
+//   QK^T: S_t = s_t * (sum_d q_d (c_td - 8) + (8 - z_t) * sum_d q_d)   INT4
+//         S_t = s_t * sum_d q_d e4m3(c_td)                             FP8
+//   PV:   O_d = sum_t W_t (c_td - 8) - sum_t W_t (z_t - 8),  W_t = P_t s_t
+// so the MMAs see exact small integers (INT4: c - 8 in [-8, 7]) or exact
+// e4m3 values, both exact in fp16, against fp16 queries / weights, with fp32
+// accumulation.
+//   INT4 nibble -> fp16: (nibble | 0x6400) is 1024 + nibble; subtracting 1032
+//   gives nibble - 8 exactly.  A 32-bit word of 8 nibbles yields four fp16
+//   pairs {d_j, d_j+4}; the k order of a k-step is permuted accordingly and
+//   the query fragment uses the same permutation.
+//   FP8 -> fp16: cvt.rn.f16x2.e4m3x2 (exact).
+//   For PV the pairs must hold two tokens of one column: a byte permute of
+//   the two token rows' words comes first.
+// Sink tokens (positions < n_sink <= 16, i.e. in logical block 0): their
+// logits are recomputed in fp32 from the 16-bit sink keys, their PV weights
+// are zero in the MMA, and P * sink_v is added to the accumulator directly.
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int BS = 16;
+constexpr int NW = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct QDecodeArgs {
+    const void* q;
+    const uint8_t* k_codes;
+    const __half* k_scale;
+    const __half* k_zero;
+    const uint8_t* v_codes;
+    const __half* v_scale;
+    const __half* v_zero;
+    const void* sink_k;
+    const void* sink_v;
+    int n_sink;
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    int hq, hkv, G, num_blocks, max_blocks, part_blocks, max_parts;
+    float scale_log2;
+    void* out;
+    float* ws_o;
+    float* ws_ml;
+    int* status;
+};
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    Half16<__half>::mma(d, a0, a1, a2, a3, b0, b1);
+}
+
+__device__ __forceinline__ uint32_t f16pair(float lo, float hi) { return Half16<__half>::pack(lo, hi); }
+
+// INT4 nibble pair at bit `shift` of both 16-bit halves -> fp16 {lo - 8, hi - 8}
+__device__ __forceinline__ uint32_t nib2(uint32_t w, int shift) {
+    const uint32_t x = ((w >> shift) & 0x000F000Fu) | 0x64006400u;
+    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2half2(__ushort_as_half(0x6408)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// two e4m3 codes in the low 16 bits of w -> fp16 pair (low byte -> low half)
+__device__ __forceinline__ uint32_t e4m3x2(uint32_t w) {
+    uint32_t d;
+    const unsigned short a = static_cast<unsigned short>(w & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(a));
+    return d;
+}
+
+template <typename T>
+__device__ __forceinline__ float tofloat(T x) {
+    return Half16<T>::to_float(x);
+}
+
+template <typename T, int D, int QMODE, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeArgs a) {
+    constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
+    constexpr int KSTEPS = D / 16;             // k-steps of QK^T
+    constexpr int MT = D / 16;                 // m-tiles of PV
+    constexpr int CB = INT4 ? D / 2 : D;       // code bytes per row
+    constexpr int KW = INT4 ? D / 32 : D / 16; // 32-bit K-code words per lane per row
+    constexpr int VW = INT4 ? D / 64 : D / 32; // 32-bit V-code words per lane per row
+    constexpr int DS = D / 8;                  // head-dim columns per lane group in PV
+
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+
+    int ctx = a.ctx_lens[b];
+    const int cap = a.max_blocks * BS;
+    if (ctx < 0 || ctx > cap) {
+        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int nblk = (ctx + BS - 1) / BS;
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    if (p >= (nparts > 0 ? nparts : 1)) return;
+    const int blk_begin = p * a.part_blocks;
+    const int blk_end = min(blk_begin + a.part_blocks, nblk);
+
+    // ---- query fragments (fp16) in the permuted k order of the code layout
+    uint32_t qf[KSTEPS][2];
+    float qsum = 0.f;  // sum over this lane's columns of query head g
+    {
+        const T* qrow = static_cast<const T*>(a.q) +
+                        (static_cast<int64_t>(b) * a.hq + kvh * a.G + (g < a.G ? g : 0)) * D;
+        const bool valid = g < a.G;
+        if constexpr (INT4) {
+            // lane c owns columns [c*D/4, (c+1)*D/4); word k covers 8 of them
+            const int base = c * (D / 4);
+#pragma unroll
+            for (int k = 0; k < KW; ++k) {
+                float x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] = valid ? tofloat(qrow[base + 8 * k + j]) : 0.f;
+                // fp16 rounding of the query, as fed to the MMA
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    x[j] = __half2float(__float2half_rn(x[j]));
+                    qsum += x[j];
+                }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    qf[2 * k + e][0] = f16pair(x[2 * e], x[2 * e + 4]);
+                    qf[2 * k + e][1] = f16pair(x[2 * e + 1], x[2 * e + 5]);
+                }
+            }
+        } else {
+            // load i covers columns [64i + 16c, +16), four k-steps
+#pragma unroll
+            for (int i = 0; i < D / 64; ++i) {
+                float x[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) x[j] = valid ? tofloat(qrow[64 * i + 16 * c + j]) : 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    qf[4 * i + e][0] = f16pair(x[4 * e], x[4 * e + 1]);
+                    qf[4 * i + e][1] = f16pair(x[4 * e + 2], x[4 * e + 3]);
+                }
+            }
+        }
+    }
+    // full per-head sums: reduce over the 4 lanes of head g, then fetch the
+    // sums of this lane's PV/S columns (heads 2c, 2c+1)
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    const float qsum0 = __shfl_sync(0xffffffffu, qsum, (2 * c) * 4);
+    const float qsum1 = __shfl_sync(0xffffffffu, qsum, (2 * c + 1) * 4);
+
+    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+    float corr0 = 0.f, corr1 = 0.f;  // INT4: sum_t W_t (z_t - 8) per head
+    float o[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    const int vr0 = 2 * c, vr1 = 2 * c + 1, vr2 = 8 + 2 * c, vr3 = 9 + 2 * c;
+
+    for (int lb = blk_begin + warp; lb < blk_end; lb += NW) {
+        const int phys = trow[lb];
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            continue;
+        }
+        const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;  // (block, head)
+        const uint8_t* kc = a.k_codes + bh * (BS * CB);
+        const uint8_t* vc = a.v_codes + bh * (BS * CB);
+
+        // ---- loads: K rows g, g+8; V rows 2c, 2c+1, 8+2c, 9+2c; scales
+        uint32_t kw0[KW], kw1[KW], vw[4][VW];
+        if constexpr (INT4) {
+            if constexpr (KW == 4) {
+                const uint4 r0 = ldg_stream(kc + g * CB + 16 * c);
+                const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 16 * c);
+                kw0[0] = r0.x; kw0[1] = r0.y; kw0[2] = r0.z; kw0[3] = r0.w;
+                kw1[0] = r1.x; kw1[1] = r1.y; kw1[2] = r1.z; kw1[3] = r1.w;
+            } else {
+                const uint2 r0 = ldg_stream8(kc + g * CB + 8 * c);
+                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 8 * c);
+                kw0[0] = r0.x; kw0[1] = r0.y;
+                kw1[0] = r1.x; kw1[1] = r1.y;
+            }
+            if constexpr (VW == 2) {
+                const int off = DS / 2 * g;  // bytes: DS columns = DS/2 bytes
+                const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
+                const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
+                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[1][0] = x1.x; vw[1][1] = x1.y;
+                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[3][0] = x3.x; vw[3][1] = x3.y;
+            } else {
+                const int off = DS / 2 * g;
+                vw[0][0] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
+                vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
+                vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
+                vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < D / 64; ++i) {
+                const uint4 r0 = ldg_stream(kc + g * CB + 64 * i + 16 * c);
+                const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 64 * i + 16 * c);
+                kw0[4 * i] = r0.x; kw0[4 * i + 1] = r0.y; kw0[4 * i + 2] = r0.z; kw0[4 * i + 3] = r0.w;
+                kw1[4 * i] = r1.x; kw1[4 * i + 1] = r1.y; kw1[4 * i + 2] = r1.z; kw1[4 * i + 3] = r1.w;
+            }
+            const int off = DS * g;  // bytes
+            if constexpr (VW == 4) {
+                const uint4 x0 = ldg_stream(vc + vr0 * CB + off), x1 = ldg_stream(vc + vr1 * CB + off);
+                const uint4 x2 = ldg_stream(vc + vr2 * CB + off), x3 = ldg_stream(vc + vr3 * CB + off);
+                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[0][2] = x0.z; vw[0][3] = x0.w;
+                vw[1][0] = x1.x; vw[1][1] = x1.y; vw[1][2] = x1.z; vw[1][3] = x1.w;
+                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[2][2] = x2.z; vw[2][3] = x2.w;
+                vw[3][0] = x3.x; vw[3][1] = x3.y; vw[3][2] = x3.z; vw[3][3] = x3.w;
+            } else {
+                const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
+                const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
+                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[1][0] = x1.x; vw[1][1] = x1.y;
+                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[3][0] = x3.x; vw[3][1] = x3.y;
+            }
+        }
+        const __half* ksc = a.k_scale + bh * BS;
+        const __half* vsc = a.v_scale + bh * BS;
+        const float ks0 = __half2float(ksc[g]), ks1 = __half2float(ksc[g + 8]);
+        const float vs0 = __half2float(vsc[g]), vs1 = __half2float(vsc[g + 8]);
+        float kz0 = 0.f, kz1 = 0.f, vz0 = 0.f, vz1 = 0.f;
+        if constexpr (INT4) {
+            kz0 = __half2float(a.k_zero[bh * BS + g]);
+            kz1 = __half2float(a.k_zero[bh * BS + g + 8]);
+            vz0 = __half2float(a.v_zero[bh * BS + g]);
+            vz1 = __half2float(a.v_zero[bh * BS + g + 8]);
+        }
+
+        // ---- S_raw^T = C Q^T over the code values
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (INT4) {
+#pragma unroll
+            for (int k = 0; k < KW; ++k) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    mma_f16(s, nib2(kw0[k], 8 * e), nib2(kw1[k], 8 * e), nib2(kw0[k], 8 * e + 4),
+                            nib2(kw1[k], 8 * e + 4), qf[2 * k + e][0], qf[2 * k + e][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < KSTEPS; ++j) {
+                // k-step j = 4i + e uses word 2e and 2e+1 of load i -> index 2j, 2j+1
+                mma_f16(s, e4m3x2(kw0[2 * j]) , e4m3x2(kw1[2 * j]), e4m3x2(kw0[2 * j] >> 16),
+                        e4m3x2(kw1[2 * j] >> 16), qf[j][0], qf[j][1]);
+            }
+        }
+        const int t0 = lb * BS;
+        const int tok0 = t0 + g;
+        const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
+        float x0, x1, x2, x3;
+        if constexpr (INT4) {
+            x0 = ks0 * (s[0] + (8.f - kz0) * qsum0) * a.scale_log2;
+            x1 = ks0 * (s[1] + (8.f - kz0) * qsum1) * a.scale_log2;
+            x2 = ks1 * (s[2] + (8.f - kz1) * qsum0) * a.scale_log2;
+            x3 = ks1 * (s[3] + (8.f - kz1) * qsum1) * a.scale_log2;
+        } else {
+            x0 = ks0 * s[0] * a.scale_log2;
+            x1 = ks0 * s[1] * a.scale_log2;
+            x2 = ks1 * s[2] * a.scale_log2;
+            x3 = ks1 * s[3] * a.scale_log2;
+        }
+        const bool sinks_here = lb == 0 && a.n_sink > 0;
+        bool sk0 = false, sk1 = false;
+        if (sinks_here) {
+            // exact 16-bit sink keys for positions < n_sink
+            sk0 = g < a.n_sink;
+            sk1 = g + 8 < a.n_sink;
+            const T* qbase = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * a.G) * D;
+            const T* skb = static_cast<const T*>(a.sink_k);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int t = g + 8 * r;
+                if (t < a.n_sink) {
+                    const T* krow = skb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D;
+                    float d0 = 0.f, d1 = 0.f;
+                    const int h0 = min(2 * c, a.G - 1), h1 = min(2 * c + 1, a.G - 1);
+                    for (int d = 0; d < D; ++d) {
+                        const float kv = tofloat(krow[d]);
+                        d0 += tofloat(qbase[h0 * D + d]) * kv;
+                        d1 += tofloat(qbase[h1 * D + d]) * kv;
+                    }
+                    if (r == 0) {
+                        x0 = d0 * a.scale_log2;
+                        x1 = d1 * a.scale_log2;
+                    } else {
+                        x2 = d0 * a.scale_log2;
+                        x3 = d1 * a.scale_log2;
+                    }
+                }
+            }
+        }
+        if (!ok0) x0 = x1 = neg_inf();
+        if (!ok1) x2 = x3 = neg_inf();
+
+        // ---- online softmax (base 2)
+        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+        const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+        const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+        l0 = l0 * al0 + (p0 + p2);
+        l1 = l1 * al1 + (p1 + p3);
+        m0 = mn0;
+        m1 = mn1;
+        corr0 *= al0;
+        corr1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+        // PV weights W = P * s (zero for masked and sink tokens)
+        const bool w0 = ok0 && !sk0, w1 = ok1 && !sk1;
+        const float W0 = w0 ? p0 * vs0 : 0.f, W1 = w0 ? p1 * vs0 : 0.f;
+        const float W2 = w1 ? p2 * vs1 : 0.f, W3 = w1 ? p3 * vs1 : 0.f;
+        const uint32_t pk0 = f16pair(W0, W1), pk1 = f16pair(W2, W3);
+        if constexpr (INT4) {
+            // the correction uses the fp16-rounded weights the MMA sees
+            const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
+            const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
+            if (w0) {
+                corr0 += __low2float(h0) * (vz0 - 8.f);
+                corr1 += __high2float(h0) * (vz0 - 8.f);
+            }
+            if (w1) {
+                corr0 += __low2float(h1) * (vz1 - 8.f);
+                corr1 += __high2float(h1) * (vz1 - 8.f);
+            }
+        }
+        const uint32_t pb0 = movmatrix_trans(pk0);
+        const uint32_t pb1 = movmatrix_trans(pk1);
+
+        if (t0 + BS > ctx) {  // partial last block: clear codes of missing tokens
+#pragma unroll
+            for (int j = 0; j < VW; ++j) {
+                if (t0 + vr0 >= ctx) vw[0][j] = 0;
+                if (t0 + vr1 >= ctx) vw[1][j] = 0;
+                if (t0 + vr2 >= ctx) vw[2][j] = 0;
+                if (t0 + vr3 >= ctx) vw[3][j] = 0;
+            }
+        }
+
+        // ---- O^T += C_v^T W^T; lane columns d = g*DS + e, e_lo = mt, e_hi = mt + MT
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t av[4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int e = mt + hf * MT;
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {  // token pair (2c, 2c+1) / (8+2c, 9+2c)
+                    const uint32_t* A = vw[2 * pr];
+                    const uint32_t* B = vw[2 * pr + 1];
+                    uint32_t v;
+                    if constexpr (INT4) {
+                        const int word = e >> 3, sub = (e >> 2) & 1, nib = e & 3;
+                        const uint32_t X = __byte_perm(A[word], B[word], sub ? 0x7632u : 0x5410u);
+                        v = nib2(X, 4 * nib);
+                    } else {
+                        const int word = e >> 2, sub = e & 3;
+                        const uint32_t X = __byte_perm(A[word], B[word], (sub >> 1) ? 0x7362u : 0x5140u);
+                        v = e4m3x2((sub & 1) ? (X >> 16) : X);
+                    }
+                    av[hf + 2 * pr] = v;
+                }
+            }
+            mma_f16(o[mt], av[0], av[1], av[2], av[3], pb0, pb1);
+        }
+
+        if (sinks_here) {
+            // add P_t * sink_v[t] for the sink positions, in fp32
+            const T* svb = static_cast<const T*>(a.sink_v);
+            for (int t = 0; t < a.n_sink && t < ctx; ++t) {
+                const int src = (t & 7) * 4 + c;
+                const float pa = __shfl_sync(0xffffffffu, t < 8 ? p0 : p2, src);
+                const float pb = __shfl_sync(0xffffffffu, t < 8 ? p1 : p3, src);
+                const T* vrow = svb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D + g * DS;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const float vl = tofloat(vrow[mt]), vh = tofloat(vrow[mt + MT]);
+                    o[mt][0] += pa * vl;
+                    o[mt][1] += pb * vl;
+                    o[mt][2] += pa * vh;
+                    o[mt][3] += pb * vh;
+                }
+            }
+        }
+    }
+
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        corr0 += __shfl_xor_sync(0xffffffffu, corr0, off);
+        corr1 += __shfl_xor_sync(0xffffffffu, corr1, off);
+    }
+
+    __shared__ float sm_ml[NW][8][2];
+    __shared__ float sm_o[NW][8][D];
+    if (g == 0) {
+        sm_ml[warp][2 * c][0] = m0;
+        sm_ml[warp][2 * c][1] = l0;
+        sm_ml[warp][2 * c + 1][0] = m1;
+        sm_ml[warp][2 * c + 1][1] = l1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int dl = g * DS + mt, dh = g * DS + mt + MT;
+        sm_o[warp][2 * c][dl] = o[mt][0] - corr0;
+        sm_o[warp][2 * c + 1][dl] = o[mt][1] - corr1;
+        sm_o[warp][2 * c][dh] = o[mt][2] - corr0;
+        sm_o[warp][2 * c + 1][dh] = o[mt][3] - corr1;
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < a.G * D; idx += NW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_ml[w][h][0]);
+        float acc = 0.f, L = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float sc = ex2(sm_ml[w][h][0] - M);
+                acc += sc * sm_o[w][h][d];
+                L += sc * sm_ml[w][h][1];
+            }
+        }
+        const int64_t qh = static_cast<int64_t>(b) * a.hq + kvh * a.G + h;
+        if constexpr (SPLIT) {
+            const int64_t row = qh * a.max_parts + p;
+            a.ws_o[row * D + d] = acc;
+            if (d == 0) {
+                a.ws_ml[2 * row] = M;
+                a.ws_ml[2 * row + 1] = L;
+            }
+        } else {
+            static_cast<T*>(a.out)[qh * D + d] = Half16<T>::from_float(L > 0.f ? acc / L : 0.f);
+        }
+    }
+}
+
+template <typename T, int D, int QMODE, bool SPLIT>
+void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
+    dim3 grid(SPLIT ? parts : 1, hkv, batch);
+    paged_decode_quant_kernel<T, D, QMODE, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+}
+
+template <bool SPLIT>
+int run(const QDecodeArgs& a, int D, int qmode, int dtype, int parts, int hkv, int batch,
+        cudaStream_t st) {
+#define PKV_QLAUNCH(TT, DD, QM) launch<TT, DD, QM, SPLIT>(a, parts, hkv, batch, st)
+    if (dtype == PKV_DTYPE_BF16) {
+        if (qmode == PKV_QMODE_INT4_ASYM) {
+            if (D == 128) PKV_QLAUNCH(__nv_bfloat16, 128, PKV_QMODE_INT4_ASYM);
+            else PKV_QLAUNCH(__nv_bfloat16, 64, PKV_QMODE_INT4_ASYM);
+        } else {
+            if (D == 128) PKV_QLAUNCH(__nv_bfloat16, 128, PKV_QMODE_FP8_E4M3);
+            else PKV_QLAUNCH(__nv_bfloat16, 64, PKV_QMODE_FP8_E4M3);
+        }
+    } else {
+        if (qmode == PKV_QMODE_INT4_ASYM) {
+            if (D == 128) PKV_QLAUNCH(__half, 128, PKV_QMODE_INT4_ASYM);
+            else PKV_QLAUNCH(__half, 64, PKV_QMODE_INT4_ASYM);
+        } else {
+            if (D == 128) PKV_QLAUNCH(__half, 128, PKV_QMODE_FP8_E4M3);
+            else PKV_QLAUNCH(__half, 64, PKV_QMODE_FP8_E4M3);
+        }
+    }
+#undef PKV_QLAUNCH
+    return launch_status();
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_attention_decode_quant(
+    const void* q, const void* k_codes, const void* k_scale, const void* k_zero, const void* v_codes,
+    const void* v_scale, const void* v_zero, const void* sink_k, const void* sink_v, int32_t n_sink,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+    int32_t max_blocks, int32_t group_size, float scale, void* out, void* workspace,
+    size_t workspace_bytes, int32_t partition_size, int qmode, int dtype, void* stream) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || max_blocks < 0 || partition_size < 0 || n_sink < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_INVALID_ARG;
+    if (qmode != PKV_QMODE_INT4_ASYM && qmode != PKV_QMODE_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) ||
+        num_q_heads / num_kv_heads > 8 || n_sink > pkv::BS || batch > 65535 || num_kv_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    if (qmode == PKV_QMODE_INT4_ASYM && group_size != head_dim) return PKV_ERR_UNSUPPORTED;
+    const int32_t ps = partition_size == 0 ? 512 : partition_size;
+    if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_codes || !k_scale || !v_codes || !v_scale || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (qmode == PKV_QMODE_INT4_ASYM && (!k_zero || !v_zero)) return PKV_ERR_INVALID_ARG;
+    if (n_sink > 0 && (!sink_k || !sink_v)) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_codes) || !pkv::aligned16(v_codes) ||
+        !pkv::aligned16(out) || (reinterpret_cast<uintptr_t>(k_scale) & 1u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 1u))
+        return PKV_ERR_MISALIGNED;
+    int* st = pkv::status_word();
+    if (!st) return PKV_ERR_CUDA;
+    pkv::QDecodeArgs a;
+    a.q = q;
+    a.k_codes = static_cast<const uint8_t*>(k_codes);
+    a.k_scale = static_cast<const __half*>(k_scale);
+    a.k_zero = static_cast<const __half*>(k_zero);
+    a.v_codes = static_cast<const uint8_t*>(v_codes);
+    a.v_scale = static_cast<const __half*>(v_scale);
+    a.v_zero = static_cast<const __half*>(v_zero);
+    a.sink_k = sink_k;
+    a.sink_v = sink_v;
+    a.n_sink = n_sink;
+    a.tables = block_tables;
+    a.ctx_lens = context_lens;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.G = num_q_heads / num_kv_heads;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.part_blocks = ps / block_size;
+    a.max_parts = (max_blocks + a.part_blocks - 1) / a.part_blocks;
+    if (a.max_parts < 1) a.max_parts = 1;
+    a.scale_log2 = scale * pkv::kLog2e;
+    a.out = out;
+    a.ws_o = nullptr;
+    a.ws_ml = nullptr;
+    a.status = st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (a.max_parts <= 1) {
+        a.part_blocks = max_blocks > 0 ? max_blocks : 1;
+        return pkv::run<false>(a, head_dim, qmode, dtype, 1, num_kv_heads, batch, cs);
+    }
+    const size_t need = static_cast<size_t>(batch) * num_q_heads * a.max_parts * (head_dim + 2) * sizeof(float);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
+    a.ws_o = static_cast<float*>(workspace);
+    a.ws_ml = a.ws_o + static_cast<size_t>(batch) * num_q_heads * a.max_parts * head_dim;
+    int r = pkv::run<true>(a, head_dim, qmode, dtype, a.max_parts, num_kv_heads, batch, cs);
+    if (r != PKV_OK) return r;
+    return pkv_paged_attention_decode_merge(context_lens, batch, num_q_heads, head_dim, max_blocks,
+                                            block_size, partition_size, workspace, workspace_bytes,
+                                            out, dtype, stream);
+}

@@ -39,7 +39,7 @@ import torch
 
 __all__ = [
     "WORKLOADS", "workload", "context_lengths", "free_order", "query",
-    "sequence_kv", "new_token_kv", "prefill_schedule", "tails",
+    "sequence_kv", "prompt_kv", "new_token_kv", "prefill_schedule", "tails",
     "kv_rows_to_numpy",
 ]
 

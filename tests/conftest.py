@@ -29,8 +29,8 @@ def read_golden(name):
 @pytest.fixture(scope="session")
 def pkv():
     """The C-ABI library, built in-tree if missing or stale."""
-    from paged_kv_cache_13_gb300 import build as _build
-    _build.build_library()
+    import __graft_entry__
+    __graft_entry__.build()
     import paged_kv_cache_13_gb300 as p
     return p
 

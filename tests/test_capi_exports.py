@@ -1,0 +1,74 @@
+"""The C-ABI library loads on a host without a GPU and exports every entry
+point the header declares; host-side argument checks reject bad calls
+before any device work."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(pkv_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_pool_create", "pkv_seq_append", "pkv_seq_fork", "pkv_kv_append",
+                     "pkv_paged_attention_decode", "pkv_kv_append_quant",
+                     "pkv_paged_attention_decode_quant", "pkv_copy_blocks", "pkv_device_status"):
+        assert required in names
+    assert len(names) >= 30
+
+
+def test_every_declared_symbol_is_exported(pkv):
+    missing = [n for n in declared_functions() if not hasattr(pkv.lib, n)]
+    assert missing == []
+
+
+def test_every_declared_symbol_has_a_binding(pkv):
+    for n in declared_functions():
+        assert hasattr(pkv, n) or n == "pkv_status_string" or n in ("pkv_pool_block_size",), n
+
+
+def test_status_strings(pkv):
+    for code in range(-10, 1):
+        s = pkv.lib.pkv_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert pkv.lib.pkv_status_string(0) == b"ok"
+    assert pkv.pkv_version() >= 1
+
+
+def test_host_validation_rejects_before_launch(pkv):
+    L = pkv.lib
+    # Hq not a multiple of Hkv
+    st = L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 6, 4, 128, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None)
+    assert st == -1
+    # unsupported head dim and block size
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 96, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -8
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 32, 4, 1.0, 16, None, 0, 0, 1, None) == -8
+    # GQA group above 8
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 32, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -8
+    # misaligned query pointer
+    assert L.pkv_paged_attention_decode(18, 16, 16, 16, 16, 1, 8, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -10
+    # partition not a multiple of the block size
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 100, 1, None) == -1
+    # bad dtype
+    assert L.pkv_kv_append(16, 16, 16, 1, 16, 16, 4, 2, 128, 16, 7, None) == -1
+    # empty work is a no-op even without a device
+    assert L.pkv_kv_append(16, 16, 16, 0, 16, 16, 4, 2, 128, 16, 1, None) == 0
+    # copy_blocks pool count limits
+    assert L.pkv_copy_blocks(None, None, 0, None, 1, 4, None) == -1
+
+
+def test_workspace_bytes(pkv):
+    # 64 sequences, 32 heads, dim 128, 256 blocks of 16, 512-token partitions
+    assert pkv.pkv_decode_workspace_bytes(64, 32, 128, 256, 16, 512) == 64 * 32 * 8 * 130 * 4
+    # one partition covers everything: single pass, no workspace
+    assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 512) == 0
+    assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == 4 * 32 * 128 * 130 * 4

@@ -1,0 +1,150 @@
+"""GPU quantised KV path: INT4 / FP8 codes bit-exact with the oracle's
+binary32 quantiser, and decode attention over the quantised cache (sinks in
+16-bit) within the acceptance bound of the oracle's attention over the
+dequantised cache."""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from cache_builder import assert_close, build, expected, logical_rows
+from oracle import kvcache as okv
+
+pytestmark = pytest.mark.gpu
+
+
+def _rand16(rng, shape, dtype, outliers=0.0):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if outliers:
+        hit = rng.random(shape) < outliers
+        x = np.where(hit, np.where(rng.random(shape) < 0.5, -8.0, 8.0), x).astype(np.float32)
+    return torch.from_numpy(x).to(dtype)
+
+
+def _empty_cache(qmode, NB, Hkv, D, g, dev, B=1, n_sink=4, dtype=torch.bfloat16):
+    cb = D // 2 if qmode == "int4" else D
+    ng = D // g if qmode == "int4" else 1
+    c = {
+        "k_codes": torch.zeros((NB, Hkv, 16, cb), dtype=torch.uint8, device=dev),
+        "v_codes": torch.zeros((NB, Hkv, 16, cb), dtype=torch.uint8, device=dev),
+        "k_scale": torch.zeros((NB, Hkv, 16, ng), dtype=torch.float16, device=dev),
+        "v_scale": torch.zeros((NB, Hkv, 16, ng), dtype=torch.float16, device=dev),
+        "sink_k": torch.zeros((B, max(n_sink, 1), Hkv, D), dtype=dtype, device=dev),
+        "sink_v": torch.zeros((B, max(n_sink, 1), Hkv, D), dtype=dtype, device=dev),
+    }
+    if qmode == "int4":
+        c["k_zero"] = torch.zeros((NB, Hkv, 16, ng), dtype=torch.float16, device=dev)
+        c["v_zero"] = torch.zeros((NB, Hkv, 16, ng), dtype=torch.float16, device=dev)
+    return c
+
+
+@pytest.mark.parametrize("qmode,D,g,dtype", [
+    ("int4", 128, 128, torch.bfloat16), ("int4", 128, 64, torch.bfloat16), ("int4", 128, 32, torch.float16),
+    ("int4", 64, 64, torch.float16), ("fp8", 128, 128, torch.bfloat16), ("fp8", 64, 64, torch.float16),
+    ("int4", 256, 256, torch.bfloat16), ("fp8", 256, 256, torch.bfloat16)])
+def test_append_quant_codes_bit_exact(pkv, cuda_dev, qmode, D, g, dtype):
+    rng = np.random.default_rng(D + g)
+    NB, Hkv, T, n_sink = 24, 4, 200, 4
+    k = _rand16(rng, (T, Hkv, D), dtype, 0.01)
+    v = _rand16(rng, (T, Hkv, D), dtype, 0.01) * 3
+    # a few degenerate rows: constant, zero, huge spread
+    k[0] = 1.5
+    k[1] = 0.0
+    k[2, :, 0] = 3e4 if dtype == torch.float16 else 3e30
+    slots = rng.choice(NB * 16, size=T, replace=False).astype(np.int64)
+    slots[-3:] = -1
+    positions = np.arange(T, dtype=np.int32)
+    seq_idx = np.zeros(T, dtype=np.int32)
+    cache = _empty_cache(qmode, NB, Hkv, D, g, cuda_dev, 1, n_sink, dtype)
+    pkv.pkv_kv_append_quant(k.to(cuda_dev), v.to(cuda_dev), torch.from_numpy(slots).to(cuda_dev),
+                            torch.from_numpy(positions).to(cuda_dev), torch.from_numpy(seq_idx).to(cuda_dev),
+                            cache, n_sink, qmode, g)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    got = {n: t.cpu().numpy() for n, t in cache.items()}
+    for name, x in (("k", k), ("v", v)):
+        _, codes, s, z = okv.quantize_sequence(x.float().numpy(), qmode, g)
+        for t in range(T):
+            if slots[t] < 0:
+                continue
+            blk, off = divmod(int(slots[t]), 16)
+            assert np.array_equal(got[name + "_codes"][blk, :, off], codes[t]), (name, t)
+            assert got[name + "_scale"][blk, :, off].tobytes() == s[t].tobytes(), (name, t)
+            if qmode == "int4":
+                assert got[name + "_zero"][blk, :, off].tobytes() == z[t].tobytes(), (name, t)
+    assert torch.equal(cache["sink_k"][0, :n_sink].cpu(), k[:n_sink])
+    assert torch.equal(cache["sink_v"][0, :n_sink].cpu(), v[:n_sink])
+
+
+def _decode_quant(pkv, c, partition_size=0):
+    w = c.w
+    B = len(c.decoded)
+    out = torch.empty((B, w["hq"], w["d"]), dtype=w["torch_dtype"], device=c.q.device)
+    n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, partition_size)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=c.q.device)
+    pkv.pkv_paged_attention_decode_quant(c.q, c.cache, c.n_sink, c.tables, c.lens, w["scale"], out,
+                                         c.quant, c.group_size, ws, partition_size)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    return out.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+@pytest.mark.parametrize("ps", [0, 64, 4096])
+def test_quant_decode_small(pkv, cuda_dev, qmode, ps):
+    w = syn.workload("quant", batch=5, ctx=1000, num_blocks=1024)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    want = expected(c)
+    got = _decode_quant(pkv, c, ps)
+    assert_close(got, want, what="%s ps %d" % (qmode, ps))
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+@pytest.mark.parametrize("ctx", [1, 3, 4, 5, 15, 16, 17, 33])
+def test_quant_decode_short_contexts_and_sinks(pkv, cuda_dev, qmode, ctx):
+    w = syn.workload("quant", batch=3, ctx=ctx, num_blocks=64)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    want = expected(c)
+    for ps in (0, 16):
+        got = _decode_quant(pkv, c, ps)
+        assert_close(got, want, what="%s ctx %d" % (qmode, ctx))
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_quant_decode_fp16_head64(pkv, cuda_dev, qmode):
+    w = syn.workload("quant", batch=4, ctx=300, num_blocks=256, hq=8, hkv=2, d=64, dtype="fp16",
+                     group_size=64)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    assert_close(_decode_quant(pkv, c, 64), expected(c), what=qmode)
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_quant_workload_full_size_sampled(pkv, cuda_dev, qmode):
+    """32 sequences x 16,384 tokens, 4 sinks, 1% outliers at +-8: codes of
+    sampled sequences bit-exact, their outputs within the bound."""
+    w = syn.workload("quant")
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    got = _decode_quant(pkv, c, 0)
+    sample = [0, 13, 31]
+    want = expected(c, sample)
+    assert_close(got[sample], want, what="quant %s" % qmode)
+    # codes of a sampled sequence at its slots
+    k, v = logical_rows(c, 13)
+    table = c.tables_host[13]
+    _, kc, ks, kz = okv.quantize_sequence(k, qmode, c.group_size)
+    gk = c.cache["k_codes"].cpu().numpy()
+    gs = c.cache["k_scale"].cpu().numpy()
+    for t in range(0, k.shape[0], 997):
+        blk, off = table[t // 16], t % 16
+        assert np.array_equal(gk[blk, :, off], kc[t])
+        assert gs[blk, :, off].tobytes() == ks[t].tobytes()
+    assert np.isfinite(got).all()
+
+
+def test_quant_prefix_cow_int4(pkv, cuda_dev):
+    """Copy-on-write of a quantised block copies codes, scales and zeros."""
+    w = syn.workload("prefix_cow_2008", n_sink=4, group_size=128)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    assert len(c.all_pairs) == 8
+    assert_close(_decode_quant(pkv, c, 0), expected(c), what="prefix int4")
