@@ -50,6 +50,28 @@ def parse_args():
 
 
 # ----------------------------------------------------------------- helpers
+def shard(n, world, rank):
+    """Contiguous share [lo, hi) of n independent units for one rank."""
+    base, extra = divmod(n, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def max_over_ranks(x, dist, device):
+    """The largest of every rank's x (the job ends with its slowest rank)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds):
+    """Units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world / seconds
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -248,10 +270,7 @@ def run_device(args, rank, world, dist):
     elapsed_ms = t0.elapsed_time(t1)
     kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     assert pkv.pkv_device_status() == 0
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
     ms_per_step = elapsed_ms / args.steps
 
     # ---------- end to end through the public API, host buffers
@@ -320,11 +339,7 @@ def run_e2e(pkv, torch, layer, steps, dist, device):
                                        d_out, ws, layer.partition_size, stream)
         h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
-    elapsed = time.perf_counter() - t_start
-    if dist is not None:
-        t = torch.tensor([elapsed], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(time.perf_counter() - t_start, dist, device)
     assert torch.isfinite(h_out.float()).all()
     return dict(gbs=total_kv / elapsed / 1e9, h2d=h2d, d2h=d2h, steps=steps)
 
@@ -418,8 +433,7 @@ def main():
         dist.destroy_process_group()
     if rank != 0:
         return
-    total_bytes = res["kv_bytes"] * world
-    value = total_bytes / (res["ms_per_step"] * 1e-3) / 1e9
+    value = whole_job_rate(res["kv_bytes"], world, res["ms_per_step"] * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
     achieved = res["kv_bytes"] / (res["kern_ms"] * 1e-3) / 1e9
     cpu = None

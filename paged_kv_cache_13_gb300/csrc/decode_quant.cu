@@ -257,9 +257,10 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
         } else {
 #pragma unroll
             for (int j = 0; j < KSTEPS; ++j) {
-                // k-step j = 4i + e uses word 2e and 2e+1 of load i -> index 2j, 2j+1
-                mma_f16(s, e4m3x2(kw0[2 * j]) , e4m3x2(kw1[2 * j]), e4m3x2(kw0[2 * j] >> 16),
-                        e4m3x2(kw1[2 * j] >> 16), qf[j][0], qf[j][1]);
+                // k-step j = 4i + e uses word e of load i (= word j): codes
+                // {0, 1} are the low k pair, codes {2, 3} the high k pair
+                mma_f16(s, e4m3x2(kw0[j]), e4m3x2(kw1[j]), e4m3x2(kw0[j] >> 16),
+                        e4m3x2(kw1[j] >> 16), qf[j][0], qf[j][1]);
             }
         }
         const int t0 = lb * BS;

@@ -62,7 +62,7 @@ def test_append_quant_codes_bit_exact(pkv, cuda_dev, qmode, D, g, dtype):
                             cache, n_sink, qmode, g)
     torch.cuda.synchronize()
     assert pkv.pkv_device_status() == 0
-    got = {n: t.cpu().numpy() for n, t in cache.items()}
+    got = {n: t.cpu().numpy() for n, t in cache.items() if not n.startswith("sink")}
     for name, x in (("k", k), ("v", v)):
         _, codes, s, z = okv.quantize_sequence(x.float().numpy(), qmode, g)
         for t in range(T):
