@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--partition-size", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-blocks", type=int, default=0,
+                    help="override the pool size (blocks); 0 keeps the workload's 40,000")
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -167,10 +169,10 @@ class ClockSampler:
 class Layer:
     """The workload's cache, built with the library's own entry points."""
 
-    def __init__(self, pkv, torch, device, partition_size, headroom_tokens):
+    def __init__(self, pkv, torch, device, partition_size, headroom_tokens, pool_blocks=0):
         import synthetic as syn
         self.pkv, self.torch, self.dev = pkv, torch, device
-        w = syn.workload(WORKLOAD)
+        w = syn.workload(WORKLOAD, **({"num_blocks": pool_blocks} if pool_blocks else {}))
         self.w = w
         NB, BS, Hkv, D, Hq = w["num_blocks"], w["block_size"], w["hkv"], w["d"], w["hq"]
         dt = w["torch_dtype"]
@@ -237,7 +239,8 @@ def run_device(args, rank, world, dist):
     torch.cuda.set_device(dev_index)
     device = torch.device("cuda", dev_index)
     e2e_steps = max(1, min(args.steps, 200))
-    layer = Layer(pkv, torch, device, args.partition_size, headroom_tokens=e2e_steps + args.warmup + 8)
+    layer = Layer(pkv, torch, device, args.partition_size, headroom_tokens=e2e_steps + args.warmup + 8,
+                  pool_blocks=args.pool_blocks)
     stream = torch.cuda.current_stream()
     kv_bytes = layer.kv_bytes()
 
