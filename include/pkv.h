@@ -231,6 +231,36 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
                                      const void* workspace, size_t workspace_bytes, void* out,
                                      int dtype, void* stream);
 
+/* Allocation-free decode.  The source pages have no counterpart for this
+ * entry point: it exists for callers that cannot provide a device workspace
+ * -- code running while a stream is captured into a CUDA graph (allocation
+ * is not a capturable operation), plugins inside a host runtime that owns all
+ * device memory and offers no allocator, and serving loops with a fixed,
+ * pre-planned memory budget that must not call cudaMalloc / cudaFree (which
+ * may synchronise the device) on the decode path.
+ * Same arguments and result as pkv_paged_attention_decode, minus the
+ * workspace: the split-K partials live in a fixed array inside the library
+ * (PKV_STATIC_WORKSPACE_BYTES per GPU, held by every GPU that loads the
+ * library until the process exits).  The call allocates nothing.
+ *   - A shape whose pkv_decode_workspace_bytes exceeds
+ *     PKV_STATIC_WORKSPACE_BYTES is rejected with PKV_ERR_WORKSPACE before
+ *     any device work.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array and it keeps whatever the
+ *     last call left in it; nothing in it needs to start at zero.  Calls whose
+ *     kernels overlap on the GPU (different streams, no ordering) race on the
+ *     array and give undefined results: order them on one stream or with
+ *     events. */
+#define PKV_STATIC_WORKSPACE_BYTES (16u << 20)
+int pkv_paged_attention_decode_static_ws(const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                         int32_t max_blocks, float scale, void* out,
+                                         int32_t partition_size, int dtype, void* stream);
+
 /* Quantised KV-append ("The 8GB VRAM Breakthrough", §4; §5 flowchart: fused
  * quantiser on the write path).  For every token t with slot >= 0 and every
  * KV head, K and V rows are quantised and written at the slot:

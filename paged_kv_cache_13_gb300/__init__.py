@@ -75,6 +75,9 @@ _SIGS = {
          _int, _vp], _int),
     "pkv_paged_attention_decode_merge": (
         [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _int, _vp], _int),
+    "pkv_paged_attention_decode_static_ws": (
+        [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _i32, _int,
+         _vp], _int),
     "pkv_kv_append_quant": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
          _i32, _i32, _i32, _i32, _int, _int, _vp], _int),
@@ -315,6 +318,22 @@ def pkv_paged_attention_decode_merge(context_lens, max_blocks, workspace, out, b
         _ptr(context_lens), B, Hq, D, max_blocks, block_size, partition_size, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(out), _dtype_code(out), _stream(stream)),
         "pkv_paged_attention_decode_merge")
+
+
+PKV_STATIC_WORKSPACE_BYTES = 16 << 20
+
+
+def pkv_paged_attention_decode_static_ws(q, k_pool, v_pool, block_tables, context_lens, scale, out,
+                                         partition_size=0, stream=None):
+    """Decode without a caller workspace: the split-K partials go to a fixed
+    array inside the library (PKV_STATIC_WORKSPACE_BYTES per GPU).  For
+    callers that cannot allocate device memory on the decode path."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    _check(lib.pkv_paged_attention_decode_static_ws(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D,
+        NB, BS, block_tables.shape[1], float(scale), _ptr(out), partition_size, _dtype_code(q),
+        _stream(stream)), "pkv_paged_attention_decode_static_ws")
 
 
 def pkv_kv_append_quant(k, v, slot_mapping, positions, seq_idx, cache, n_sink, qmode,
