@@ -217,18 +217,12 @@ class Layer:
     def kv_bytes(self, ctx=None):
         return int(np.sum(self.ctx_host if ctx is None else ctx)) * KV_BYTES_PER_TOKEN
 
-    # one step, device-resident inputs
-    def append(self):
-        self.pkv.pkv_kv_append(self.new_k, self.new_v, self.slots, self.k_pool, self.v_pool)
-
-    def partials(self):
-        self.pkv.pkv_paged_attention_decode_partials(
-            self.q, self.k_pool, self.v_pool, self.tables, self.lens, self.w["scale"], self.ws,
-            partition_size=self.partition_size)
-
-    def merge(self):
-        self.pkv.pkv_paged_attention_decode_merge(self.lens, self.max_blocks, self.ws, self.out,
-                                                  partition_size=self.partition_size)
+    # one step, device-resident inputs: one kernel appends the new rows and
+    # attends (split-K partials merged by the last CTA of each sequence/head)
+    def step(self):
+        self.pkv.pkv_paged_attention_decode_append(
+            self.q, self.new_k, self.new_v, self.slots, self.k_pool, self.v_pool, self.tables,
+            self.lens, self.w["scale"], self.out, self.ws, self.partition_size)
 
 
 def run_device(args, rank, world, dist):
@@ -246,9 +240,7 @@ def run_device(args, rank, world, dist):
 
     # ---------- device-resident timed region
     for _ in range(args.warmup):
-        layer.append()
-        layer.partials()
-        layer.merge()
+        layer.step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -260,11 +252,9 @@ def run_device(args, rank, world, dist):
     clocks.start()
     t0.record(stream)
     for i in range(args.steps):
-        layer.append()
         ev[i][0].record(stream)
-        layer.partials()
+        layer.step()
         ev[i][1].record(stream)
-        layer.merge()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -280,7 +270,7 @@ def run_device(args, rank, world, dist):
     e2e = run_e2e(pkv, torch, layer, e2e_steps, dist, device)
 
     return dict(ms_per_step=ms_per_step, kern_ms=kern_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
-                B=layer.B, launches=3 * args.steps)
+                B=layer.B, launches=2 * args.steps)  # partials + merge per step
 
 
 def run_e2e(pkv, torch, layer, steps, dist, device):
@@ -337,9 +327,9 @@ def run_e2e(pkv, torch, layer, steps, dist, device):
         d_slots.copy_(h_slots, non_blocking=True)
         d_tab.copy_(h_tab, non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
-        pkv.pkv_kv_append(d_k, d_v, d_slots, layer.k_pool, layer.v_pool, stream)
-        pkv.pkv_paged_attention_decode(d_q, layer.k_pool, layer.v_pool, d_tab, d_lens, w["scale"],
-                                       d_out, ws, layer.partition_size, stream)
+        pkv.pkv_paged_attention_decode_append(d_q, d_k, d_v, d_slots, layer.k_pool, layer.v_pool,
+                                              d_tab, d_lens, w["scale"], d_out, ws,
+                                              layer.partition_size, stream)
         h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
     elapsed = max_over_ranks(time.perf_counter() - t_start, dist, device)
@@ -406,7 +396,7 @@ def config_block(B, kv_bytes, partition_size):
         "workload": "%s: one Llama-3-8B-shaped layer, %d sequences, context uniform in [512, 4096] "
                     "(seeded), 32 q / 8 KV heads, head dim 128, bf16, 16-token blocks, 40,000-block "
                     "pool in seeded random order; step = KV-append of 1 token per sequence + paged "
-                    "decode attention (split-K, %d-token partitions)" % (WORKLOAD, B, partition_size),
+                    "decode attention (split-K partials with the append fused, then a merge launched with programmatic dependent launch; %d-token partitions)" % (WORKLOAD, B, partition_size),
         "batch": B,
         "kv_bytes_per_step": kv_bytes,
         "partition_size": partition_size,
@@ -461,7 +451,7 @@ def main():
         "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_kernel<bf16, 128, split>",
+            "kernel": "paged_decode_kernel<bf16, 128, split-K partials, fused append> + merge_kernel (programmatic dependent launch)",
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)" if peak_kind == "measured" else peak_kind,

@@ -203,8 +203,10 @@ int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int
  * processed by independent CTAs; when more than one partition can occur
  * (max_blocks * block_size > partition_size) partial (max, sum, output)
  * triples go to `workspace` (device, >= pkv_decode_workspace_bytes) and a
- * second kernel merges them with a log-sum-exp rescale (flash-decoding
- * split-K); otherwise the first kernel writes out directly.
+ * second kernel, launched behind the first with programmatic dependent
+ * launch, merges them with a log-sum-exp rescale (flash-decoding split-K);
+ * otherwise one pass writes out directly.  Calls that share a workspace must
+ * not overlap on the GPU.
  * Supported: block_size 16, head_dim 64 or 128, 1 <= num_q_heads /
  * num_kv_heads <= 8 (else UNSUPPORTED). */
 int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_pool,
@@ -214,6 +216,27 @@ int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_
                                int32_t max_blocks, float scale, void* out, void* workspace,
                                size_t workspace_bytes, int32_t partition_size, int dtype,
                                void* stream);
+
+/* One decode step in one kernel: for every sequence b with
+ * slot_mapping[b] >= 0, writes k_new[b] / v_new[b] ([batch, num_kv_heads,
+ * head_dim], 16-bit) into the pools at slot_mapping[b] and attends exactly
+ * as pkv_paged_attention_decode, the new row being the last token
+ * (position context_lens[b] - 1).  The slot must be that position's slot,
+ * block_tables[b][(ctx-1)/block_size] * block_size + (ctx-1) % block_size
+ * (what pkv_seq_append returned for the decode step); otherwise
+ * PKV_STATUS_BAD_SLOT is set and the row is neither written nor used.
+ * The new row is taken from k_new / v_new, never read back from the pool, so
+ * no ordering against a separate append kernel is needed.  The pools are
+ * written (not const).  Same workspace, shapes and errors as
+ * pkv_paged_attention_decode. */
+int pkv_paged_attention_decode_append(const void* q, const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, void* k_pool, void* v_pool,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                      int32_t max_blocks, float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t partition_size, int dtype,
+                                      void* stream);
 
 /* The two phases of pkv_paged_attention_decode, for callers that time or
  * overlap them.  _partials always writes the workspace (never out);

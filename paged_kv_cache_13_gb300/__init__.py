@@ -70,6 +70,9 @@ _SIGS = {
     "pkv_paged_attention_decode": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
          _i32, _int, _vp], _int),
+    "pkv_paged_attention_decode_append": (
+        [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32,
+         _vp, _vp, _sz, _i32, _int, _vp], _int),
     "pkv_paged_attention_decode_partials": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _sz, _i32,
          _int, _vp], _int),
@@ -298,6 +301,21 @@ def pkv_paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, sc
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D,
         NB, BS, mb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, partition_size,
         _dtype_code(q), _stream(stream)), "pkv_paged_attention_decode")
+
+
+def pkv_paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,
+                                      context_lens, scale, out, workspace=None, partition_size=0,
+                                      stream=None):
+    """Fused decode step: write k_new/v_new [B, Hkv, D] at slot_mapping [B]
+    and attend over context_lens tokens (the new row being the last)."""
+    B, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_pool), _ptr(v_pool),
+        _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D, NB, BS, block_tables.shape[1],
+        float(scale), _ptr(out), _ptr(workspace), ws_bytes, partition_size, _dtype_code(q),
+        _stream(stream)), "pkv_paged_attention_decode_append")
 
 
 def pkv_paged_attention_decode_partials(q, k_pool, v_pool, block_tables, context_lens, scale,

@@ -5,16 +5,23 @@
 // with K_t, V_t gathered through the block table ("The 8GB VRAM
 // Breakthrough", §3 "How Logical-to-Physical Block Tables Work": the kernel
 // reads the table on the fly and gathers the non-contiguous physical blocks
-// for QK^T and the softmax-weighted sum of V).
+// for QK^T and the softmax-weighted sum of V).  Optionally the same kernel
+// first writes the decode step's new K/V row into its slot (the KV-append of
+// §1, "write one new KV vector back"), taking that row from the inputs
+// instead of reading it back.
 //
 // Design (sm_103a):
 // * Work unit = (sequence, KV head, partition of `part_blocks` blocks).  One
 //   CTA of NW warps per unit; the warps take the partition's blocks
 //   round-robin, each keeping its own online-softmax state (running max m,
 //   sum l, accumulator o) for the G query heads of the KV head; the CTA merges
-//   the warps through shared memory at the end.  With more than one partition
-//   per sequence the CTA writes an fp32 (m, l, o) partial and a second kernel
-//   merges the partials with a log-sum-exp rescale (flash-decoding split-K).
+//   its warps through shared memory at the end.  With several partitions per
+//   sequence (flash-decoding split-K) each CTA writes an fp32 (m, l, o)
+//   partial and a merge kernel, launched behind it with programmatic
+//   dependent launch, combines the partials with a log-sum-exp rescale.
+// * Each warp loads the physical ids of all its blocks with one coalesced
+//   load (lane k holds the id of the warp's k-th block), so a block's K/V
+//   loads never wait behind a table load.
 // * A block of one KV head is 16 tokens x D contiguous 16-bit values (4 KiB
 //   for D = 128).  Each lane issues 16-byte loads straight from global memory
 //   into registers, shaped so that the registers ARE the tensor-core fragments
@@ -38,21 +45,26 @@
 // * Tokens at or past ctx in the last block get logit -inf, and their V rows
 //   are zeroed in registers (an unwritten slot may hold NaN bit patterns).
 
-#include <cfloat>
-
 #include "common.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int BS = 16;  // tokens per block (the kernels are specialised to 16)
-constexpr int NW = 4;   // warps per CTA
+constexpr int kNW = 4;  // warps per CTA (4 beat 8 in a sweep on the 64-sequence layer)
 constexpr float kLog2e = 1.4426950408889634f;
+
+enum Mode { kSingle = 0, kPartials = 1 };
 
 struct DecodeArgs {
     const void* q;
     const void* k_pool;
     const void* v_pool;
+    void* k_pool_w;        // writable views of the pools (fused append)
+    void* v_pool_w;
+    const void* k_new;     // [B, Hkv, D] new rows (fused append)
+    const void* v_new;
+    const int64_t* slots;  // [B] slot of each new row (fused append)
     const int32_t* tables;
     const int32_t* ctx_lens;
     int hq, hkv, G, num_blocks, max_blocks, part_blocks, max_parts;
@@ -65,16 +77,194 @@ struct DecodeArgs {
 
 // Element e (0 .. D/8-1) of lane group g in the PV fragment layout sits at
 // head-dim column 64 * (e / 8) + 8 * g + e % 8.
-template <int D>
-__device__ __forceinline__ int pv_col(int e, int g) {
-    return 64 * (e >> 3) + 8 * g + (e & 7);
+__device__ __forceinline__ int pv_col(int e, int g) { return 64 * (e >> 3) + 8 * g + (e & 7); }
+
+// Log-sum-exp merge of `np` partition partials (m_q, l_q, o_q[d]) of one
+// (sequence, query head, column d): the loads of 8 partitions are issued
+// together, then folded into a running (M, L, acc) with one rescale per
+// chunk.  Partials are read from L2 (.cg): they may have been written by
+// other CTAs of the same launch.
+__device__ __forceinline__ float merge_partials(const float* __restrict__ ml,
+                                                const float* __restrict__ ov, int64_t stride_o,
+                                                int np) {
+    float M = neg_inf(), L = 0.f, acc = 0.f;
+    for (int q0 = 0; q0 < np; q0 += 8) {
+        float mq[8], lq[8], oq[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const bool v = q0 + j < np;
+            mq[j] = v ? __ldcg(ml + 2 * (q0 + j)) : neg_inf();
+            lq[j] = v ? __ldcg(ml + 2 * (q0 + j) + 1) : 0.f;
+            oq[j] = v ? __ldcg(ov + (q0 + j) * stride_o) : 0.f;
+        }
+        float mx = M;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx = fmaxf(mx, mq[j]);
+        if (mx == neg_inf()) continue;  // every partition so far was empty
+        const float sc = ex2(M - mx);   // 0 when M is still -inf
+        acc *= sc;
+        L *= sc;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float w = ex2(mq[j] - mx);
+            acc += w * oq[j];
+            L += w * lq[j];
+        }
+        M = mx;
+    }
+    return L > 0.f ? acc / L : 0.f;
 }
 
-template <typename T, int D, bool SPLIT>
-__global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) {
+// Online-softmax state of one warp for the query heads 2c, 2c+1 of its lanes.
+template <int MT>
+struct WarpState {
+    float m0, m1, l0, l1;
+    float o[MT][4];
+};
+
+// Attend one 16-token block (physical id `phys`, logical index lb) into the
+// warp state.  INJECT: row app_off of the block is the decode step's new row;
+// it is taken from the inputs (and stored to the pool) instead of the loads.
+template <typename T, int D, bool INJECT>
+__device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh, int lb, int phys,
+                                             int ctx, int app_off, const uint4 (&qf)[D / 32],
+                                             WarpState<D / 16>& w, int g, int c) {
+    using H = Half16<T>;
+    constexpr int KC = D / 32;
+    constexpr int VC = D / 64;
+    constexpr int MT = D / 16;
+    const int vrow0 = 2 * c, vrow1 = 2 * c + 1, vrow2 = 8 + 2 * c, vrow3 = 9 + 2 * c;
+    const int64_t base = (static_cast<int64_t>(phys) * a.hkv + kvh) * (BS * D);
+    const T* kb = static_cast<const T*>(a.k_pool) + base;
+    const T* vb = static_cast<const T*>(a.v_pool) + base;
+    // Row sources: the pool, except that with INJECT the lanes holding row
+    // app_off read the decode step's new row from the inputs instead.
+    const T* kr0p = kb + g * D;
+    const T* kr1p = kb + (g + 8) * D;
+    const T* vp0 = vb + vrow0 * D;
+    const T* vp1 = vb + vrow1 * D;
+    const T* vp2 = vb + vrow2 * D;
+    const T* vp3 = vb + vrow3 * D;
+    if constexpr (INJECT) {
+        const int64_t nrow = (static_cast<int64_t>(b) * a.hkv + kvh) * D;
+        const T* kn = static_cast<const T*>(a.k_new) + nrow;
+        const T* vn = static_cast<const T*>(a.v_new) + nrow;
+        if (g == app_off) kr0p = kn;
+        if (g + 8 == app_off) kr1p = kn;
+        if (vrow0 == app_off) vp0 = vn;
+        if (vrow1 == app_off) vp1 = vn;
+        if (vrow2 == app_off) vp2 = vn;
+        if (vrow3 == app_off) vp3 = vn;
+    }
+
+    uint4 kr0[KC], kr1[KC], vr[4][VC];
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+        kr0[i] = ldg_stream(kr0p + 32 * i + 8 * c);
+        kr1[i] = ldg_stream(kr1p + 32 * i + 8 * c);
+    }
+#pragma unroll
+    for (int j = 0; j < VC; ++j) {
+        vr[0][j] = ldg_stream(vp0 + 64 * j + 8 * g);
+        vr[1][j] = ldg_stream(vp1 + 64 * j + 8 * g);
+        vr[2][j] = ldg_stream(vp2 + 64 * j + 8 * g);
+        vr[3][j] = ldg_stream(vp3 + 64 * j + 8 * g);
+    }
+
+    if constexpr (INJECT) {
+        // Store the new row to the pool from the lanes that hold its pieces
+        // (each 16-byte piece exactly once).
+        T* kw = static_cast<T*>(a.k_pool_w) + base + app_off * D;
+        T* vw = static_cast<T*>(a.v_pool_w) + base + app_off * D;
+#pragma unroll
+        for (int i = 0; i < KC; ++i) {
+            if (g == app_off) *reinterpret_cast<uint4*>(kw + 32 * i + 8 * c) = kr0[i];
+            if (g + 8 == app_off) *reinterpret_cast<uint4*>(kw + 32 * i + 8 * c) = kr1[i];
+        }
+#pragma unroll
+        for (int j = 0; j < VC; ++j) {
+            if (vrow0 == app_off) *reinterpret_cast<uint4*>(vw + 64 * j + 8 * g) = vr[0][j];
+            if (vrow1 == app_off) *reinterpret_cast<uint4*>(vw + 64 * j + 8 * g) = vr[1][j];
+            if (vrow2 == app_off) *reinterpret_cast<uint4*>(vw + 64 * j + 8 * g) = vr[2][j];
+            if (vrow3 == app_off) *reinterpret_cast<uint4*>(vw + 64 * j + 8 * g) = vr[3][j];
+        }
+    }
+
+    // ---- S^T = K Q^T: s[0]=S(t=g,h=2c) s[1]=S(g,2c+1) s[2]=S(g+8,2c) s[3]=S(g+8,2c+1)
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            H::mma(s, word(kr0[i], 2 * e), word(kr1[i], 2 * e), word(kr0[i], 2 * e + 1),
+                   word(kr1[i], 2 * e + 1), word(qf[i], 2 * e), word(qf[i], 2 * e + 1));
+        }
+    }
+    const int tok0 = lb * BS + g;
+    const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
+    const float x0 = ok0 ? s[0] * a.scale_log2 : neg_inf();
+    const float x1 = ok0 ? s[1] * a.scale_log2 : neg_inf();
+    const float x2 = ok1 ? s[2] * a.scale_log2 : neg_inf();
+    const float x3 = ok1 ? s[3] * a.scale_log2 : neg_inf();
+
+    // ---- online softmax (base 2); heads 2c (x0, x2) and 2c+1 (x1, x3)
+    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+    }
+    const float mn0 = fmaxf(w.m0, bm0), mn1 = fmaxf(w.m1, bm1);
+    const float al0 = ex2(w.m0 - mn0), al1 = ex2(w.m1 - mn1);
+    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
+    const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
+    w.l0 = w.l0 * al0 + (p0 + p2);
+    w.l1 = w.l1 * al1 + (p1 + p3);
+    w.m0 = mn0;
+    w.m1 = mn1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        w.o[mt][0] *= al0;
+        w.o[mt][1] *= al1;
+        w.o[mt][2] *= al0;
+        w.o[mt][3] *= al1;
+    }
+    // P^T B-fragments: transpose the two 8x8 (token x head) halves.
+    const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
+    const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+
+    if (lb * BS + BS > ctx) {  // last, partial block: zero masked V rows
+        const int t0 = lb * BS;
+#pragma unroll
+        for (int j = 0; j < VC; ++j) {
+            if (t0 + vrow0 >= ctx) vr[0][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + vrow1 >= ctx) vr[1][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + vrow2 >= ctx) vr[2][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + vrow3 >= ctx) vr[3][j] = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // ---- O^T += V^T P^T
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        constexpr int HALF = D / 16;
+        const int elo = mt, ehi = mt + HALF;
+        const int jl = elo >> 3, wl = (elo & 7) >> 1, hl = elo & 1;
+        const int jh = ehi >> 3, wh = (ehi & 7) >> 1, hh = ehi & 1;
+        const uint32_t sl = hl ? 0x7632u : 0x5410u;
+        const uint32_t sh = hh ? 0x7632u : 0x5410u;
+        const uint32_t a0 = __byte_perm(word(vr[0][jl], wl), word(vr[1][jl], wl), sl);
+        const uint32_t a1 = __byte_perm(word(vr[0][jh], wh), word(vr[1][jh], wh), sh);
+        const uint32_t a2 = __byte_perm(word(vr[2][jl], wl), word(vr[3][jl], wl), sl);
+        const uint32_t a3 = __byte_perm(word(vr[2][jh], wh), word(vr[3][jh], wh), sh);
+        H::mma(w.o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+}
+
+template <typename T, int D, int NW, int MODE, bool APPEND>
+__global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeArgs a) {
     using H = Half16<T>;
     constexpr int KC = D / 32;  // 16-byte K pieces per lane per row
-    constexpr int VC = D / 64;  // 16-byte V pieces per lane per row
     constexpr int MT = D / 16;  // PV m-tiles
 
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -88,10 +278,35 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) 
         ctx = ctx < 0 ? 0 : cap;
     }
     const int nblk = (ctx + BS - 1) / BS;
-    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
-    if (p >= (nparts > 0 ? nparts : 1)) return;
-    const int blk_begin = p * a.part_blocks;
-    const int blk_end = min(blk_begin + a.part_blocks, nblk);
+    const int nparts = MODE == kSingle ? 1 : max((nblk + a.part_blocks - 1) / a.part_blocks, 1);
+    if constexpr (MODE == kPartials) {
+        // let the merge grid (launched with programmatic serialization) be
+        // scheduled while this grid drains; it waits for our completion
+        asm volatile("griddepcontrol.launch_dependents;");
+    }
+    if (p >= nparts) return;
+    const int blk_begin = MODE == kSingle ? 0 : p * a.part_blocks;
+    const int blk_end = MODE == kSingle ? nblk : min(blk_begin + a.part_blocks, nblk);
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+
+    // fused append: the new row belongs at logical position ctx - 1
+    int app_lb = -1, app_off = 0;
+    if constexpr (APPEND) {
+        const int64_t slot = ctx > 0 ? a.slots[b] : -1;
+        if (slot >= 0) {
+            const int lb_last = (ctx - 1) / BS, off = (ctx - 1) % BS;
+            if (lb_last >= blk_begin && lb_last < blk_end) {
+                const int phys = trow[lb_last];
+                if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks) &&
+                    slot == static_cast<int64_t>(phys) * BS + off) {
+                    app_lb = lb_last;
+                    app_off = off;
+                } else if (threadIdx.x == 0) {
+                    atomicOr(a.status, PKV_STATUS_BAD_SLOT);
+                }
+            }
+        }
+    }
 
     // Q^T B-fragments: lane (g, c) holds query head g's columns [32i + 8c, +8).
     uint4 qf[KC];
@@ -104,110 +319,35 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) 
         for (int i = 0; i < KC; ++i) qf[i] = make_uint4(0, 0, 0, 0);
     }
 
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
-    float o[MT][4];
+    WarpState<MT> ws;
+    ws.m0 = ws.m1 = neg_inf();
+    ws.l0 = ws.l1 = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int mt = 0; mt < MT; ++mt) ws.o[mt][0] = ws.o[mt][1] = ws.o[mt][2] = ws.o[mt][3] = 0.f;
 
-    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
-    const T* kpool = static_cast<const T*>(a.k_pool);
-    const T* vpool = static_cast<const T*>(a.v_pool);
-    const int vrow0 = 2 * c, vrow1 = 2 * c + 1, vrow2 = 8 + 2 * c, vrow3 = 9 + 2 * c;
-
-    for (int lb = blk_begin + warp; lb < blk_end; lb += NW) {
-        const int phys = trow[lb];
+    // The appended block, if any, is the last block of this partition and so
+    // the last one its warp visits: the loop stops there and the block is
+    // attended after the loop with the injection.
+    int tab = 0, k = 0, lb = blk_begin + warp;
+    for (; lb < blk_end && lb != app_lb; ++k, lb += NW) {
+        if ((k & 31) == 0) {  // physical ids of this warp's next 32 blocks
+            const int idx = lb + NW * lane;
+            tab = idx < blk_end ? trow[idx] : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, tab, k & 31);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
             if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
             continue;
         }
-        const int64_t base = (static_cast<int64_t>(phys) * a.hkv + kvh) * (BS * D);
-        const T* kb = kpool + base;
-        const T* vb = vpool + base;
-
-        uint4 kr0[KC], kr1[KC], vr[4][VC];
-#pragma unroll
-        for (int i = 0; i < KC; ++i) {
-            kr0[i] = ldg_stream(kb + g * D + 32 * i + 8 * c);
-            kr1[i] = ldg_stream(kb + (g + 8) * D + 32 * i + 8 * c);
-        }
-#pragma unroll
-        for (int j = 0; j < VC; ++j) {
-            vr[0][j] = ldg_stream(vb + vrow0 * D + 64 * j + 8 * g);
-            vr[1][j] = ldg_stream(vb + vrow1 * D + 64 * j + 8 * g);
-            vr[2][j] = ldg_stream(vb + vrow2 * D + 64 * j + 8 * g);
-            vr[3][j] = ldg_stream(vb + vrow3 * D + 64 * j + 8 * g);
-        }
-
-        // ---- S^T = K Q^T: s[0]=S(t=g,h=2c) s[1]=S(g,2c+1) s[2]=S(g+8,2c) s[3]=S(g+8,2c+1)
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < KC; ++i) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                H::mma(s, word(kr0[i], 2 * e), word(kr1[i], 2 * e), word(kr0[i], 2 * e + 1),
-                       word(kr1[i], 2 * e + 1), word(qf[i], 2 * e), word(qf[i], 2 * e + 1));
-            }
-        }
-        const int tok0 = lb * BS + g;
-        const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
-        const float x0 = ok0 ? s[0] * a.scale_log2 : neg_inf();
-        const float x1 = ok0 ? s[1] * a.scale_log2 : neg_inf();
-        const float x2 = ok1 ? s[2] * a.scale_log2 : neg_inf();
-        const float x3 = ok1 ? s[3] * a.scale_log2 : neg_inf();
-
-        // ---- online softmax (base 2); heads 2c (x0, x2) and 2c+1 (x1, x3)
-        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        }
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-        const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-        const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-        }
-        // P^T B-fragments: transpose the two 8x8 (token x head) halves.
-        const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
-
-        if (lb * BS + BS > ctx) {  // last, partial block: zero masked V rows
-            const int t0 = lb * BS;
-#pragma unroll
-            for (int j = 0; j < VC; ++j) {
-                if (t0 + vrow0 >= ctx) vr[0][j] = make_uint4(0, 0, 0, 0);
-                if (t0 + vrow1 >= ctx) vr[1][j] = make_uint4(0, 0, 0, 0);
-                if (t0 + vrow2 >= ctx) vr[2][j] = make_uint4(0, 0, 0, 0);
-                if (t0 + vrow3 >= ctx) vr[3][j] = make_uint4(0, 0, 0, 0);
-            }
-        }
-
-        // ---- O^T += V^T P^T
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            constexpr int HALF = D / 16;
-            const int elo = mt, ehi = mt + HALF;
-            const int jl = elo >> 3, wl = (elo & 7) >> 1, hl = elo & 1;
-            const int jh = ehi >> 3, wh = (ehi & 7) >> 1, hh = ehi & 1;
-            const uint32_t sl = hl ? 0x7632u : 0x5410u;
-            const uint32_t sh = hh ? 0x7632u : 0x5410u;
-            const uint32_t a0 = __byte_perm(word(vr[0][jl], wl), word(vr[1][jl], wl), sl);
-            const uint32_t a1 = __byte_perm(word(vr[0][jh], wh), word(vr[1][jh], wh), sh);
-            const uint32_t a2 = __byte_perm(word(vr[2][jl], wl), word(vr[3][jl], wl), sl);
-            const uint32_t a3 = __byte_perm(word(vr[2][jh], wh), word(vr[3][jh], wh), sh);
-            H::mma(o[mt], a0, a1, a2, a3, pb0, pb1);
+        attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qf, ws, g, c);
+    }
+    if constexpr (APPEND) {
+        if (lb == app_lb) {  // app_lb was validated above
+            attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qf, ws, g, c);
         }
     }
+    float m0 = ws.m0, m1 = ws.m1, l0 = ws.l0, l1 = ws.l1;
+    auto& o = ws.o;
 
     // finish the per-lane partial sums over the 8 token lanes
 #pragma unroll
@@ -227,7 +367,7 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) 
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        const int dl = pv_col<D>(mt, g), dh = pv_col<D>(mt + D / 16, g);
+        const int dl = pv_col(mt, g), dh = pv_col(mt + D / 16, g);
         sm_o[warp][2 * c][dl] = o[mt][0];
         sm_o[warp][2 * c + 1][dl] = o[mt][1];
         sm_o[warp][2 * c][dh] = o[mt][2];
@@ -250,21 +390,23 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_kernel(DecodeArgs a) 
             }
         }
         const int64_t qh = static_cast<int64_t>(b) * a.hq + kvh * a.G + h;
-        if constexpr (SPLIT) {
+        if constexpr (MODE == kSingle) {
+            static_cast<T*>(a.out)[qh * D + d] = H::from_float(L > 0.f ? acc / L : 0.f);
+        } else {
             const int64_t row = qh * a.max_parts + p;
             a.ws_o[row * D + d] = acc;
             if (d == 0) {
                 a.ws_ml[2 * row] = M;
                 a.ws_ml[2 * row + 1] = L;
             }
-        } else {
-            static_cast<T*>(a.out)[qh * D + d] = H::from_float(L > 0.f ? acc / L : 0.f);
         }
     }
+
 }
 
 // Merge the partition partials of one (sequence, query head): one thread per
-// head-dim column.
+// head-dim column.  Launched right behind the partition kernel with
+// programmatic dependent launch (see run_merge).
 template <typename T, int D>
 __global__ void __launch_bounds__(D) merge_kernel(const int32_t* __restrict__ ctx_lens, int hq,
                                                  int max_blocks, int part_blocks, int max_parts,
@@ -277,17 +419,11 @@ __global__ void __launch_bounds__(D) merge_kernel(const int32_t* __restrict__ ct
     const int nblk = (ctx + BS - 1) / BS;
     const int np = (nblk + part_blocks - 1) / part_blocks;
     const int64_t row0 = (static_cast<int64_t>(b) * hq + h) * max_parts;
-    float M = neg_inf();
-    for (int p = 0; p < np; ++p) M = fmaxf(M, ws_ml[2 * (row0 + p)]);
-    float acc = 0.f, L = 0.f;
-    if (M != neg_inf()) {
-        for (int p = 0; p < np; ++p) {
-            const float sc = ex2(ws_ml[2 * (row0 + p)] - M);
-            acc += sc * ws_o[(row0 + p) * D + d];
-            L += sc * ws_ml[2 * (row0 + p) + 1];
-        }
-    }
-    out[(static_cast<int64_t>(b) * hq + h) * D + d] = Half16<T>::from_float(L > 0.f ? acc / L : 0.f);
+    // partials are produced by the preceding grid: wait for it (a no-op
+    // when this grid was launched without programmatic serialization)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    out[(static_cast<int64_t>(b) * hq + h) * D + d] =
+        Half16<T>::from_float(merge_partials(ws_ml + 2 * row0, ws_o + row0 * D + d, D, np));
 }
 
 struct Shape {
@@ -319,43 +455,59 @@ int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_b
     return PKV_OK;
 }
 
-size_t ws_bytes(const Shape& s) {
+size_t partial_bytes(const Shape& s) {
     return static_cast<size_t>(s.batch) * s.hq * s.max_parts * (s.D + 2) * sizeof(float);
 }
 
-template <typename T, int D, bool SPLIT>
-void launch_partitions(const DecodeArgs& a, const Shape& s, cudaStream_t st) {
-    dim3 grid(SPLIT ? s.max_parts : 1, s.hkv, s.batch);
-    paged_decode_kernel<T, D, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+template <typename T, int D, int MODE, bool APPEND>
+int launch_kernel(const DecodeArgs& a, const Shape& s, cudaStream_t st) {
+    dim3 grid(MODE == kSingle ? 1 : s.max_parts, s.hkv, s.batch);
+    paged_decode_kernel<T, D, kNW, MODE, APPEND><<<grid, kNW * 32, 0, st>>>(a);
+    return launch_status();
 }
 
-template <bool SPLIT>
-int run_partitions(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
+template <int MODE, bool APPEND>
+int dispatch(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
     if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128) launch_partitions<__nv_bfloat16, 128, SPLIT>(a, s, st);
-        else launch_partitions<__nv_bfloat16, 64, SPLIT>(a, s, st);
-    } else {
-        if (s.D == 128) launch_partitions<__half, 128, SPLIT>(a, s, st);
-        else launch_partitions<__half, 64, SPLIT>(a, s, st);
+        if (s.D == 128) return launch_kernel<__nv_bfloat16, 128, MODE, APPEND>(a, s, st);
+        return launch_kernel<__nv_bfloat16, 64, MODE, APPEND>(a, s, st);
     }
-    return launch_status();
+    if (s.D == 128) return launch_kernel<__half, 128, MODE, APPEND>(a, s, st);
+    return launch_kernel<__half, 64, MODE, APPEND>(a, s, st);
+}
+
+// The merge grid is launched with programmatic stream serialization: it may
+// be scheduled as soon as every CTA of the preceding grid has started, and
+// its griddepcontrol.wait holds each CTA until that grid has completed and
+// its writes are visible.  This hides the second launch behind the first
+// grid's last wave.
+template <typename T, int D>
+int launch_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, const float* ws_ml,
+                 void* out, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s.hq, s.batch);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D>, ctx_lens, s.hq, s.max_blocks,
+                                             s.part_blocks, s.max_parts, ws_o, ws_ml,
+                                             static_cast<T*>(out));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 int run_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, const float* ws_ml,
               void* out, int dtype, cudaStream_t st) {
-    dim3 grid(s.hq, s.batch);
     if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128)
-            merge_kernel<__nv_bfloat16, 128><<<grid, 128, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__nv_bfloat16*>(out));
-        else
-            merge_kernel<__nv_bfloat16, 64><<<grid, 64, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__nv_bfloat16*>(out));
-    } else {
-        if (s.D == 128)
-            merge_kernel<__half, 128><<<grid, 128, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__half*>(out));
-        else
-            merge_kernel<__half, 64><<<grid, 64, 0, st>>>(ctx_lens, s.hq, s.max_blocks, s.part_blocks, s.max_parts, ws_o, ws_ml, static_cast<__half*>(out));
+        if (s.D == 128) return launch_merge<__nv_bfloat16, 128>(ctx_lens, s, ws_o, ws_ml, out, st);
+        return launch_merge<__nv_bfloat16, 64>(ctx_lens, s, ws_o, ws_ml, out, st);
     }
-    return launch_status();
+    if (s.D == 128) return launch_merge<__half, 128>(ctx_lens, s, ws_o, ws_ml, out, st);
+    return launch_merge<__half, 64>(ctx_lens, s, ws_o, ws_ml, out, st);
 }
 
 int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_pool,
@@ -366,6 +518,7 @@ int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_po
         return PKV_ERR_MISALIGNED;
     int* st = status_word();
     if (!st) return PKV_ERR_CUDA;
+    *a = DecodeArgs{};
     a->q = q;
     a->k_pool = k_pool;
     a->v_pool = v_pool;
@@ -379,19 +532,33 @@ int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_po
     a->part_blocks = s.part_blocks;
     a->max_parts = s.max_parts;
     a->scale_log2 = scale * kLog2e;
-    a->out = nullptr;
-    a->ws_o = nullptr;
-    a->ws_ml = nullptr;
     a->status = st;
     return PKV_OK;
 }
 
 int set_workspace(DecodeArgs* a, const Shape& s, void* ws, size_t bytes) {
-    if (!ws || bytes < ws_bytes(s)) return PKV_ERR_WORKSPACE;
+    if (!ws || bytes < partial_bytes(s)) return PKV_ERR_WORKSPACE;
     if (!aligned16(ws)) return PKV_ERR_MISALIGNED;
     a->ws_o = static_cast<float*>(ws);
     a->ws_ml = a->ws_o + static_cast<size_t>(s.batch) * s.hq * s.max_parts * s.D;
     return PKV_OK;
+}
+
+// One decode call: single pass when one partition covers every table,
+// otherwise the partition kernel then the merge kernel.
+template <bool APPEND>
+int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_bytes, int dtype,
+           cudaStream_t cs) {
+    DecodeArgs a = a0;
+    a.out = out;
+    if (s.max_parts <= 1) {
+        a.part_blocks = s.max_blocks > 0 ? s.max_blocks : 1;
+        return dispatch<kSingle, APPEND>(a, s, dtype, cs);
+    }
+    int st = set_workspace(&a, s, ws, ws_bytes);
+    if (st != PKV_OK) return st;
+    if ((st = dispatch<kPartials, APPEND>(a, s, dtype, cs)) != PKV_OK) return st;
+    return run_merge(a.ctx_lens, s, a.ws_o, a.ws_ml, out, dtype, cs);
 }
 
 }  // namespace
@@ -429,7 +596,8 @@ extern "C" int pkv_paged_attention_decode_partials(
     if ((st = pkv::fill_args(&a, q, k_pool, v_pool, block_tables, context_lens, s, scale)) != PKV_OK)
         return st;
     if ((st = pkv::set_workspace(&a, s, workspace, workspace_bytes)) != PKV_OK) return st;
-    return pkv::run_partitions<true>(a, s, dtype, static_cast<cudaStream_t>(stream));
+    pkv::dispatch<pkv::kPartials, false>(a, s, dtype, static_cast<cudaStream_t>(stream));
+    return pkv::launch_status();
 }
 
 extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
@@ -461,7 +629,7 @@ extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int
     if (batch == 0) return PKV_OK;
     if (!context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!pkv::aligned16(out)) return PKV_ERR_MISALIGNED;
-    if (!workspace || workspace_bytes < pkv::ws_bytes(s)) return PKV_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < pkv::partial_bytes(s)) return PKV_ERR_WORKSPACE;
     if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
     const float* ws_o = static_cast<const float*>(workspace);
     const float* ws_ml = ws_o + static_cast<size_t>(s.batch) * s.hq * s.max_parts * s.D;
@@ -485,13 +653,33 @@ extern "C" int pkv_paged_attention_decode(const void* q, const void* k_pool, con
     pkv::DecodeArgs a;
     if ((st = pkv::fill_args(&a, q, k_pool, v_pool, block_tables, context_lens, s, scale)) != PKV_OK)
         return st;
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (s.max_parts <= 1) {
-        a.out = out;
-        a.part_blocks = s.max_blocks > 0 ? s.max_blocks : 1;
-        return pkv::run_partitions<false>(a, s, dtype, cs);
-    }
-    if ((st = pkv::set_workspace(&a, s, workspace, workspace_bytes)) != PKV_OK) return st;
-    if ((st = pkv::run_partitions<true>(a, s, dtype, cs)) != PKV_OK) return st;
-    return pkv::run_merge(context_lens, s, a.ws_o, a.ws_ml, out, dtype, cs);
+    return pkv::decode<false>(a, s, out, workspace, workspace_bytes, dtype,
+                              static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_decode_append(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_pool, void* v_pool, const int32_t* block_tables, const int32_t* context_lens,
+    int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t num_blocks, int32_t block_size, int32_t max_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int32_t partition_size, int dtype, void* stream) {
+    pkv::Shape s;
+    int st = pkv::check_shape(batch, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                              max_blocks, partition_size, dtype, &s);
+    if (st != PKV_OK) return st;
+    if (batch == 0) return PKV_OK;
+    if (!out || !k_new || !v_new || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(out) || !pkv::aligned16(k_new) || !pkv::aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PKV_ERR_MISALIGNED;
+    pkv::DecodeArgs a;
+    if ((st = pkv::fill_args(&a, q, k_pool, v_pool, block_tables, context_lens, s, scale)) != PKV_OK)
+        return st;
+    a.k_pool_w = k_pool;
+    a.v_pool_w = v_pool;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slots = slot_mapping;
+    return pkv::decode<true>(a, s, out, workspace, workspace_bytes, dtype,
+                             static_cast<cudaStream_t>(stream));
 }

@@ -34,7 +34,7 @@ def _rows_source(w):
     return rows
 
 
-def build(pkv, w, device, quant=None, empty_fill=None):
+def build(pkv, w, device, quant=None, empty_fill=None, step_append=True):
     """Prefill the workload and run its decode-step append.
 
     quant: None for a 16-bit cache, "int4" / "fp8" for a quantised cache.
@@ -139,10 +139,21 @@ def build(pkv, w, device, quant=None, empty_fill=None):
         pkv.pkv_copy_blocks(c.pools, torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
     c.step_pairs = [tuple(int(x) for x in p) for p in pairs]
     c.all_pairs += c.step_pairs
-    for i, h in enumerate(decoded):
-        do_append(h, 1, slots[i:i + 1], [])
     c.step_slots = slots.copy()
-    flush()
+    if step_append:
+        for i, h in enumerate(decoded):
+            do_append(h, 1, slots[i:i + 1], [])
+        flush()
+    else:
+        # leave the step's rows unwritten: a fused append+decode writes them
+        nk, nv = [], []
+        for h in decoded:
+            k, v = rows(h, lens.get(h, 0), 1)
+            nk.append(k[0])
+            nv.append(v[0])
+            lens[h] = lens.get(h, 0) + 1
+        c.new_k = torch.stack(nk).to(device)
+        c.new_v = torch.stack(nv).to(device)
     c.max_blocks = max(pkv.pkv_seq_num_blocks(pool, h) for h in decoded)
     tables, ctx = pkv.pkv_build_block_tables(pool, decoded, c.max_blocks)
     c.tables_host, c.lens_host = tables, ctx

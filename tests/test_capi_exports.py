@@ -68,7 +68,9 @@ def test_host_validation_rejects_before_launch(pkv):
 
 def test_workspace_bytes(pkv):
     # 64 sequences, 32 heads, dim 128, 256 blocks of 16, 512-token partitions
+    # fp32 partials: o [B, Hq, P, D] and (m, l) [B, Hq, P, 2]
     assert pkv.pkv_decode_workspace_bytes(64, 32, 128, 256, 16, 512) == 64 * 32 * 8 * 130 * 4
     # one partition covers everything: single pass, no workspace
     assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 512) == 0
     assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == 4 * 32 * 128 * 130 * 4
+    assert pkv.pkv_decode_workspace_bytes(1, 3, 64, 64, 16, 512) == 3 * 2 * 66 * 4

@@ -194,3 +194,49 @@ def test_bad_table_entry_sets_status_and_is_skipped(pkv, cuda_dev):
                                    kp[0].float().cpu().numpy().transpose(1, 0, 2), 0.1)
     assert_close(out[0].float().cpu().numpy(), want)
     assert pkv.pkv_device_status() == 0
+
+
+def _decode_append(pkv, c, partition_size=0):
+    w = c.w
+    B = len(c.decoded)
+    out = torch.empty((B, w["hq"], w["d"]), dtype=w["torch_dtype"], device=c.q.device)
+    n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, partition_size)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=c.q.device)
+    slots = torch.from_numpy(c.step_slots.copy()).to(c.q.device)
+    pkv.pkv_paged_attention_decode_append(c.q, c.new_k, c.new_v, slots, c.k_pool, c.v_pool, c.tables,
+                                          c.lens, w["scale"], out, ws, partition_size)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name,ps", [("tiny", 0), ("tiny", 16), ("llama3_8b_b64", 512),
+                                     ("long_splitk", 512), ("prefix_cow_2008", 256)])
+def test_fused_append_decode(pkv, cuda_dev, name, ps):
+    """One kernel writes the step's new rows and attends with them: the
+    output matches the oracle and the pool then holds the new rows exactly."""
+    w = syn.workload(name)
+    c = build(pkv, w, cuda_dev, step_append=False, empty_fill=float("nan"))
+    out = _decode_append(pkv, c, ps)
+    assert pkv.pkv_device_status() == 0
+    assert_close(out.float().cpu().numpy(), expected(c), what="fused %s" % name)
+    for i, slot in enumerate(c.step_slots):
+        blk, off = divmod(int(slot), 16)
+        assert torch.equal(c.k_pool[blk, :, off], c.new_k[i])
+        assert torch.equal(c.v_pool[blk, :, off], c.new_v[i])
+    # a second call with the rows now in the pool gives the same bits
+    out2 = _decode_append(pkv, c, ps)
+    assert torch.equal(out, out2)
+
+
+def test_fused_append_rejects_wrong_slot(pkv, cuda_dev):
+    w = syn.workload("tiny")
+    c = build(pkv, w, cuda_dev, step_append=False, empty_fill=0.0)
+    c.step_slots = c.step_slots.copy()
+    good = int(c.step_slots[1])
+    c.step_slots[1] = good + 1 if good % 16 < 15 else good - 1  # wrong offset
+    pkv.pkv_device_status()
+    _decode_append(pkv, c, 0)
+    assert pkv.pkv_device_status() & pkv.PKV_STATUS_BAD_SLOT
+    blk, off = divmod(int(c.step_slots[1]), 16)
+    assert (c.k_pool[blk, :, off] == 0).all()  # nothing written at the wrong slot
+    assert pkv.pkv_device_status() == 0
