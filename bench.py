@@ -1,14 +1,26 @@
-"""Benchmark: paged decode attention on one Llama-3-8B-shaped layer.
+"""Benchmark: paged decode attention (KV GB/s, % of HBM peak, sequences/s).
 
-One step = the decode-step KV-append of one new token per sequence followed
-by paged GQA decode attention (partition kernel + split-K merge) over
-64 sequences with context lengths uniform in [512, 4096] (seeded), 32 query /
-8 KV heads, head dim 128, bf16, 16-token blocks from a 40,000-block pool in
-seeded random order.  The metric is decode-attention KV bytes per second
-(4,096 bytes per token per layer: K and V, 8 heads x 128 x 2 bytes).
+Default workload (the one the headline metric is quoted on): one
+Llama-3-8B-shaped layer -- 64 sequences with context lengths uniform in
+[512, 4096] (seeded), 32 query / 8 KV heads, head dim 128, bf16, 16-token
+blocks from a 40,000-block pool in seeded random order.  One step = the
+decode step's KV-append of one new token per sequence and paged GQA decode
+attention over the whole context (split-K partition kernel with the append
+fused in, then the merge kernel).  The metric counts the KV bytes the decode
+attention reads: 4,096 bytes per token per layer (K and V, 8 heads x 128 x
+2 bytes).
+
+Other workloads (``--workload``, one JSON line each):
+  long_splitk   4 sequences of 65,536 / 32,768 x 3 tokens, interleaved blocks
+  quant_int4    32 x 16,384 tokens, INT4 cache (group = head dim), 4 sinks:
+                step = quantised append + quantised decode, 1,088 B/token
+  quant_fp8     the same with an FP8 E4M3 cache, 2,080 B/token
+  prefix_cow    8 children forked from a 2,000-token prompt + tails of
+                1..300 tokens (logical bytes: shared blocks counted per child)
 
 Prints ONE JSON line.  Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
+                    [--workload NAME]
 N > 1 runs under torch.distributed.run, one rank per GPU; every rank decodes
 its own batch (weak scaling, no collective on the data path; the barrier and
 the max-over-ranks of the elapsed time are the only cross-rank calls).
@@ -28,13 +40,37 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "llama3_8b_b64"
 METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; sequences/s per layer"
 KV_BYTES_PER_TOKEN = 2 * 8 * 128 * 2  # K and V, 8 KV heads, head dim 128, bf16
-L2_BYTES = 129 * 10 ** 6
 NOMINAL_HBM_GBS = 8000.0
 DECODE_SOURCES = ["paged_kv_cache_13_gb300/csrc/decode.cu", "paged_kv_cache_13_gb300/csrc/common.cuh"]
 TRAFFIC_FILE = "profiles/paged_decode_bf16_llama3_8b_b64_traffic.txt"
+
+# name -> (synthetic workload, overrides, cache mode)
+WORKLOADS = {
+    "llama3_8b_b64": ("llama3_8b_b64", {}, None),
+    "long_splitk": ("long_splitk", {}, None),
+    "quant_int4": ("quant", {}, "int4"),
+    "quant_fp8": ("quant", {}, "fp8"),
+    "prefix_cow": ("prefix_cow", {}, None),
+}
+
+DESCRIPTIONS = {
+    "llama3_8b_b64": "one Llama-3-8B-shaped layer, 64 sequences, context uniform in [512, 4096] "
+                     "(seeded), 32 q / 8 KV heads, head dim 128, bf16, 16-token blocks, "
+                     "40,000-block pool in seeded random order",
+    "long_splitk": "4 sequences of 65,536 / 32,768 / 32,768 / 32,768 tokens, blocks allocated "
+                   "round-robin across the sequences from a shuffled 12,288-block pool, 32 q / 8 "
+                   "KV heads, head dim 128, bf16",
+    "quant_int4": "32 sequences x 16,384 tokens, 32 q / 8 KV heads, head dim 128, bf16 queries, "
+                  "INT4 asymmetric cache with fp16 scale/zero per (token, head), 4 bf16 sink "
+                  "tokens, values N(0,1) with 1% outliers at +-8",
+    "quant_fp8": "32 sequences x 16,384 tokens, 32 q / 8 KV heads, head dim 128, bf16 queries, "
+                 "FP8 E4M3 cache with an fp16 scale per (token, head), 4 bf16 sink tokens, "
+                 "values N(0,1) with 1% outliers at +-8",
+    "prefix_cow": "8 sequences forked from a shared 2,000-token prompt, each extended by a "
+                  "seeded tail of 1..300 tokens, 32 q / 8 KV heads, head dim 128, bf16",
+}
 
 
 def parse_args():
@@ -43,10 +79,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_b64", choices=sorted(WORKLOADS))
     ap.add_argument("--partition-size", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-blocks", type=int, default=0,
-                    help="override the pool size (blocks); 0 keeps the workload's 40,000")
+                    help="override the pool size (blocks); 0 keeps the workload's")
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -166,63 +203,161 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------- device setup
-class Layer:
-    """The workload's cache, built with the library's own entry points."""
+class Cache:
+    """A workload's paged cache, built with the library's own entry points
+    (host block manager, KV-append / quantised append, copy-on-write copy)."""
 
-    def __init__(self, pkv, torch, device, partition_size, headroom_tokens, pool_blocks=0):
+    def __init__(self, pkv, torch, device, name, partition_size, headroom_tokens, pool_blocks=0):
         import synthetic as syn
-        self.pkv, self.torch, self.dev = pkv, torch, device
-        w = syn.workload(WORKLOAD, **({"num_blocks": pool_blocks} if pool_blocks else {}))
-        self.w = w
+        base, over, qmode = WORKLOADS[name]
+        over = dict(over)
+        if pool_blocks:
+            over["num_blocks"] = pool_blocks
+        w = syn.workload(base, **over)
+        self.pkv, self.torch, self.dev, self.w, self.qmode, self.name = pkv, torch, device, w, qmode, name
         NB, BS, Hkv, D, Hq = w["num_blocks"], w["block_size"], w["hkv"], w["d"], w["hq"]
         dt = w["torch_dtype"]
         self.pool = pkv.pkv_pool_create(NB, BS, syn.free_order(w))
-        self.k_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
-        self.v_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
         ops, decoded = syn.prefill_schedule(w)
         self.seqs = np.array(decoded, dtype=np.int64)
         B = len(decoded)
-        rows = {}
+        self.B = B
+        self.n_sink = w.get("n_sink", 0)
+        if qmode is None:
+            self.k_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
+            self.v_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
+            self.pools = [self.k_pool, self.v_pool]
+        else:
+            cb = D // 2 if qmode == "int4" else D
+            u8, f16 = torch.uint8, torch.float16
+            self.cache = {
+                "k_codes": torch.empty((NB, Hkv, BS, cb), dtype=u8, device=device),
+                "v_codes": torch.empty((NB, Hkv, BS, cb), dtype=u8, device=device),
+                "k_scale": torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device),
+                "v_scale": torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device),
+                "sink_k": torch.zeros((B, max(self.n_sink, 1), Hkv, D), dtype=dt, device=device),
+                "sink_v": torch.zeros((B, max(self.n_sink, 1), Hkv, D), dtype=dt, device=device),
+            }
+            if qmode == "int4":
+                self.cache["k_zero"] = torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device)
+                self.cache["v_zero"] = torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device)
+            self.pools = [self.cache[k] for k in ("k_codes", "k_scale", "k_zero", "v_codes",
+                                                  "v_scale", "v_zero") if k in self.cache]
+        row_of = {h: i for i, h in enumerate(decoded)}
+        src = {}
+
+        def rows(h, start, n):
+            key = "prompt" if ("prompt" in w and h == 0) else (h - 1 if "prompt" in w else h)
+            if key not in src:
+                src[key] = syn.prompt_kv(w) if key == "prompt" else syn.sequence_kv(w, key)
+            k, v = src[key]
+            return k[start:start + n], v[start:start + n]
+
+        lens = {}
         for op in ops:
             if op[0] == "create":
                 pkv.pkv_seq_create(self.pool)
-            elif op[0] == "append":
+            elif op[0] == "fork":
+                child = pkv.pkv_seq_fork(self.pool, op[1])
+                lens[child] = lens.get(op[1], 0)
+            else:
                 _, h, n = op
+                start = lens.get(h, 0)
                 slots, pairs = pkv.pkv_seq_append(self.pool, h, n)
-                assert not pairs
-                k, v = syn.sequence_kv(w, h)
-                rows[h] = (k, v)
-                pkv.pkv_kv_append(k[:n].to(device), v[:n].to(device),
-                                  torch.from_numpy(slots).to(device), self.k_pool, self.v_pool)
+                if pairs:
+                    pkv.pkv_copy_blocks(self.pools, torch.tensor(pairs, dtype=torch.int32, device=device))
+                k, v = rows(h, start, n)
+                self._append(k.to(device), v.to(device), torch.from_numpy(slots).to(device),
+                             np.arange(start, start + n), row_of.get(h, 0))
+                lens[h] = start + n
+        if qmode is not None and "prompt" in w:
+            kp, vp = rows(0, 0, self.n_sink)
+            for r in range(B):
+                self.cache["sink_k"][r, :self.n_sink] = kp.to(device)
+                self.cache["sink_v"][r, :self.n_sink] = vp.to(device)
         # the decode step's append: token L-1 of every sequence
         slots, pairs = pkv.pkv_seq_append_batch(self.pool, self.seqs, 1)
-        self.new_k = torch.stack([rows[h][0][-1] for h in decoded]).to(device)
-        self.new_v = torch.stack([rows[h][1][-1] for h in decoded]).to(device)
+        if len(pairs):
+            pkv.pkv_copy_blocks(self.pools, torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
+        nk, nv = [], []
+        for h in decoded:
+            k, v = rows(h, lens[h], 1)
+            nk.append(k[0])
+            nv.append(v[0])
+        self.new_k = torch.stack(nk).to(device)
+        self.new_v = torch.stack(nv).to(device)
         self.slots = torch.from_numpy(slots.copy()).to(device)
-        lens = syn.context_lengths(w)
-        self.max_blocks = -(-max(lens) // BS)  # exact: the timed decode reads these tables
-        self.max_blocks_grown = -(-(max(lens) + headroom_tokens) // BS)  # for the e2e loop
+        self.positions = torch.tensor([lens[h] for h in decoded], dtype=torch.int32, device=device)
+        self.seq_idx = torch.arange(B, dtype=torch.int32, device=device)
+        ctx_list = syn.context_lengths(w)
+        self.max_blocks = -(-max(ctx_list) // BS)  # exact: the timed decode reads these tables
+        self.max_blocks_grown = -(-(max(ctx_list) + headroom_tokens) // BS)  # for the e2e loop
         tables, ctx = pkv.pkv_build_block_tables(self.pool, self.seqs, self.max_blocks)
         self.tables = torch.from_numpy(tables.copy()).to(device)
         self.lens = torch.from_numpy(ctx.copy()).to(device)
         self.ctx_host = ctx.copy()
+        self.unique_blocks = len(set(int(x) for x in tables.ravel() if x >= 0))
         self.q = syn.query(w).to(device)
         self.out = torch.empty((B, Hq, D), dtype=dt, device=device)
         self.partition_size = partition_size
         ws = pkv.pkv_decode_workspace_bytes(B, Hq, D, self.max_blocks, BS, partition_size)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
-        self.B = B
         torch.cuda.synchronize()
 
-    def kv_bytes(self, ctx=None):
-        return int(np.sum(self.ctx_host if ctx is None else ctx)) * KV_BYTES_PER_TOKEN
+    def _append(self, k, v, slots, positions, seq_row):
+        if self.qmode is None:
+            self.pkv.pkv_kv_append(k, v, slots, self.k_pool, self.v_pool)
+            return
+        torch = self.torch
+        if not torch.is_tensor(positions):
+            positions = torch.from_numpy(np.asarray(positions, dtype=np.int32)).to(self.dev)
+        sidx = torch.full((k.shape[0],), seq_row, dtype=torch.int32, device=self.dev)
+        self.pkv.pkv_kv_append_quant(k, v, slots, positions, sidx, self.cache, self.n_sink,
+                                     self.qmode)
 
-    # one step, device-resident inputs: one kernel appends the new rows and
-    # attends (split-K partials merged by the last CTA of each sequence/head)
-    def step(self):
-        self.pkv.pkv_paged_attention_decode_append(
-            self.q, self.new_k, self.new_v, self.slots, self.k_pool, self.v_pool, self.tables,
-            self.lens, self.w["scale"], self.out, self.ws, self.partition_size)
+    def bytes_per_token(self):
+        Hkv, D = self.w["hkv"], self.w["d"]
+        if self.qmode == "int4":
+            return 2 * Hkv * (D // 2 + 4)
+        if self.qmode == "fp8":
+            return 2 * Hkv * (D + 2)
+        return 2 * Hkv * D * 2
+
+    def kv_bytes(self, ctx=None):
+        """Algorithmic KV bytes one decode reads (sinks read in 16-bit)."""
+        ctx = self.ctx_host if ctx is None else ctx
+        total = int(np.sum(ctx)) * self.bytes_per_token()
+        if self.qmode is not None:
+            total += int(np.sum(np.minimum(ctx, self.n_sink))) * 2 * self.w["hkv"] * self.w["d"] * 2
+        return total
+
+    def step(self, q=None, k_new=None, v_new=None, slots=None, tables=None, lens=None, out=None,
+             ws=None, positions=None, stream=None):
+        """One decode step: append each sequence's new row, then attend."""
+        pkv = self.pkv
+        q = self.q if q is None else q
+        k_new = self.new_k if k_new is None else k_new
+        v_new = self.new_v if v_new is None else v_new
+        slots = self.slots if slots is None else slots
+        tables = self.tables if tables is None else tables
+        lens = self.lens if lens is None else lens
+        out = self.out if out is None else out
+        ws = self.ws if ws is None else ws
+        if self.qmode is None:
+            pkv.pkv_paged_attention_decode_append(q, k_new, v_new, slots, self.k_pool, self.v_pool,
+                                                  tables, lens, self.w["scale"], out, ws,
+                                                  self.partition_size, stream)
+            return
+        positions = self.positions if positions is None else positions
+        pkv.pkv_kv_append_quant(k_new, v_new, slots, positions, self.seq_idx, self.cache,
+                                self.n_sink, self.qmode, 0, stream)
+        pkv.pkv_paged_attention_decode_quant(q, self.cache, self.n_sink, tables, lens,
+                                             self.w["scale"], out, self.qmode, 0, ws,
+                                             self.partition_size, stream)
+
+    def launches_per_step(self):
+        split = self.max_blocks * 16 > self.partition_size
+        return (2 if split else 1) + (1 if self.qmode else 0)
 
 
 def run_device(args, rank, world, dist):
@@ -233,14 +368,14 @@ def run_device(args, rank, world, dist):
     torch.cuda.set_device(dev_index)
     device = torch.device("cuda", dev_index)
     e2e_steps = max(1, min(args.steps, 200))
-    layer = Layer(pkv, torch, device, args.partition_size, headroom_tokens=e2e_steps + args.warmup + 8,
-                  pool_blocks=args.pool_blocks)
+    cache = Cache(pkv, torch, device, args.workload, args.partition_size,
+                  headroom_tokens=e2e_steps + 8, pool_blocks=args.pool_blocks)
     stream = torch.cuda.current_stream()
-    kv_bytes = layer.kv_bytes()
+    kv_bytes = cache.kv_bytes()
 
     # ---------- device-resident timed region
     for _ in range(args.warmup):
-        layer.step()
+        cache.step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -253,7 +388,7 @@ def run_device(args, rank, world, dist):
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
-        layer.step()
+        cache.step()
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -261,53 +396,49 @@ def run_device(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
-    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     assert pkv.pkv_device_status() == 0
     elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
     ms_per_step = elapsed_ms / args.steps
 
     # ---------- end to end through the public API, host buffers
-    e2e = run_e2e(pkv, torch, layer, e2e_steps, dist, device)
+    e2e = run_e2e(pkv, torch, cache, e2e_steps, dist, device)
 
-    return dict(ms_per_step=ms_per_step, kern_ms=kern_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
-                B=layer.B, launches=2 * args.steps)  # partials + merge per step
+    return dict(ms_per_step=ms_per_step, call_ms=call_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
+                B=cache.B, launches=cache.launches_per_step() * args.steps,
+                unique_blocks=cache.unique_blocks)
 
 
-def run_e2e(pkv, torch, layer, steps, dist, device):
-    """Every step: host allocator append + tables, H2D of q / new K,V / slots /
-    tables / lens from pinned memory, KV-append + decode, D2H of the output."""
+def run_e2e(pkv, torch, cache, steps, dist, device):
+    """Every step: host block manager append + tables, H2D of q / new K,V /
+    slots / tables / lens (and positions for a quantised cache) from pinned
+    memory, the decode step, D2H of the output."""
     import synthetic as syn
-    w = layer.w
-    B, Hq, Hkv, D = layer.B, w["hq"], w["hkv"], w["d"]
+    w = cache.w
+    B, Hq, Hkv, D = cache.B, w["hq"], w["hkv"], w["d"]
     dt = w["torch_dtype"]
+    mb = cache.max_blocks_grown
     pin = dict(pin_memory=True)
     h_q = torch.empty((B, Hq, D), dtype=dt, **pin)
     h_k = torch.empty((B, Hkv, D), dtype=dt, **pin)
     h_v = torch.empty((B, Hkv, D), dtype=dt, **pin)
     h_slots = torch.empty(B, dtype=torch.int64, **pin)
     h_pairs = torch.empty(2 * B, dtype=torch.int32, **pin)
-    mb = layer.max_blocks_grown
     h_tab = torch.empty((B, mb), dtype=torch.int32, **pin)
     h_lens = torch.empty(B, dtype=torch.int32, **pin)
+    h_pos = torch.empty(B, dtype=torch.int32, **pin)
     h_out = torch.empty((B, Hq, D), dtype=dt, **pin)
-    d_q = torch.empty_like(h_q, device=device)
-    d_k = torch.empty_like(h_k, device=device)
-    d_v = torch.empty_like(h_v, device=device)
-    d_slots = torch.empty_like(h_slots, device=device)
-    d_tab = torch.empty_like(h_tab, device=device)
-    d_lens = torch.empty_like(h_lens, device=device)
+    d_q, d_k, d_v = (torch.empty_like(t, device=device) for t in (h_q, h_k, h_v))
+    d_slots, d_tab, d_lens, d_pos = (torch.empty_like(t, device=device)
+                                     for t in (h_slots, h_tab, h_lens, h_pos))
     d_out = torch.empty_like(h_out, device=device)
-    ws = torch.empty(max(16, pkv.pkv_decode_workspace_bytes(B, Hq, D, mb, 16, layer.partition_size)),
+    ws = torch.empty(max(16, pkv.pkv_decode_workspace_bytes(B, Hq, D, mb, 16, cache.partition_size)),
                      dtype=torch.uint8, device=device)
-    # fresh per-step inputs, generated before the timed region
-    inputs = []
-    for s in range(steps):
-        k, v = syn.new_token_kv(w, s)
-        inputs.append((k, v))
+    inputs = [syn.new_token_kv(w, s) for s in range(steps)]
     h_q.copy_(syn.query(w))
     stream = torch.cuda.current_stream()
     h2d = (h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_slots.numel() * 8
-           + h_tab.numel() * 4 + h_lens.numel() * 4)
+           + h_tab.numel() * 4 + h_lens.numel() * 4 + (h_pos.numel() * 4 if cache.qmode else 0))
     d2h = h_out.numel() * 2
     total_kv = 0
     if dist is not None:
@@ -317,19 +448,23 @@ def run_e2e(pkv, torch, layer, steps, dist, device):
     for s in range(steps):
         h_k.copy_(inputs[s][0])
         h_v.copy_(inputs[s][1])
-        slots, pairs = pkv.pkv_seq_append_batch(layer.pool, layer.seqs, 1, h_slots.numpy(), h_pairs.numpy())
-        assert len(pairs) == 0
-        pkv.pkv_build_block_tables(layer.pool, layer.seqs, mb, h_tab.numpy(), h_lens.numpy())
-        total_kv += int(h_lens.numpy().sum()) * KV_BYTES_PER_TOKEN
+        _, pairs = pkv.pkv_seq_append_batch(cache.pool, cache.seqs, 1, h_slots.numpy(), h_pairs.numpy())
+        if len(pairs):
+            pkv.pkv_copy_blocks(cache.pools, torch.from_numpy(np.ascontiguousarray(pairs)).to(device))
+        pkv.pkv_build_block_tables(cache.pool, cache.seqs, mb, h_tab.numpy(), h_lens.numpy())
+        lens = h_lens.numpy()
+        total_kv += cache.kv_bytes(lens)
         d_q.copy_(h_q, non_blocking=True)
         d_k.copy_(h_k, non_blocking=True)
         d_v.copy_(h_v, non_blocking=True)
         d_slots.copy_(h_slots, non_blocking=True)
         d_tab.copy_(h_tab, non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
-        pkv.pkv_paged_attention_decode_append(d_q, d_k, d_v, d_slots, layer.k_pool, layer.v_pool,
-                                              d_tab, d_lens, w["scale"], d_out, ws,
-                                              layer.partition_size, stream)
+        if cache.qmode:
+            np.subtract(lens, 1, out=h_pos.numpy())
+            d_pos.copy_(h_pos, non_blocking=True)
+        cache.step(q=d_q, k_new=d_k, v_new=d_v, slots=d_slots, tables=d_tab, lens=d_lens,
+                   out=d_out, ws=ws, positions=d_pos, stream=stream)
         h_out.copy_(d_out, non_blocking=True)
         stream.synchronize()
     elapsed = max_over_ranks(time.perf_counter() - t_start, dist, device)
@@ -338,13 +473,14 @@ def run_e2e(pkv, torch, layer, steps, dist, device):
 
 
 # -------------------------------------------------------------- CPU oracle
-def cpu_worker(min_seconds):
-    """Times the oracle's paged decode on a sample of the workload (16 of
-    the 64 sequences, all 32 query heads), repeated until min_seconds."""
+def oracle_sample(name, S):
+    """The first S decoded sequences of a workload as an oracle-side paged
+    cache.  Returns (decode(), kv bytes per decode, S, tokens)."""
     import synthetic as syn
     from oracle import allocator, attention, kvcache
-    w = syn.workload(WORKLOAD)
-    S = 16
+    base, over, qmode = WORKLOADS[name]
+    w = syn.workload(base, **over)
+    S = min(S, len(syn.context_lengths(w)))
     q = syn.kv_rows_to_numpy(syn.query(w))[:S]
     ks, vs = [], []
     for i in range(S):
@@ -353,30 +489,77 @@ def cpu_worker(min_seconds):
         vs.append(syn.kv_rows_to_numpy(v))
     nb = sum(-(-k.shape[0] // 16) for k in ks)
     m = allocator.KVCacheManager(nb, 16, syn.free_order(dict(w, num_blocks=nb)))
-    kp = np.zeros((nb, w["hkv"], 16, w["d"]), np.float32)
-    vp = np.zeros_like(kp)
-    sids = []
+    Hkv, D = w["hkv"], w["d"]
+    sids, all_slots = [], []
     for i in range(S):
         s = m.create()
         slots, _ = m.append(s, ks[i].shape[0])
-        kvcache.kv_append(ks[i], vs[i], slots, kp, vp)
         sids.append(s)
+        all_slots.append(slots)
     tables, ctx = m.block_tables(sids, max(len(m.table(s)) for s in sids))
+    if qmode is None:
+        kp = np.zeros((nb, Hkv, 16, D), np.float32)
+        vp = np.zeros_like(kp)
+        for i in range(S):
+            kvcache.kv_append(ks[i], vs[i], all_slots[i], kp, vp)
+
+        def decode():
+            attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"])
+        kvb = int(np.sum(ctx)) * 2 * Hkv * D * 2
+    else:
+        ns = w["n_sink"]
+        cb = D // 2 if qmode == "int4" else D
+        cache = {"k_codes": np.zeros((nb, Hkv, 16, cb), np.uint8),
+                 "v_codes": np.zeros((nb, Hkv, 16, cb), np.uint8),
+                 "k_scale": np.zeros((nb, Hkv, 16, 1), np.float16),
+                 "v_scale": np.zeros((nb, Hkv, 16, 1), np.float16),
+                 "k_zero": np.zeros((nb, Hkv, 16, 1), np.float16),
+                 "v_zero": np.zeros((nb, Hkv, 16, 1), np.float16),
+                 "sink_k": np.zeros((S, ns, Hkv, D)), "sink_v": np.zeros((S, ns, Hkv, D))}
+        for i in range(S):
+            # the oracle's vectorised quantiser, written at the slots
+            _, kc, ksc, kz = kvcache.quantize_sequence(ks[i], qmode, D)
+            _, vc, vsc, vz = kvcache.quantize_sequence(vs[i], qmode, D)
+            for t, slot in enumerate(all_slots[i]):
+                blk, off = divmod(int(slot), 16)
+                cache["k_codes"][blk, :, off] = kc[t]
+                cache["v_codes"][blk, :, off] = vc[t]
+                cache["k_scale"][blk, :, off] = ksc[t]
+                cache["v_scale"][blk, :, off] = vsc[t]
+                if kz is not None:
+                    cache["k_zero"][blk, :, off] = kz[t]
+                    cache["v_zero"][blk, :, off] = vz[t]
+            cache["sink_k"][i] = ks[i][:ns]
+            cache["sink_v"][i] = vs[i][:ns]
+
+        def decode():
+            kvcache.paged_attention_decode_quant(q, cache, tables, ctx, w["scale"], ns, qmode, D)
+        per_tok = 2 * Hkv * (D // 2 + 4) if qmode == "int4" else 2 * Hkv * (D + 2)
+        kvb = int(np.sum(ctx)) * per_tok + int(np.sum(np.minimum(ctx, ns))) * 2 * Hkv * D * 2
+    return decode, kvb, S, int(np.sum(ctx))
+
+
+def cpu_worker(name, min_seconds, S):
+    decode, kvb, S, toks = oracle_sample(name, S)
     reps, t0 = 0, time.perf_counter()
     while True:
-        attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"])
+        decode()
         reps += 1
         if time.perf_counter() - t0 >= min_seconds:
             break
     dt = time.perf_counter() - t0
-    kv = int(np.sum(ctx)) * KV_BYTES_PER_TOKEN * reps
-    print(json.dumps({"seconds": dt, "reps": reps, "kv_bytes": kv, "seqs": S * reps}))
+    print(json.dumps({"seconds": dt, "reps": reps, "kv_bytes": kvb * reps, "seqs": S * reps,
+                      "sample_seqs": S, "sample_tokens": toks}))
 
 
-def cpu_baseline(min_seconds):
+CPU_SAMPLE_SEQS = {"llama3_8b_b64": 16, "long_splitk": 1, "quant_int4": 1, "quant_fp8": 1,
+                   "prefix_cow": 8}
+
+
+def cpu_baseline(name, min_seconds):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(min_seconds)],
-                       capture_output=True, text=True, env=env, cwd=ROOT)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(min_seconds),
+                        "--workload", name], capture_output=True, text=True, env=env, cwd=ROOT)
     if r.returncode != 0:
         return None
     res = json.loads(r.stdout.strip().splitlines()[-1])
@@ -385,29 +568,35 @@ def cpu_baseline(min_seconds):
         "unit": "GB/s",
         "cores": 1,
         "kind": "oracle",
-        "sample": "float64 NumPy oracle paged decode of 16 of the 64 sequences (all 32 query "
-                  "heads), repeated %d times in %.1f s, single thread" % (res["reps"], res["seconds"]),
+        "sample": "float64 NumPy oracle paged decode of %d sequence(s) of the workload (%d tokens, "
+                  "all 32 query heads), repeated %d times in %.1f s, single thread"
+                  % (res["sample_seqs"], res["sample_tokens"], res["reps"], res["seconds"]),
         "seq_per_s": res["seqs"] / res["seconds"],
     }
 
 
-def config_block(B, kv_bytes, partition_size):
+def config_block(name, B, kv_bytes, partition_size):
+    step = ("quantised KV-append of 1 token per sequence + paged decode over the quantised "
+            "cache (split-K partials, merge kernel)" if WORKLOADS[name][2] else
+            "KV-append of 1 token per sequence fused into the paged decode (split-K "
+            "partials, then a merge kernel with programmatic dependent launch)")
     return {
-        "workload": "%s: one Llama-3-8B-shaped layer, %d sequences, context uniform in [512, 4096] "
-                    "(seeded), 32 q / 8 KV heads, head dim 128, bf16, 16-token blocks, 40,000-block "
-                    "pool in seeded random order; step = KV-append of 1 token per sequence + paged "
-                    "decode attention (split-K partials with the append fused, then a merge launched with programmatic dependent launch; %d-token partitions)" % (WORKLOAD, B, partition_size),
+        "workload": "%s: %s; step = %s, %d-token partitions" % (name, DESCRIPTIONS[name], step,
+                                                              partition_size),
         "batch": B,
         "kv_bytes_per_step": kv_bytes,
         "partition_size": partition_size,
-        "l2": "inputs larger than L2 (%.0f MB of KV read per step vs 129 MB L2), no flush" % (kv_bytes / 1e6),
+        "l2": ("inputs larger than L2 (%.0f MB of KV read per step vs 129 MB L2), no flush"
+               % (kv_bytes / 1e6)) if kv_bytes > 129e6 else
+              ("KV working set %.0f MB fits the 129 MB L2: numbers are L2-resident"
+               % (kv_bytes / 1e6)),
     }
 
 
 def main():
     args = parse_args()
     if args.cpu_worker is not None:
-        cpu_worker(args.cpu_worker)
+        cpu_worker(args.workload, args.cpu_worker, CPU_SAMPLE_SEQS[args.workload])
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -428,10 +617,11 @@ def main():
         return
     value = whole_job_rate(res["kv_bytes"], world, res["ms_per_step"] * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    achieved = res["kv_bytes"] / (res["kern_ms"] * 1e-3) / 1e9
+    achieved = res["kv_bytes"] / (res["call_ms"] * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(10.0)
+        cpu = cpu_baseline(args.workload, 10.0)
+    quant = WORKLOADS[args.workload][2]
     line = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -443,23 +633,25 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if not quant else ("bf16 q, u4 KV codes" if quant == "int4" else "bf16 q, e4m3 KV codes"),
         "data": "synthetic",
-        "config": config_block(res["B"], res["kv_bytes"], args.partition_size),
+        "config": config_block(args.workload, res["B"], res["kv_bytes"], args.partition_size),
         "seq_per_s_per_layer": round(res["B"] * world / (res["ms_per_step"] * 1e-3), 1),
         "pct_of_8tbs_nominal": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": "hbm",
-            "kernel": "paged_decode_kernel<bf16, 128, split-K partials, fused append> + merge_kernel (programmatic dependent launch)",
+            "kernel": ("kv_append_quant + paged_decode_quant_kernel + merge_kernel" if quant else
+                       "paged_decode_kernel<bf16, 128, partials, fused append> + merge_kernel"),
             "achieved": round(achieved, 1),
             "peak": peak,
-            "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)" if peak_kind == "measured" else peak_kind,
+            "peak_kind": ("measured (MEASURED_PEAKS.json hbm_gbs, copy, burst)"
+                          if peak_kind == "measured" else "fallback"),
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(res["kv_bytes"]),
+            "traffic": recorded_traffic(res["kv_bytes"]) if args.workload == "llama3_8b_b64" else None,
             "algorithmic_bytes_per_launch": res["kv_bytes"],
-            "avg_launch_ms": res["kern_ms"],
+            "avg_launch_ms": res["call_ms"],
         },
         "e2e": {
             "value": round(res["e2e"]["gbs"] * world, 1),
@@ -472,41 +664,22 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
     }
+    if args.workload == "prefix_cow":
+        line["unique_kv_bytes_per_step"] = res["unique_blocks"] * 16 * KV_BYTES_PER_TOKEN
     print(json.dumps(line))
 
 
 def run_reference(args, world):
     """The oracle, as it stands, on the host cores: each step is the oracle's
-    paged decode of a bounded sample (2 of the 64 sequences, all heads)."""
-    import synthetic as syn
-    from oracle import allocator, attention, kvcache
-    w = syn.workload(WORKLOAD)
-    S = 2
-    q = syn.kv_rows_to_numpy(syn.query(w))[:S]
-    ks, vs = [], []
-    for i in range(S):
-        k, v = syn.sequence_kv(w, i)
-        ks.append(syn.kv_rows_to_numpy(k))
-        vs.append(syn.kv_rows_to_numpy(v))
-    nb = sum(-(-k.shape[0] // 16) for k in ks)
-    m = allocator.KVCacheManager(nb, 16, syn.free_order(dict(w, num_blocks=nb)))
-    kp = np.zeros((nb, w["hkv"], 16, w["d"]), np.float32)
-    vp = np.zeros_like(kp)
-    sids = []
-    for i in range(S):
-        s = m.create()
-        slots, _ = m.append(s, ks[i].shape[0])
-        kvcache.kv_append(ks[i], vs[i], slots, kp, vp)
-        sids.append(s)
-    tables, ctx = m.block_tables(sids, max(len(m.table(s)) for s in sids))
+    paged decode of a bounded sample (2 sequences of the workload, all heads)."""
+    decode, kvb, S, toks = oracle_sample(args.workload, 2 if args.workload != "long_splitk" else 1)
     for _ in range(args.warmup):
-        attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"])
+        decode()
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"])
+        decode()
     dt = time.perf_counter() - t0
-    kv = int(np.sum(ctx)) * KV_BYTES_PER_TOKEN
-    value = kv * args.steps / dt / 1e9
+    value = kvb * args.steps / dt / 1e9
     threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
     cores = int(threads) if threads and threads.isdigit() else len(os.sched_getaffinity(0))
     line = {
@@ -523,10 +696,10 @@ def run_reference(args, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": config_block(64, kv, args.partition_size),
+        "config": config_block(args.workload, S, kvb, args.partition_size),
         "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
-                         "sample": "float64 NumPy oracle paged decode of 2 of the 64 sequences "
-                                   "(%d tokens, all 32 query heads) per step" % int(np.sum(ctx))},
+                         "sample": "float64 NumPy oracle paged decode of %d sequence(s) of the "
+                                   "workload (%d tokens, all 32 query heads) per step" % (S, toks)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
