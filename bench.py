@@ -80,7 +80,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--workload", default="llama3_8b_b64", choices=sorted(WORKLOADS))
-    ap.add_argument("--partition-size", type=int, default=512)
+    ap.add_argument("--partition-size", type=int, default=0,
+                    help="tokens per split-K partition; 0 = the library's automatic choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="override the pool size (blocks); 0 keeps the workload's")
@@ -299,8 +300,8 @@ class Cache:
         self.unique_blocks = len(set(int(x) for x in tables.ravel() if x >= 0))
         self.q = syn.query(w).to(device)
         self.out = torch.empty((B, Hq, D), dtype=dt, device=device)
-        self.partition_size = partition_size
-        ws = pkv.pkv_decode_workspace_bytes(B, Hq, D, self.max_blocks, BS, partition_size)
+        self.partition_size = partition_size or pkv.pkv_decode_auto_partition_size(B, Hq, self.max_blocks)
+        ws = pkv.pkv_decode_workspace_bytes(B, Hq, D, self.max_blocks, BS, self.partition_size)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
 
@@ -406,7 +407,7 @@ def run_device(args, rank, world, dist):
 
     return dict(ms_per_step=ms_per_step, call_ms=call_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
                 B=cache.B, launches=cache.launches_per_step() * args.steps,
-                unique_blocks=cache.unique_blocks)
+                unique_blocks=cache.unique_blocks, partition_size=cache.partition_size)
 
 
 def run_e2e(pkv, torch, cache, steps, dist, device):
@@ -635,7 +636,7 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if not quant else ("bf16 q, u4 KV codes" if quant == "int4" else "bf16 q, e4m3 KV codes"),
         "data": "synthetic",
-        "config": config_block(args.workload, res["B"], res["kv_bytes"], args.partition_size),
+        "config": config_block(args.workload, res["B"], res["kv_bytes"], res["partition_size"]),
         "seq_per_s_per_layer": round(res["B"] * world / (res["ms_per_step"] * 1e-3), 1),
         "pct_of_8tbs_nominal": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),

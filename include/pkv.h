@@ -176,12 +176,22 @@ int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
 /* Bytes of the split-K workspace pkv_paged_attention_decode* needs for this
  * shape: fp32 partial outputs [batch, num_q_heads, P, head_dim] and fp32
  * (max, sum) pairs [batch, num_q_heads, P, 2], P = ceil(max_blocks *
- * block_size / partition_size).  partition_size 0 selects the default (512);
- * otherwise it must be a positive multiple of block_size.  Zero when a
+ * block_size / partition_size).  partition_size 0 selects the automatic size
+ * (pkv_decode_auto_partition_size); otherwise it must be a positive multiple
+ * of block_size.  Zero when a
  * single partition covers max_blocks * block_size (single-pass decode). */
 int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                int32_t max_blocks, int32_t block_size, int32_t partition_size,
                                size_t* out);
+
+/* The partition size a decode call uses when it is passed partition_size 0:
+ * the largest of 512, 256, 128, 64 tokens for which batch * num_q_heads *
+ * ceil(max_blocks * block_size / size) >= 8 * (SM count of the current
+ * device, 152 if none), else 64.  Small batches get finer splits so the GPU
+ * has enough partition CTAs.  pkv_decode_workspace_bytes with partition_size 0
+ * applies the same rule. */
+int pkv_decode_auto_partition_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                                   int32_t block_size, int32_t* out);
 
 /* =============================================================== device */
 
@@ -199,7 +209,7 @@ int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int
  * block_tables[b, t / block_size], offset t % block_size, KV head
  * h / (num_q_heads / num_kv_heads).  fp32 accumulation; out has q's dtype;
  * a sequence with context 0 gets zeros.
- * The context is cut into partitions of partition_size tokens (0 = 512)
+ * The context is cut into partitions of partition_size tokens (0 = automatic)
  * processed by independent CTAs; when more than one partition can occur
  * (max_blocks * block_size > partition_size) partial (max, sum, output)
  * triples go to `workspace` (device, >= pkv_decode_workspace_bytes) and a

@@ -66,6 +66,7 @@ _SIGS = {
     "pkv_build_block_tables": ([_vp, _vp, _i32, _vp, _i32, _vp], _int),
     "pkv_debug_fail_after": ([_vp, _i64], _int),
     "pkv_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _int),
+    "pkv_decode_auto_partition_size": ([_i32, _i32, _i32, _i32, _p_i32], _int),
     "pkv_kv_append": ([_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _int, _vp], _int),
     "pkv_paged_attention_decode": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
@@ -279,6 +280,10 @@ def pkv_decode_workspace_bytes(batch, num_q_heads, head_dim, max_blocks, block_s
                                           partition_size, ctypes.byref(v)),
            "pkv_decode_workspace_bytes")
     return v.value
+
+
+def pkv_decode_auto_partition_size(batch, num_q_heads, max_blocks, block_size=16):
+    return _out_i32("pkv_decode_auto_partition_size", batch, num_q_heads, max_blocks, block_size)
 
 
 # ------------------------------------------------------------------ device

@@ -45,6 +45,8 @@
 // * Tokens at or past ctx in the last block get logit -inf, and their V rows
 //   are zeroed in registers (an unwritten slot may hold NaN bit patterns).
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace pkv {
@@ -79,40 +81,45 @@ struct DecodeArgs {
 // head-dim column 64 * (e / 8) + 8 * g + e % 8.
 __device__ __forceinline__ int pv_col(int e, int g) { return 64 * (e >> 3) + 8 * g + (e & 7); }
 
-// Log-sum-exp merge of `np` partition partials (m_q, l_q, o_q[d]) of one
-// (sequence, query head, column d): the loads of 8 partitions are issued
-// together, then folded into a running (M, L, acc) with one rescale per
-// chunk.  Partials are read from L2 (.cg): they may have been written by
-// other CTAs of the same launch.
-__device__ __forceinline__ float merge_partials(const float* __restrict__ ml,
+// Log-sum-exp merge of the partition partials q = q0, q0 + step, ... < np of
+// one (sequence, query head, column): each partial holds (m_q, l_q, o_q[d])
+// with o_q unnormalised.  Loads of 8 partitions are issued together, then
+// folded into a running (M, L, acc) with one rescale per chunk.  Partials
+// are read from L2 (.cg): they were written by another grid.
+struct MergeAcc {
+    float M, L, acc;
+};
+
+__device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml,
                                                 const float* __restrict__ ov, int64_t stride_o,
-                                                int np) {
-    float M = neg_inf(), L = 0.f, acc = 0.f;
-    for (int q0 = 0; q0 < np; q0 += 8) {
+                                                int q0, int np, int step) {
+    MergeAcc r{neg_inf(), 0.f, 0.f};
+    for (int qa = q0; qa < np; qa += 8 * step) {
         float mq[8], lq[8], oq[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const bool v = q0 + j < np;
-            mq[j] = v ? __ldcg(ml + 2 * (q0 + j)) : neg_inf();
-            lq[j] = v ? __ldcg(ml + 2 * (q0 + j) + 1) : 0.f;
-            oq[j] = v ? __ldcg(ov + (q0 + j) * stride_o) : 0.f;
+            const int q = qa + j * step;
+            const bool v = q < np;
+            mq[j] = v ? __ldcg(ml + 2 * q) : neg_inf();
+            lq[j] = v ? __ldcg(ml + 2 * q + 1) : 0.f;
+            oq[j] = v ? __ldcg(ov + q * stride_o) : 0.f;
         }
-        float mx = M;
+        float mx = r.M;
 #pragma unroll
         for (int j = 0; j < 8; ++j) mx = fmaxf(mx, mq[j]);
         if (mx == neg_inf()) continue;  // every partition so far was empty
-        const float sc = ex2(M - mx);   // 0 when M is still -inf
-        acc *= sc;
-        L *= sc;
+        const float sc = ex2(r.M - mx);  // 0 while M is still -inf
+        r.acc *= sc;
+        r.L *= sc;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float w = ex2(mq[j] - mx);
-            acc += w * oq[j];
-            L += w * lq[j];
+            r.acc += w * oq[j];
+            r.L += w * lq[j];
         }
-        M = mx;
+        r.M = mx;
     }
-    return L > 0.f ? acc / L : 0.f;
+    return r;
 }
 
 // Online-softmax state of one warp for the query heads 2c, 2c+1 of its lanes.
@@ -404,15 +411,18 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
 
 }
 
-// Merge the partition partials of one (sequence, query head): one thread per
-// head-dim column.  Launched right behind the partition kernel with
-// programmatic dependent launch (see run_merge).
-template <typename T, int D>
-__global__ void __launch_bounds__(D) merge_kernel(const int32_t* __restrict__ ctx_lens, int hq,
-                                                 int max_blocks, int part_blocks, int max_parts,
-                                                 const float* __restrict__ ws_o,
-                                                 const float* __restrict__ ws_ml, T* __restrict__ out) {
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+// Merge the partition partials of one (sequence, query head).  CTA of
+// D x PG threads: thread (group pg, column d) folds partitions pg, pg + PG,
+// ...; the PG running triples are then combined through shared memory.
+// PG = 1 for up to 16 partitions, 4 beyond (long contexts).  Launched right
+// behind the partition kernel with programmatic dependent launch (see
+// launch_merge).
+template <typename T, int D, int PG>
+__global__ void __launch_bounds__(D * PG) merge_kernel(
+    const int32_t* __restrict__ ctx_lens, int hq, int max_blocks, int part_blocks, int max_parts,
+    const float* __restrict__ ws_o, const float* __restrict__ ws_ml, T* __restrict__ out) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int d = threadIdx.x % D, pg = threadIdx.x / D;
     int ctx = ctx_lens[b];
     const int cap = max_blocks * BS;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
@@ -422,13 +432,63 @@ __global__ void __launch_bounds__(D) merge_kernel(const int32_t* __restrict__ ct
     // partials are produced by the preceding grid: wait for it (a no-op
     // when this grid was launched without programmatic serialization)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    out[(static_cast<int64_t>(b) * hq + h) * D + d] =
-        Half16<T>::from_float(merge_partials(ws_ml + 2 * row0, ws_o + row0 * D + d, D, np));
+    const MergeAcc r = merge_range(ws_ml + 2 * row0, ws_o + row0 * D + d, D, pg, np, PG);
+    if constexpr (PG == 1) {
+        out[(static_cast<int64_t>(b) * hq + h) * D + d] =
+            Half16<T>::from_float(r.L > 0.f ? r.acc / r.L : 0.f);
+        return;
+    }
+    __shared__ float sm[3][PG][D];
+    sm[0][pg][d] = r.M;
+    sm[1][pg][d] = r.L;
+    sm[2][pg][d] = r.acc;
+    __syncthreads();
+    if (pg == 0) {
+        float M = neg_inf();
+#pragma unroll
+        for (int j = 0; j < PG; ++j) M = fmaxf(M, sm[0][j][d]);
+        float L = 0.f, acc = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int j = 0; j < PG; ++j) {
+                const float w = ex2(sm[0][j][d] - M);
+                L += w * sm[1][j][d];
+                acc += w * sm[2][j][d];
+            }
+        }
+        out[(static_cast<int64_t>(b) * hq + h) * D + d] = Half16<T>::from_float(L > 0.f ? acc / L : 0.f);
+    }
 }
 
 struct Shape {
     int batch, hq, hkv, D, num_blocks, block_size, max_blocks, part_blocks, max_parts;
 };
+
+}  // namespace
+
+// Automatic partition size: the largest of 512, 256, 128, 64 tokens that
+// still gives >= 8 x SMs (query head, partition) work items, i.e. ~2
+// partition CTAs per SM at a GQA group of 4; small batches get finer splits.
+// (Measured on the 8-sequence prefix workload: 256 beat both 128 and 512.)
+int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
+    static std::atomic<int> sms{0};
+    int n = sms.load();
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        sms.store(n);
+    }
+    const int64_t tokens = static_cast<int64_t>(max_blocks) * BS;
+    for (int ps = 512; ps > 64; ps /= 2) {
+        const int64_t parts = (tokens + ps - 1) / ps;
+        if (static_cast<int64_t>(batch) * hq * parts >= 8LL * n) return ps;
+    }
+    return 64;
+}
+
+namespace {
 
 int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_blocks,
                 int32_t block_size, int32_t max_blocks, int32_t partition_size, int dtype,
@@ -440,7 +500,7 @@ int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_b
     if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
     if (block_size != BS || (D != 64 && D != 128) || hq / hkv > 8) return PKV_ERR_UNSUPPORTED;
     if (batch > 65535 || hkv > 65535) return PKV_ERR_UNSUPPORTED;
-    if (partition_size == 0) partition_size = 512;
+    if (partition_size == 0) partition_size = auto_partition_size(batch, hq, max_blocks);
     if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
     s->batch = batch;
     s->hq = hq;
@@ -481,12 +541,12 @@ int dispatch(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
 // its griddepcontrol.wait holds each CTA until that grid has completed and
 // its writes are visible.  This hides the second launch behind the first
 // grid's last wave.
-template <typename T, int D>
+template <typename T, int D, int PG>
 int launch_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, const float* ws_ml,
                  void* out, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(s.hq, s.batch);
-    cfg.blockDim = dim3(D);
+    cfg.blockDim = dim3(D * PG);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -494,7 +554,7 @@ int launch_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D>, ctx_lens, s.hq, s.max_blocks,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D, PG>, ctx_lens, s.hq, s.max_blocks,
                                              s.part_blocks, s.max_parts, ws_o, ws_ml,
                                              static_cast<T*>(out));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -502,12 +562,17 @@ int launch_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, con
 
 int run_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, const float* ws_ml,
               void* out, int dtype, cudaStream_t st) {
+    const bool many = s.max_parts > 16;
+#define PKV_MERGE(TT, DD)                                                                       \
+    return many ? launch_merge<TT, DD, 4>(ctx_lens, s, ws_o, ws_ml, out, st)                   \
+                : launch_merge<TT, DD, 1>(ctx_lens, s, ws_o, ws_ml, out, st)
     if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128) return launch_merge<__nv_bfloat16, 128>(ctx_lens, s, ws_o, ws_ml, out, st);
-        return launch_merge<__nv_bfloat16, 64>(ctx_lens, s, ws_o, ws_ml, out, st);
+        if (s.D == 128) PKV_MERGE(__nv_bfloat16, 128);
+        PKV_MERGE(__nv_bfloat16, 64);
     }
-    if (s.D == 128) return launch_merge<__half, 128>(ctx_lens, s, ws_o, ws_ml, out, st);
-    return launch_merge<__half, 64>(ctx_lens, s, ws_o, ws_ml, out, st);
+    if (s.D == 128) PKV_MERGE(__half, 128);
+    PKV_MERGE(__half, 64);
+#undef PKV_MERGE
 }
 
 int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_pool,
@@ -570,7 +635,7 @@ extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
     if (!out || batch < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks < 0 ||
         block_size <= 0 || partition_size < 0)
         return PKV_ERR_INVALID_ARG;
-    if (partition_size == 0) partition_size = 512;
+    if (partition_size == 0) partition_size = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
     if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
     const int64_t part_blocks = partition_size / block_size;
     const int64_t parts = (max_blocks + part_blocks - 1) / part_blocks;
@@ -613,7 +678,8 @@ extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int
     if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) || batch > 65535 ||
         num_q_heads > 65535)
         return PKV_ERR_UNSUPPORTED;
-    const int32_t ps = partition_size == 0 ? 512 : partition_size;
+    const int32_t ps = partition_size == 0 ? pkv::auto_partition_size(batch, num_q_heads, max_blocks)
+                                           : partition_size;
     if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
     pkv::Shape s;
     s.batch = batch;
@@ -682,4 +748,12 @@ extern "C" int pkv_paged_attention_decode_append(
     a.slots = slot_mapping;
     return pkv::decode<true>(a, s, out, workspace, workspace_bytes, dtype,
                              static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_decode_auto_partition_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks,
+                                              int32_t block_size, int32_t* out) {
+    if (!out || batch < 0 || num_q_heads <= 0 || max_blocks < 0) return PKV_ERR_INVALID_ARG;
+    if (block_size != pkv::BS) return PKV_ERR_UNSUPPORTED;
+    *out = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
+    return PKV_OK;
 }

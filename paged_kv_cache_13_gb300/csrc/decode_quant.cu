@@ -518,7 +518,8 @@ extern "C" int pkv_paged_attention_decode_quant(
         num_q_heads / num_kv_heads > 8 || n_sink > pkv::BS || batch > 65535 || num_kv_heads > 65535)
         return PKV_ERR_UNSUPPORTED;
     if (qmode == PKV_QMODE_INT4_ASYM && group_size != head_dim) return PKV_ERR_UNSUPPORTED;
-    const int32_t ps = partition_size == 0 ? 512 : partition_size;
+    const int32_t ps = partition_size == 0 ? pkv::auto_partition_size(batch, num_q_heads, max_blocks)
+                                           : partition_size;
     if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
     if (batch == 0) return PKV_OK;
     if (!q || !k_codes || !k_scale || !v_codes || !v_scale || !block_tables || !context_lens || !out)
@@ -570,6 +571,6 @@ extern "C" int pkv_paged_attention_decode_quant(
     int r = pkv::run<true>(a, head_dim, qmode, dtype, a.max_parts, num_kv_heads, batch, cs);
     if (r != PKV_OK) return r;
     return pkv_paged_attention_decode_merge(context_lens, batch, num_q_heads, head_dim, max_blocks,
-                                            block_size, partition_size, workspace, workspace_bytes,
-                                            out, dtype, stream);
+                                            block_size, ps, workspace, workspace_bytes, out, dtype,
+                                            stream);
 }

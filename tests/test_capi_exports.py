@@ -74,3 +74,15 @@ def test_workspace_bytes(pkv):
     assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 512) == 0
     assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == 4 * 32 * 128 * 130 * 4
     assert pkv.pkv_decode_workspace_bytes(1, 3, 64, 64, 16, 512) == 3 * 2 * 66 * 4
+
+
+def test_auto_partition_size(pkv):
+    # enough (query head, partition) items at 512 tokens: keep 512
+    assert pkv.pkv_decode_auto_partition_size(64, 32, 256) == 512
+    # 8 sequences of ~2,300 tokens: finer splits to fill 152 SMs
+    assert pkv.pkv_decode_auto_partition_size(8, 32, 144) == 256
+    assert pkv.pkv_decode_auto_partition_size(2, 32, 144) == 64
+    # tiny: the smallest size (a single partition then covers it)
+    assert pkv.pkv_decode_auto_partition_size(3, 8, 3) == 64
+    # the workspace for partition 0 follows the same rule
+    assert pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 0) == pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 256)
