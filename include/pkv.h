@@ -186,7 +186,7 @@ int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_
 
 /* The partition size a decode call uses when it is passed partition_size 0:
  * the largest of 512, 256, 128, 64 tokens for which batch * num_q_heads *
- * ceil(max_blocks * block_size / size) >= 8 * (SM count of the current
+ * ceil(max_blocks * block_size / size) >= 12 * (SM count of the current
  * device, 152 if none), else 64.  Small batches get finer splits so the GPU
  * has enough partition CTAs.  pkv_decode_workspace_bytes with partition_size 0
  * applies the same rule. */

@@ -467,7 +467,7 @@ struct Shape {
 }  // namespace
 
 // Automatic partition size: the largest of 512, 256, 128, 64 tokens that
-// still gives >= 8 x SMs (query head, partition) work items, i.e. ~2
+// still gives >= 12 x SMs (query head, partition) work items, i.e. ~3
 // partition CTAs per SM at a GQA group of 4; small batches get finer splits.
 // (Measured on the 8-sequence prefix workload: 256 beat both 128 and 512.)
 int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
@@ -483,7 +483,7 @@ int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
     const int64_t tokens = static_cast<int64_t>(max_blocks) * BS;
     for (int ps = 512; ps > 64; ps /= 2) {
         const int64_t parts = (tokens + ps - 1) / ps;
-        if (static_cast<int64_t>(batch) * hq * parts >= 8LL * n) return ps;
+        if (static_cast<int64_t>(batch) * hq * parts >= 12LL * n) return ps;
     }
     return 64;
 }
