@@ -300,7 +300,18 @@ class Cache:
         self.unique_blocks = len(set(int(x) for x in tables.ravel() if x >= 0))
         self.q = syn.query(w).to(device)
         self.out = torch.empty((B, Hq, D), dtype=dt, device=device)
-        self.partition_size = partition_size or pkv.pkv_decode_auto_partition_size(B, Hq, self.max_blocks)
+        # 0 = the library's automatic split: balanced over the GPU's warps for
+        # the 16-bit cache, automatic partitions for the quantised one
+        self.partition_size = partition_size
+        auto_ps = pkv.pkv_decode_auto_partition_size(B, Hq, self.max_blocks)
+        self.split = self.max_blocks * BS > (partition_size or auto_ps)
+        if not self.split:
+            self.split_desc = "single pass (one partition covers every context)"
+        elif partition_size == 0 and qmode is None and B <= 1024:
+            self.split_desc = ("balanced split-K: every warp of 4 resident 4-warp CTAs per SM "
+                               "streams an equal share of the (sequence, KV head, block) items")
+        else:
+            self.split_desc = "%d-token split-K partitions" % (partition_size or auto_ps)
         ws = pkv.pkv_decode_workspace_bytes(B, Hq, D, self.max_blocks, BS, self.partition_size)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
@@ -357,8 +368,7 @@ class Cache:
                                              self.partition_size, stream)
 
     def launches_per_step(self):
-        split = self.max_blocks * 16 > self.partition_size
-        return (2 if split else 1) + (1 if self.qmode else 0)
+        return (2 if self.split else 1) + (1 if self.qmode else 0)
 
 
 def run_device(args, rank, world, dist):
@@ -407,7 +417,8 @@ def run_device(args, rank, world, dist):
 
     return dict(ms_per_step=ms_per_step, call_ms=call_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
                 B=cache.B, launches=cache.launches_per_step() * args.steps,
-                unique_blocks=cache.unique_blocks, partition_size=cache.partition_size)
+                unique_blocks=cache.unique_blocks, partition_size=cache.partition_size,
+                split_desc=cache.split_desc)
 
 
 def run_e2e(pkv, torch, cache, steps, dist, device):
@@ -615,17 +626,16 @@ def cpu_baseline(name, min_seconds):
     }
 
 
-def config_block(name, B, kv_bytes, partition_size):
+def config_block(name, B, kv_bytes, partition_size, split_desc):
     step = ("quantised KV-append of 1 token per sequence + paged decode over the quantised "
             "cache (split-K partials, merge kernel)" if WORKLOADS[name][2] else
             "KV-append of 1 token per sequence fused into the paged decode (split-K "
             "partials, then a merge kernel with programmatic dependent launch)")
     return {
-        "workload": "%s: %s; step = %s, %d-token partitions" % (name, DESCRIPTIONS[name], step,
-                                                              partition_size),
+        "workload": "%s: %s; step = %s; %s" % (name, DESCRIPTIONS[name], step, split_desc),
         "batch": B,
         "kv_bytes_per_step": kv_bytes,
-        "partition_size": partition_size,
+        "partition_size": partition_size or "auto",
         "l2": ("inputs larger than L2 (%.0f MB of KV read per step vs 129 MB L2), no flush"
                % (kv_bytes / 1e6)) if kv_bytes > 129e6 else
               ("KV working set %.0f MB fits the 129 MB L2: numbers are L2-resident"
@@ -675,13 +685,16 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16" if not quant else ("bf16 q, u4 KV codes" if quant == "int4" else "bf16 q, e4m3 KV codes"),
         "data": "synthetic",
-        "config": config_block(args.workload, res["B"], res["kv_bytes"], res["partition_size"]),
+        "config": config_block(args.workload, res["B"], res["kv_bytes"], res["partition_size"],
+                               res["split_desc"]),
         "seq_per_s_per_layer": round(res["B"] * world / (res["ms_per_step"] * 1e-3), 1),
         "pct_of_8tbs_nominal": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),
         "roofline": {
             "bound": "hbm",
             "kernel": ("kv_append_quant + paged_decode_quant_kernel + merge_kernel" if quant else
+                       "paged_decode_balanced_kernel<bf16, 128, fused append> + merge_balanced_kernel"
+                       if "balanced" in res["split_desc"] else
                        "paged_decode_kernel<bf16, 128, partials, fused append> + merge_kernel"),
             "achieved": round(achieved, 1),
             "peak": peak,
@@ -736,7 +749,8 @@ def run_reference(args, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": config_block(args.workload, S, kvb, args.partition_size),
+        "config": config_block(args.workload, S, kvb, args.partition_size,
+                               "the oracle has no split: plain softmax per (sequence, query head)"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
                          "sample": "float64 NumPy oracle paged decode of %d sequence(s) of the "
                                    "workload (%d tokens, all 32 query heads) per step" % (S, toks)},

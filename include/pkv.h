@@ -174,22 +174,30 @@ int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
 /* ================================================================ sizes */
 
 /* Bytes of the split-K workspace pkv_paged_attention_decode* needs for this
- * shape: fp32 partial outputs [batch, num_q_heads, P, head_dim] and fp32
- * (max, sum) pairs [batch, num_q_heads, P, 2], P = ceil(max_blocks *
- * block_size / partition_size).  partition_size 0 selects the automatic size
- * (pkv_decode_auto_partition_size); otherwise it must be a positive multiple
- * of block_size.  Zero when a
- * single partition covers max_blocks * block_size (single-pass decode). */
+ * shape.  Zero when a single partition covers max_blocks * block_size
+ * (single-pass decode).
+ *   - partition_size > 0 (a positive multiple of block_size): fixed
+ *     partitions, fp32 partial outputs [batch, num_q_heads, P, head_dim] and
+ *     fp32 (max, sum) pairs [batch, num_q_heads, P, 2], P = ceil(max_blocks *
+ *     block_size / partition_size).
+ *   - partition_size 0 (automatic): the same for the automatic partition
+ *     size (pkv_decode_auto_partition_size), or, when the automatic split
+ *     may be balanced (batch <= 1024 and batch * num_q_heads * max_blocks >=
+ *     32 * 16 * SMs), the larger of that and the balanced split's need:
+ *     (nwt * 8 + batch * num_q_heads) * (head_dim + 2) * 4 bytes,
+ *     nwt = min(16 * SMs, batch * num_q_heads * max_blocks / 2)
+ *     launched warps (SMs of the current device, 152 if none). */
 int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                int32_t max_blocks, int32_t block_size, int32_t partition_size,
                                size_t* out);
 
-/* The partition size a decode call uses when it is passed partition_size 0:
- * the largest of 512, 256, 128, 64 tokens for which batch * num_q_heads *
- * ceil(max_blocks * block_size / size) >= 12 * (SM count of the current
- * device, 152 if none), else 64.  Small batches get finer splits so the GPU
- * has enough partition CTAs.  pkv_decode_workspace_bytes with partition_size 0
- * applies the same rule. */
+/* The partition size of an automatic split that is not balanced (see
+ * pkv_paged_attention_decode), of the quantised decode with partition_size
+ * 0, and of _partials / _merge with partition_size 0: the largest of 512,
+ * 256, 128, 64 tokens for which batch * num_q_heads * ceil(max_blocks *
+ * block_size / size) >= 12 * (SM count of the current device, 152 if none),
+ * else 64.  Small batches get finer splits so the GPU has enough partition
+ * CTAs. */
 int pkv_decode_auto_partition_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                                    int32_t block_size, int32_t* out);
 
@@ -209,14 +217,21 @@ int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int
  * block_tables[b, t / block_size], offset t % block_size, KV head
  * h / (num_q_heads / num_kv_heads).  fp32 accumulation; out has q's dtype;
  * a sequence with context 0 gets zeros.
- * The context is cut into partitions of partition_size tokens (0 = automatic)
- * processed by independent CTAs; when more than one partition can occur
- * (max_blocks * block_size > partition_size) partial (max, sum, output)
- * triples go to `workspace` (device, >= pkv_decode_workspace_bytes) and a
- * second kernel, launched behind the first with programmatic dependent
- * launch, merges them with a log-sum-exp rescale (flash-decoding split-K);
- * otherwise one pass writes out directly.  Calls that share a workspace must
- * not overlap on the GPU.
+ * Split-K: when more than one partition can occur (max_blocks * block_size
+ * > the partition size) partial (max, sum, output) triples go to
+ * `workspace` (device, >= pkv_decode_workspace_bytes) and a second kernel,
+ * launched behind the first with programmatic dependent launch, merges them
+ * with a log-sum-exp rescale (flash-decoding split-K); otherwise one pass
+ * writes out directly.
+ *   - partition_size > 0: the context is cut into partitions of that many
+ *     tokens, one CTA each.
+ *   - partition_size 0 (automatic): if batch <= 1024 and batch *
+ *     num_kv_heads * max_blocks is at least 32 items per launched warp
+ *     (16 warps per SM) and below 2^30, a balanced split: the (sequence, KV
+ *     head, block) items of the call, in that order, are cut into one
+ *     contiguous, equal share per warp, whatever the mix of context
+ *     lengths; else partitions of pkv_decode_auto_partition_size tokens.
+ * Calls that share a workspace must not overlap on the GPU.
  * Supported: block_size 16, head_dim 64 or 128, 1 <= num_q_heads /
  * num_kv_heads <= 8 (else UNSUPPORTED). */
 int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_pool,
@@ -248,9 +263,12 @@ int pkv_paged_attention_decode_append(const void* q, const void* k_new, const vo
                                       size_t workspace_bytes, int32_t partition_size, int dtype,
                                       void* stream);
 
-/* The two phases of pkv_paged_attention_decode, for callers that time or
- * overlap them.  _partials always writes the workspace (never out);
- * _merge reads it and writes out.  Same arguments and requirements. */
+/* The two phases of a partitioned pkv_paged_attention_decode, for callers
+ * that time or overlap them.  _partials always writes the workspace (never
+ * out); _merge reads it and writes out.  Same arguments and requirements,
+ * except that partition_size 0 means the automatic partition size
+ * (pkv_decode_auto_partition_size), never the balanced split; size the
+ * workspace with that partition size. */
 int pkv_paged_attention_decode_partials(const void* q, const void* k_pool, const void* v_pool,
                                         const int32_t* block_tables, const int32_t* context_lens,
                                         int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,

@@ -55,6 +55,9 @@ namespace {
 constexpr int BS = 16;  // tokens per block (the kernels are specialised to 16)
 constexpr int kNW = 4;  // warps per CTA (4 beat 8 in a sweep on the 64-sequence layer)
 constexpr float kLog2e = 1.4426950408889634f;
+// Headroom (log2 units) a logit may rise above the running reference max
+// before the online softmax rescales: weights stay <= 2^8.
+constexpr float kSlack = 8.f;
 
 enum Mode { kSingle = 0, kPartials = 1 };
 
@@ -90,7 +93,7 @@ struct MergeAcc {
     float M, L, acc;
 };
 
-__device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml,
+__device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml, int64_t stride_ml,
                                                 const float* __restrict__ ov, int64_t stride_o,
                                                 int q0, int np, int step) {
     MergeAcc r{neg_inf(), 0.f, 0.f};
@@ -100,8 +103,8 @@ __device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml,
         for (int j = 0; j < 8; ++j) {
             const int q = qa + j * step;
             const bool v = q < np;
-            mq[j] = v ? __ldcg(ml + 2 * q) : neg_inf();
-            lq[j] = v ? __ldcg(ml + 2 * q + 1) : 0.f;
+            mq[j] = v ? __ldcg(ml + q * stride_ml) : neg_inf();
+            lq[j] = v ? __ldcg(ml + q * stride_ml + 1) : 0.f;
             oq[j] = v ? __ldcg(ov + q * stride_o) : 0.f;
         }
         float mx = r.M;
@@ -122,6 +125,16 @@ __device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml,
     return r;
 }
 
+// Whether P enters the PV product as two 16-bit terms (value + residual).
+template <typename T>
+constexpr bool kSplitP = false;
+template <>
+constexpr bool kSplitP<__nv_bfloat16> = true;
+
+// The bf16 halves of a packed pair, as floats (exact).
+__device__ __forceinline__ float lo_float(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float hi_float(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
 // Online-softmax state of one warp for the query heads 2c, 2c+1 of its lanes.
 template <int MT>
 struct WarpState {
@@ -129,12 +142,53 @@ struct WarpState {
     float o[MT][4];
 };
 
+// 16-byte shared-memory load at a shared-window address, kept in place (not
+// hoisted out of the block loop, so the query fragments cost no registers).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+// Query fragment sources for attend_block: registers, or this warp's
+// shared slice re-read for every block (16 fewer live registers).
+template <int KC>
+struct QRegs {
+    uint4 f[KC];
+    __device__ __forceinline__ uint4 get(int i) const { return f[i]; }
+};
+struct QShared {
+    uint32_t addr;
+    __device__ __forceinline__ uint4 get(int i) const { return lds128(addr + i * 512); }
+};
+
+// Q^T B-fragments of KV head kvh's query group, staged in this warp's
+// shared slice: lane (g, c) holds query head g's columns [32i + 8c, +8) at
+// slot[i * 32] (zero for g >= G).  Returns the lane's shared address.
+template <typename T, int D>
+__device__ __forceinline__ uint32_t stage_query(const DecodeArgs& a, int b, int kvh, int g, int c,
+                                                uint4* slot) {
+    constexpr int KC = D / 32;
+    if (g < a.G) {
+        const T* qrow = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * a.G + g) * D;
+#pragma unroll
+        for (int i = 0; i < KC; ++i) slot[i * 32] = *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * c);
+    } else {
+#pragma unroll
+        for (int i = 0; i < KC; ++i) slot[i * 32] = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    return static_cast<uint32_t>(__cvta_generic_to_shared(slot));
+}
+
 // Attend one 16-token block (physical id `phys`, logical index lb) into the
 // warp state.  INJECT: row app_off of the block is the decode step's new row;
 // it is taken from the inputs (and stored to the pool) instead of the loads.
-template <typename T, int D, bool INJECT>
+template <typename T, int D, bool INJECT, typename QS>
 __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh, int lb, int phys,
-                                             int ctx, int app_off, const uint4 (&qf)[D / 32],
+                                             int ctx, int app_off, const QS& qs,
                                              WarpState<D / 16>& w, int g, int c) {
     using H = Half16<T>;
     constexpr int KC = D / 32;
@@ -201,10 +255,11 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
     float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < KC; ++i) {
+        const uint4 qf = qs.get(i);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             H::mma(s, word(kr0[i], 2 * e), word(kr1[i], 2 * e), word(kr0[i], 2 * e + 1),
-                   word(kr1[i], 2 * e + 1), word(qf[i], 2 * e), word(qf[i], 2 * e + 1));
+                   word(kr1[i], 2 * e + 1), word(qf, 2 * e), word(qf, 2 * e + 1));
         }
     }
     const int tok0 = lb * BS + g;
@@ -214,31 +269,49 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
     const float x2 = ok1 ? s[2] * a.scale_log2 : neg_inf();
     const float x3 = ok1 ? s[3] * a.scale_log2 : neg_inf();
 
-    // ---- online softmax (base 2); heads 2c (x0, x2) and 2c+1 (x1, x3)
-    float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+    // ---- online softmax (base 2); heads 2c (x0, x2) and 2c+1 (x1, x3).
+    // The reference max m is raised only when a logit of this block exceeds
+    // it by more than kSlack; otherwise the weights 2^(x - m) <= 2^kSlack are
+    // taken against the old m, skipping the warp-wide max and the rescale of
+    // o and l (any reference works: m cancels in o / l and in the merges).
+    const float bx0 = fmaxf(x0, x2), bx1 = fmaxf(x1, x3);
+    if (__any_sync(0xffffffffu, bx0 > w.m0 + kSlack || bx1 > w.m1 + kSlack)) {
+        float bm0 = bx0, bm1 = bx1;
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-    }
-    const float mn0 = fmaxf(w.m0, bm0), mn1 = fmaxf(w.m1, bm1);
-    const float al0 = ex2(w.m0 - mn0), al1 = ex2(w.m1 - mn1);
-    const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-    const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-    w.l0 = w.l0 * al0 + (p0 + p2);
-    w.l1 = w.l1 * al1 + (p1 + p3);
-    w.m0 = mn0;
-    w.m1 = mn1;
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(w.m0, bm0), mn1 = fmaxf(w.m1, bm1);
+        const float al0 = ex2(w.m0 - mn0), al1 = ex2(w.m1 - mn1);
+        w.l0 *= al0;
+        w.l1 *= al1;
+        w.m0 = mn0;
+        w.m1 = mn1;
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        w.o[mt][0] *= al0;
-        w.o[mt][1] *= al1;
-        w.o[mt][2] *= al0;
-        w.o[mt][3] *= al1;
+        for (int mt = 0; mt < MT; ++mt) {
+            w.o[mt][0] *= al0;
+            w.o[mt][1] *= al1;
+            w.o[mt][2] *= al0;
+            w.o[mt][3] *= al1;
+        }
     }
-    // P^T B-fragments: transpose the two 8x8 (token x head) halves.
-    const uint32_t pb0 = movmatrix_trans(H::pack(p0, p1));
-    const uint32_t pb1 = movmatrix_trans(H::pack(p2, p3));
+    const float p0 = ex2(x0 - w.m0), p1 = ex2(x1 - w.m1);
+    const float p2 = ex2(x2 - w.m0), p3 = ex2(x3 - w.m1);
+    w.l0 += p0 + p2;
+    w.l1 += p1 + p3;
+    // P^T B-fragments: transpose the two 8x8 (token x head) halves.  bf16
+    // keeps 8 bits of P, which alone can move a short context's output by
+    // ~2e-3; there P also goes in as a second bf16 term, its rounding
+    // residual, so the products see ~16 bits of P (fp16's 11 suffice).
+    const uint32_t h01 = H::pack(p0, p1), h23 = H::pack(p2, p3);
+    const uint32_t pb0 = movmatrix_trans(h01);
+    const uint32_t pb1 = movmatrix_trans(h23);
+    uint32_t pr0 = 0, pr1 = 0;
+    if constexpr (kSplitP<T>) {
+        pr0 = movmatrix_trans(H::pack(p0 - lo_float(h01), p1 - hi_float(h01)));
+        pr1 = movmatrix_trans(H::pack(p2 - lo_float(h23), p3 - hi_float(h23)));
+    }
 
     if (lb * BS + BS > ctx) {  // last, partial block: zero masked V rows
         const int t0 = lb * BS;
@@ -265,7 +338,58 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
         const uint32_t a2 = __byte_perm(word(vr[2][jl], wl), word(vr[3][jl], wl), sl);
         const uint32_t a3 = __byte_perm(word(vr[2][jh], wh), word(vr[3][jh], wh), sh);
         H::mma(w.o[mt], a0, a1, a2, a3, pb0, pb1);
+        if constexpr (kSplitP<T>) H::mma(w.o[mt], a0, a1, a2, a3, pr0, pr1);
     }
+}
+
+// Merge the NW warps' online-softmax states of one CTA through shared memory
+// and pass each query head h < G, column d result -- unnormalised output
+// acc, max M, sum L -- to store(h, d, acc, M, L).  Ends with a barrier, so
+// the shared arrays may be reused right after.
+template <int D, int NW, typename Store>
+__device__ __forceinline__ void cta_merge(const WarpState<D / 16>& ws, int warp, int g, int c, int G,
+                                          float (&sm_ml)[NW][8][2], float (&sm_o)[NW][8][D],
+                                          Store store) {
+    constexpr int MT = D / 16;
+    float l0 = ws.l0, l1 = ws.l1;
+    // finish the per-lane partial sums over the 8 token lanes
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (g == 0) {
+        sm_ml[warp][2 * c][0] = ws.m0;
+        sm_ml[warp][2 * c][1] = l0;
+        sm_ml[warp][2 * c + 1][0] = ws.m1;
+        sm_ml[warp][2 * c + 1][1] = l1;
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int dl = pv_col(mt, g), dh = pv_col(mt + D / 16, g);
+        sm_o[warp][2 * c][dl] = ws.o[mt][0];
+        sm_o[warp][2 * c + 1][dl] = ws.o[mt][1];
+        sm_o[warp][2 * c][dh] = ws.o[mt][2];
+        sm_o[warp][2 * c + 1][dh] = ws.o[mt][3];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += NW * 32) {
+        const int h = idx / D, d = idx - h * D;
+        float M = neg_inf();
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_ml[w][h][0]);
+        float acc = 0.f, L = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float sc = ex2(sm_ml[w][h][0] - M);
+                acc += sc * sm_o[w][h][d];
+                L += sc * sm_ml[w][h][1];
+            }
+        }
+        store(h, d, acc, M, L);
+    }
+    __syncthreads();
 }
 
 template <typename T, int D, int NW, int MODE, bool APPEND>
@@ -316,15 +440,8 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
     }
 
     // Q^T B-fragments: lane (g, c) holds query head g's columns [32i + 8c, +8).
-    uint4 qf[KC];
-    if (g < a.G) {
-        const T* qrow = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * a.G + g) * D;
-#pragma unroll
-        for (int i = 0; i < KC; ++i) qf[i] = *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * c);
-    } else {
-#pragma unroll
-        for (int i = 0; i < KC; ++i) qf[i] = make_uint4(0, 0, 0, 0);
-    }
+    __shared__ uint4 sm_q[NW][KC][32];
+    const QShared qs{stage_query<T, D>(a, b, kvh, g, c, &sm_q[warp][0][lane])};
 
     WarpState<MT> ws;
     ws.m0 = ws.m1 = neg_inf();
@@ -346,56 +463,16 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
             if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
             continue;
         }
-        attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qf, ws, g, c);
+        attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qs, ws, g, c);
     }
     if constexpr (APPEND) {
         if (lb == app_lb) {  // app_lb was validated above
-            attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qf, ws, g, c);
+            attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qs, ws, g, c);
         }
     }
-    float m0 = ws.m0, m1 = ws.m1, l0 = ws.l0, l1 = ws.l1;
-    auto& o = ws.o;
-
-    // finish the per-lane partial sums over the 8 token lanes
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-
-    // ---- merge the NW warps of the CTA
     __shared__ float sm_ml[NW][8][2];
     __shared__ float sm_o[NW][8][D];
-    if (g == 0) {
-        sm_ml[warp][2 * c][0] = m0;
-        sm_ml[warp][2 * c][1] = l0;
-        sm_ml[warp][2 * c + 1][0] = m1;
-        sm_ml[warp][2 * c + 1][1] = l1;
-    }
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const int dl = pv_col(mt, g), dh = pv_col(mt + D / 16, g);
-        sm_o[warp][2 * c][dl] = o[mt][0];
-        sm_o[warp][2 * c + 1][dl] = o[mt][1];
-        sm_o[warp][2 * c][dh] = o[mt][2];
-        sm_o[warp][2 * c + 1][dh] = o[mt][3];
-    }
-    __syncthreads();
-
-    for (int idx = threadIdx.x; idx < a.G * D; idx += NW * 32) {
-        const int h = idx / D, d = idx - h * D;
-        float M = neg_inf();
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_ml[w][h][0]);
-        float acc = 0.f, L = 0.f;
-        if (M != neg_inf()) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) {
-                const float sc = ex2(sm_ml[w][h][0] - M);
-                acc += sc * sm_o[w][h][d];
-                L += sc * sm_ml[w][h][1];
-            }
-        }
+    cta_merge<D, NW>(ws, warp, g, c, a.G, sm_ml, sm_o, [&](int h, int d, float acc, float M, float L) {
         const int64_t qh = static_cast<int64_t>(b) * a.hq + kvh * a.G + h;
         if constexpr (MODE == kSingle) {
             static_cast<T*>(a.out)[qh * D + d] = H::from_float(L > 0.f ? acc / L : 0.f);
@@ -407,8 +484,263 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
                 a.ws_ml[2 * row + 1] = L;
             }
         }
+    });
+}
+
+__device__ __forceinline__ int blocks_of(int ctx, int cap) {
+    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+    return (ctx + BS - 1) / BS;
+}
+
+// First warp of a balanced split whose range holds item x: the largest i
+// with floor(i W / nwt) <= x.
+__device__ __forceinline__ int64_t first_warp(int64_t x, int64_t W, int64_t nwt) {
+    return ((x + 1) * nwt - 1) / W;
+}
+
+// Balanced split-K ("stream-K" over block-heads).  The work of one call is
+// the ordered list of (sequence, KV head, logical block) items, sequence-
+// major, then KV head, then block: W = Hkv * sum_b nblk_b items.  Warp i of
+// nwt = min(launched warps, W / min_items) takes the contiguous range
+// [i W / nwt, (i + 1) W / nwt), so every warp streams the same number of
+// blocks whatever the mix of context lengths: no wave quantisation, no short
+// last partitions, one prologue per warp, and no barrier anywhere.  A warp
+// writes one fp32 partial (m, l, o) per (sequence, KV head) run it touches,
+// at slot i + b * Hkv + kvh: the warps touching one run are consecutive and
+// every range is non-empty, so slots never collide.
+template <typename T, int D, bool APPEND>
+__global__ void __launch_bounds__(kNW * 32, 16 / kNW)
+    paged_decode_balanced_kernel(DecodeArgs a, int batch, int nwt_launch, int min_items) {
+    constexpr int KC = D / 32;
+    constexpr int MT = D / 16;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    // the merge grid may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ __align__(16) float sm_o[kNW][8][D];
+    __shared__ uint4 sm_q[kNW][KC][32];
+
+    // every warp counts the items (the host keeps batch * Hkv * max_blocks
+    // below 2^30)
+    const int cap = a.max_blocks * BS;
+    int mine = 0;
+    bool bad = false;
+    for (int j = lane; j < batch; j += 32) {
+        const int x = a.ctx_lens[j];
+        bad |= x < 0 || x > cap;
+        mine += blocks_of(x, cap);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+    const int W = mine * a.hkv;
+    const int nwt = max(min(W / min_items, nwt_launch), 1);
+    const int i = blockIdx.x * kNW + warp;
+
+    if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+    if (W == 0 || i >= nwt) return;
+    const int S = static_cast<int>(static_cast<int64_t>(i) * W / nwt);
+    const int E = static_cast<int>(static_cast<int64_t>(i + 1) * W / nwt);
+
+    // the sequence holding item S: its first item (cs) and block count (nb)
+    int b = 0, nb = 0, cs = 0;
+    {
+        int run = 0;
+        for (int base = 0; base < batch; base += 32) {
+            const int j = base + lane;
+            const int nbj = j < batch ? blocks_of(a.ctx_lens[j], cap) : 0;
+            int incl = nbj;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, j < batch && S < (run + incl) * a.hkv);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                b = base + src;
+                nb = __shfl_sync(0xffffffffu, nbj, src);
+                cs = (run + __shfl_sync(0xffffffffu, incl - nbj, src)) * a.hkv;
+                break;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
     }
 
+    for (int pos = S; pos < E;) {
+        while (pos >= cs + nb * a.hkv) {  // next non-empty sequence
+            cs += nb * a.hkv;
+            ++b;
+            nb = blocks_of(a.ctx_lens[b], cap);
+        }
+        const int ctx = min(max(a.ctx_lens[b], 0), cap);
+        const int kvh = (pos - cs) / nb;
+        const int lb0 = pos - cs - kvh * nb;
+        const int lb1 = min(nb, lb0 + (E - pos));
+        pos += lb1 - lb0;
+        const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+
+        // fused append: the new row is at ctx - 1, in the run's last block
+        int app_lb = -1, app_off = 0;
+        if constexpr (APPEND) {
+            if (lb1 == nb) {
+                const int64_t slot = a.slots[b];
+                if (slot >= 0) {
+                    const int phys = trow[nb - 1], off = (ctx - 1) % BS;
+                    if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks) &&
+                        slot == static_cast<int64_t>(phys) * BS + off) {
+                        app_lb = nb - 1;
+                        app_off = off;
+                    } else if (lane == 0) {
+                        atomicOr(a.status, PKV_STATUS_BAD_SLOT);
+                    }
+                }
+            }
+        }
+
+        __syncwarp();  // the previous run's query fragments are no longer read
+        const QShared qs{stage_query<T, D>(a, b, kvh, g, c, &sm_q[warp][0][lane])};
+        WarpState<MT> ws;
+        ws.m0 = ws.m1 = neg_inf();
+        ws.l0 = ws.l1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) ws.o[mt][0] = ws.o[mt][1] = ws.o[mt][2] = ws.o[mt][3] = 0.f;
+
+        // the appended block is the run's last: attended after the loop
+        int tab = 0, k = 0, lb = lb0;
+        for (; lb < lb1 && lb != app_lb; ++k, ++lb) {
+            if ((k & 31) == 0) {  // physical ids of the next 32 blocks of the run
+                const int idx = lb + lane;
+                tab = idx < lb1 ? trow[idx] : 0;
+            }
+            const int phys = __shfl_sync(0xffffffffu, tab, k & 31);
+            if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+                if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+                continue;
+            }
+            attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qs, ws, g, c);
+        }
+        if constexpr (APPEND) {
+            if (lb == app_lb) attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qs, ws, g, c);
+        }
+
+        float l0 = ws.l0, l1 = ws.l1;
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        // partial (m, l, o) of this run: o staged through shared memory so
+        // the G x D rows go out in 16-byte stores
+        __syncwarp();
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int dl = pv_col(mt, g), dh = pv_col(mt + D / 16, g);
+            sm_o[warp][2 * c][dl] = ws.o[mt][0];
+            sm_o[warp][2 * c + 1][dl] = ws.o[mt][1];
+            sm_o[warp][2 * c][dh] = ws.o[mt][2];
+            sm_o[warp][2 * c + 1][dh] = ws.o[mt][3];
+        }
+        __syncwarp();
+        const int64_t slot = i + b * a.hkv + kvh;
+        float4* po = reinterpret_cast<float4*>(a.ws_o + slot * a.G * D);
+        const float4* so = reinterpret_cast<const float4*>(&sm_o[warp][0][0]);
+        for (int x = lane; x < a.G * D / 4; x += 32) po[x] = so[x];
+        if (g == 0) {
+            float* pml = a.ws_ml + slot * a.G * 2;
+            if (2 * c < a.G) {
+                pml[4 * c] = ws.m0;
+                pml[4 * c + 1] = l0;
+            }
+            if (2 * c + 1 < a.G) {
+                pml[4 * c + 2] = ws.m1;
+                pml[4 * c + 3] = l1;
+            }
+        }
+    }
+}
+
+// Merge of a balanced split for one (sequence, query head): the partials of
+// the consecutive warps whose ranges met the (sequence, KV head) run, folded
+// as in merge_kernel.  Launched behind the balanced kernel with programmatic
+// dependent launch.
+template <typename T, int D, int PG>
+__global__ void __launch_bounds__(D * PG) merge_balanced_kernel(
+    const int32_t* __restrict__ ctx_lens, int batch, int hq, int hkv, int max_blocks,
+    int nwt_launch, int min_items, const float* __restrict__ ws_o,
+    const float* __restrict__ ws_ml, T* __restrict__ out) {
+    constexpr int NT = D * PG, NWARP = NT / 32;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int d = threadIdx.x % D, pg = threadIdx.x / D;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int G = hq / hkv, kvh = h / G, hl = h - kvh * G;
+    const int cap = max_blocks * BS;
+    // Where the run sits among the items follows from the context lengths
+    // alone -- inputs of the call, not outputs of the decode grid -- so it is
+    // worked out before the wait: the blocks of the sequences before b and
+    // of all sequences.
+    int before = 0, total = 0;
+    for (int j = threadIdx.x; j < batch; j += NT) {
+        const int nbj = blocks_of(ctx_lens[j], cap);
+        total += nbj;
+        before += j < b ? nbj : 0;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        total += __shfl_xor_sync(0xffffffffu, total, off);
+        before += __shfl_xor_sync(0xffffffffu, before, off);
+    }
+    __shared__ int red[2][NWARP];
+    if (lane == 0) {
+        red[0][warp] = total;
+        red[1][warp] = before;
+    }
+    __syncthreads();
+    total = before = 0;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) {
+        total += red[0][w];
+        before += red[1][w];
+    }
+    const int nb = blocks_of(ctx_lens[b], cap);
+    T* o = out + (static_cast<int64_t>(b) * hq + h) * D + d;
+    // partials are produced by the preceding grid: wait for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (nb == 0) {
+        if (pg == 0) *o = Half16<T>::from_float(0.f);
+        return;
+    }
+    const int W = total * hkv;
+    const int nwt = max(min(W / min_items, nwt_launch), 1);
+    const int S = before * hkv + kvh * nb;
+    const int64_t i0 = first_warp(S, W, nwt), i1 = first_warp(S + nb - 1, W, nwt);
+    const int np = static_cast<int>(i1 - i0 + 1);
+    const int64_t slot0 = i0 + static_cast<int64_t>(b) * hkv + kvh;
+    const MergeAcc r = merge_range(ws_ml + (slot0 * G + hl) * 2, 2 * G, ws_o + (slot0 * G + hl) * D + d,
+                                   static_cast<int64_t>(G) * D, pg, np, PG);
+    if constexpr (PG == 1) {
+        *o = Half16<T>::from_float(r.L > 0.f ? r.acc / r.L : 0.f);
+        return;
+    }
+    __shared__ float sm[3][PG][D];
+    sm[0][pg][d] = r.M;
+    sm[1][pg][d] = r.L;
+    sm[2][pg][d] = r.acc;
+    __syncthreads();
+    if (pg == 0) {
+        float M = neg_inf();
+#pragma unroll
+        for (int j = 0; j < PG; ++j) M = fmaxf(M, sm[0][j][d]);
+        float L = 0.f, acc = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int j = 0; j < PG; ++j) {
+                const float w = ex2(sm[0][j][d] - M);
+                L += w * sm[1][j][d];
+                acc += w * sm[2][j][d];
+            }
+        }
+        *o = Half16<T>::from_float(L > 0.f ? acc / L : 0.f);
+    }
 }
 
 // Merge the partition partials of one (sequence, query head).  CTA of
@@ -432,7 +764,7 @@ __global__ void __launch_bounds__(D * PG) merge_kernel(
     // partials are produced by the preceding grid: wait for it (a no-op
     // when this grid was launched without programmatic serialization)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const MergeAcc r = merge_range(ws_ml + 2 * row0, ws_o + row0 * D + d, D, pg, np, PG);
+    const MergeAcc r = merge_range(ws_ml + 2 * row0, 2, ws_o + row0 * D + d, D, pg, np, PG);
     if constexpr (PG == 1) {
         out[(static_cast<int64_t>(b) * hq + h) * D + d] =
             Half16<T>::from_float(r.L > 0.f ? r.acc / r.L : 0.f);
@@ -462,15 +794,24 @@ __global__ void __launch_bounds__(D * PG) merge_kernel(
 
 struct Shape {
     int batch, hq, hkv, D, num_blocks, block_size, max_blocks, part_blocks, max_parts;
+    bool balanced;  // automatic split: balanced over warps instead of fixed partitions
 };
+
+// Batches up to this size use the balanced split when the partition size is
+// automatic (every warp scans the context lengths once).
+constexpr int kBalancedMaxBatch = 1024;
+// Fewest (sequence, KV head, block) items a warp of the balanced split takes.
+constexpr int kBalancedMinItems = 2;
+// The automatic split is balanced when the tables could hold this many items
+// per launched warp: below it the fixed partitions measured as fast or faster
+// (the balanced split's per-warp scan, partial rows and merge cost more than
+// the wave-quantisation they remove).
+constexpr int kBalancedItemsPerWarp = 32;
 
 }  // namespace
 
-// Automatic partition size: the largest of 512, 256, 128, 64 tokens that
-// still gives >= 12 x SMs (query head, partition) work items, i.e. ~3
-// partition CTAs per SM at a GQA group of 4; small batches get finer splits.
-// (Measured on the 8-sequence prefix workload: 256 beat both 128 and 512.)
-int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
+// SM count of the current device (152 when it cannot be queried), cached.
+int num_sms() {
     static std::atomic<int> sms{0};
     int n = sms.load();
     if (n == 0) {
@@ -480,12 +821,48 @@ int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
             n = 152;
         sms.store(n);
     }
+    return n;
+}
+
+// Automatic partition size: the largest of 512, 256, 128, 64 tokens that
+// still gives >= 12 x SMs (query head, partition) work items, i.e. ~3
+// partition CTAs per SM at a GQA group of 4; small batches get finer splits.
+// (Measured on the 8-sequence prefix workload: 256 beat both 128 and 512.)
+int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
+    const int n = num_sms();
     const int64_t tokens = static_cast<int64_t>(max_blocks) * BS;
     for (int ps = 512; ps > 64; ps /= 2) {
         const int64_t parts = (tokens + ps - 1) / ps;
         if (static_cast<int64_t>(batch) * hq * parts >= 12LL * n) return ps;
     }
     return 64;
+}
+
+// Warps a balanced split launches: 4 CTAs of 4 warps per SM, all resident at
+// once, but no more than the largest possible item count allows at
+// kBalancedMinItems each, so small problems launch (and need room for) fewer.
+int balanced_warps(int64_t max_items) {
+    const int64_t full = num_sms() * 16LL;
+    const int64_t n = max_items / kBalancedMinItems < full ? max_items / kBalancedMinItems : full;
+    return n < 1 ? 1 : static_cast<int>(n);
+}
+
+// Whether an automatic split may be balanced for this many items at most
+// (the tables' capacity), and whether it is (else fixed partitions).
+bool balanced_candidate(int64_t batch, int64_t max_items) {
+    return batch <= kBalancedMaxBatch &&
+           max_items >= static_cast<int64_t>(kBalancedItemsPerWarp) * num_sms() * 16;
+}
+bool use_balanced(int64_t batch, int64_t hkv, int64_t max_blocks) {
+    const int64_t items = batch * hkv * max_blocks;
+    return balanced_candidate(batch, items) && items < (1LL << 30);
+}
+
+// Bytes of a balanced split's workspace: nwt * G + batch * hq partial rows
+// of D + 2 floats (o, then (m, l)).
+size_t balanced_bytes(int32_t batch, int32_t hq, int32_t G, int32_t D, int32_t nwt) {
+    const size_t rows = static_cast<size_t>(nwt) * G + static_cast<size_t>(batch) * hq;
+    return rows * (D + 2) * sizeof(float);
 }
 
 namespace {
@@ -500,6 +877,7 @@ int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_b
     if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
     if (block_size != BS || (D != 64 && D != 128) || hq / hkv > 8) return PKV_ERR_UNSUPPORTED;
     if (batch > 65535 || hkv > 65535) return PKV_ERR_UNSUPPORTED;
+    s->balanced = partition_size == 0 && use_balanced(batch, hkv, max_blocks);
     if (partition_size == 0) partition_size = auto_partition_size(batch, hq, max_blocks);
     if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
     s->batch = batch;
@@ -534,6 +912,56 @@ int dispatch(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
     }
     if (s.D == 128) return launch_kernel<__half, 128, MODE, APPEND>(a, s, st);
     return launch_kernel<__half, 64, MODE, APPEND>(a, s, st);
+}
+
+template <typename T, int D, bool APPEND>
+int launch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, cudaStream_t st) {
+    paged_decode_balanced_kernel<T, D, APPEND>
+        <<<(nwt + kNW - 1) / kNW, kNW * 32, 0, st>>>(a, s.batch, nwt, min_items);
+    return launch_status();
+}
+
+template <typename T, int D, int PG>
+int launch_merge_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items,
+                          cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(s.hq, s.batch);
+    cfg.blockDim = dim3(D * PG);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_balanced_kernel<T, D, PG>, a.ctx_lens, s.batch,
+                                             s.hq, s.hkv, s.max_blocks, nwt, min_items,
+                                             static_cast<const float*>(a.ws_o),
+                                             static_cast<const float*>(a.ws_ml), static_cast<T*>(a.out));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Balanced split: the warp-range kernel, then its merge.  Runs of one
+// (sequence, KV head) span about nwt / (batch * Hkv) warp ranges at the
+// longest; beyond 16 the merge folds with 4 partial groups per CTA.
+template <typename T, int D, bool APPEND>
+int run_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, cudaStream_t st) {
+    int r = launch_balanced<T, D, APPEND>(a, s, nwt, min_items, st);
+    if (r != PKV_OK) return r;
+    const bool many = nwt > 16LL * s.batch * s.hkv;
+    return many ? launch_merge_balanced<T, D, 4>(a, s, nwt, min_items, st)
+                : launch_merge_balanced<T, D, 1>(a, s, nwt, min_items, st);
+}
+
+template <bool APPEND>
+int dispatch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, int dtype,
+                      cudaStream_t st) {
+    if (dtype == PKV_DTYPE_BF16) {
+        if (s.D == 128) return run_balanced<__nv_bfloat16, 128, APPEND>(a, s, nwt, min_items, st);
+        return run_balanced<__nv_bfloat16, 64, APPEND>(a, s, nwt, min_items, st);
+    }
+    if (s.D == 128) return run_balanced<__half, 128, APPEND>(a, s, nwt, min_items, st);
+    return run_balanced<__half, 64, APPEND>(a, s, nwt, min_items, st);
 }
 
 // The merge grid is launched with programmatic stream serialization: it may
@@ -609,8 +1037,9 @@ int set_workspace(DecodeArgs* a, const Shape& s, void* ws, size_t bytes) {
     return PKV_OK;
 }
 
-// One decode call: single pass when one partition covers every table,
-// otherwise the partition kernel then the merge kernel.
+// One decode call: single pass when one partition covers every table;
+// otherwise, with the automatic split, the balanced kernel then its merge,
+// else the partition kernel then the merge kernel.
 template <bool APPEND>
 int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_bytes, int dtype,
            cudaStream_t cs) {
@@ -619,6 +1048,16 @@ int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_
     if (s.max_parts <= 1) {
         a.part_blocks = s.max_blocks > 0 ? s.max_blocks : 1;
         return dispatch<kSingle, APPEND>(a, s, dtype, cs);
+    }
+    if (s.balanced) {
+        const int nwt = balanced_warps(static_cast<int64_t>(s.batch) * s.hkv * s.max_blocks);
+        const int G = s.hq / s.hkv;
+        if (!ws || ws_bytes < balanced_bytes(s.batch, s.hq, G, s.D, nwt)) return PKV_ERR_WORKSPACE;
+        if (!aligned16(ws)) return PKV_ERR_MISALIGNED;
+        const size_t rows = static_cast<size_t>(nwt) * G + static_cast<size_t>(s.batch) * s.hq;
+        a.ws_o = static_cast<float*>(ws);
+        a.ws_ml = a.ws_o + rows * s.D;
+        return dispatch_balanced<APPEND>(a, s, nwt, kBalancedMinItems, dtype, cs);
     }
     int st = set_workspace(&a, s, ws, ws_bytes);
     if (st != PKV_OK) return st;
@@ -635,7 +1074,8 @@ extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
     if (!out || batch < 0 || num_q_heads <= 0 || head_dim <= 0 || max_blocks < 0 ||
         block_size <= 0 || partition_size < 0)
         return PKV_ERR_INVALID_ARG;
-    if (partition_size == 0) partition_size = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
+    const bool automatic = partition_size == 0;
+    if (automatic) partition_size = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
     if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
     const int64_t part_blocks = partition_size / block_size;
     const int64_t parts = (max_blocks + part_blocks - 1) / part_blocks;
@@ -643,7 +1083,18 @@ extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
         *out = 0;
         return PKV_OK;
     }
-    *out = static_cast<size_t>(batch) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+    const size_t fixed = static_cast<size_t>(batch) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
+    const int64_t max_items = static_cast<int64_t>(batch) * num_q_heads * max_blocks;  // Hkv <= Hq
+    if (automatic && pkv::balanced_candidate(batch, max_items)) {
+        // room for a balanced split (16-bit cache) with Hkv anywhere in
+        // [1, Hq] and a GQA group up to 8; the quantised decode still splits
+        // into the automatic partitions
+        const int nwt = pkv::balanced_warps(max_items);
+        const size_t bal = pkv::balanced_bytes(batch, num_q_heads, 8, head_dim, nwt);
+        *out = bal > fixed ? bal : fixed;
+        return PKV_OK;
+    }
+    *out = fixed;
     return PKV_OK;
 }
 

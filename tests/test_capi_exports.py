@@ -72,8 +72,38 @@ def test_workspace_bytes(pkv):
     assert pkv.pkv_decode_workspace_bytes(64, 32, 128, 256, 16, 512) == 64 * 32 * 8 * 130 * 4
     # one partition covers everything: single pass, no workspace
     assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 512) == 0
-    assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == 4 * 32 * 128 * 130 * 4
     assert pkv.pkv_decode_workspace_bytes(1, 3, 64, 64, 16, 512) == 3 * 2 * 66 * 4
+
+
+def _sms():
+    import torch
+    if torch.cuda.is_available():
+        return torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 152  # the library's default without a device
+
+
+def test_workspace_bytes_automatic(pkv):
+    # automatic split on tables of >= 32 items per launched warp (16 warps
+    # per SM; items = batch x Hq x max_blocks bounds batch x Hkv x blocks):
+    # room for the balanced split (partial rows for a GQA group of up to 8 per
+    # warp, one row per (sequence, query head)) and for the automatic
+    # partitions, whichever is more
+    nwt = 16 * _sms()
+    assert 4 * 32 * 4096 >= 32 * nwt
+    balanced = (nwt * 8 + 4 * 32) * 130 * 4
+    fixed = 4 * 32 * 128 * 130 * 4
+    assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == max(balanced, fixed)
+    # 300 sequences of 64k tokens: the fixed partitions dominate
+    fixed = 300 * 32 * 128 * 130 * 4
+    assert pkv.pkv_decode_workspace_bytes(300, 32, 128, 4096, 16, 0) == fixed
+    # above 1,024 sequences only the partitions are used
+    assert pkv.pkv_decode_workspace_bytes(1025, 32, 128, 64, 16, 0) == \
+        pkv.pkv_decode_workspace_bytes(1025, 32, 128, 64, 16, 512)
+    # small tables: the automatic partitions only (64 tokens here)
+    assert 3 * 8 * 19 < 32 * nwt
+    assert pkv.pkv_decode_workspace_bytes(3, 8, 128, 19, 16, 0) == 3 * 8 * 5 * 130 * 4
+    # one partition covers everything: single pass, no workspace
+    assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 0) == 0
 
 
 def test_auto_partition_size(pkv):
@@ -84,5 +114,5 @@ def test_auto_partition_size(pkv):
     assert pkv.pkv_decode_auto_partition_size(2, 32, 144) == 64
     # tiny: the smallest size (a single partition then covers it)
     assert pkv.pkv_decode_auto_partition_size(3, 8, 3) == 64
-    # the workspace for partition 0 follows the same rule
-    assert pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 0) == pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 256)
+    # the workspace for partition 0 covers the automatic partitions
+    assert pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 0) >= pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 256)
