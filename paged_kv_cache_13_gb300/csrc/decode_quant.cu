@@ -13,19 +13,25 @@
 // Design: the tensor-core layout of decode.cu (tokens as M for QK^T, head dim
 // as M for PV, the GQA group as N), with fragments built from the codes in
 // registers and the per-token scale / zero factored out of the products:
-//   QK^T: S_t = s_t * (sum_d q_d (c_td - 8) + (8 - z_t) * sum_d q_d)   INT4
-//         S_t = s_t * sum_d q_d e4m3(c_td)                             FP8
-//   PV:   O_d = sum_t W_t (c_td - 8) - sum_t W_t (z_t - 8),  W_t = P_t s_t
-// so the MMAs see exact small integers (INT4: c - 8 in [-8, 7]) or exact
-// e4m3 values, both exact in fp16, against fp16 queries / weights, with fp32
-// accumulation.
-//   INT4 nibble -> fp16: (nibble | 0x6400) is 1024 + nibble; subtracting 1032
-//   gives nibble - 8 exactly.  A 32-bit word of 8 nibbles yields four fp16
-//   pairs {d_j, d_j+4}; the k order of a k-step is permuted accordingly and
-//   the query fragment uses the same permutation.
+//   QK^T: S_t = s_t * (sum_d q_d c_td - z_t * sum_d q_d)   INT4
+//         S_t = s_t * sum_d q_d e4m3(c_td)                 FP8
+//   PV:   O_d = sum_t W_t c_td - sum_t W_t z_t,  W_t = P_t s_t
+// so the MMAs see exact code values against fp16 queries / weights, with
+// fp32 accumulation.
+//   INT4 codes -> fp16 with one AND per pair: a nibble c in the low bits of
+//   a 16-bit half is the fp16 subnormal c x 2^-24 (exact), the next nibble up
+//   is 16 c x 2^-24.  A 32-bit word of 8 nibbles yields four pairs
+//   {d_j, d_j+4}: masks 0x000F000F / 0x00F000F0 on the word and on the word
+//   shifted by 8.  The k order of a k-step is permuted accordingly; the
+//   query columns that meet the 16x nibbles go in divided by 16, and the PV
+//   accumulator columns fed by them are scaled back by 2^20 (the others by
+//   2^24) at the end.
 //   FP8 -> fp16: cvt.rn.f16x2.e4m3x2 (exact).
 //   For PV the pairs must hold two tokens of one column: a byte permute of
 //   the two token rows' words comes first.
+// Online softmax: the warp-wide block max is exact; the rescale of o, l and
+// the zero-point correction is skipped when no max changed (the usual case
+// once a few blocks are in).
 // Sink tokens (positions < n_sink <= 16, i.e. in logical block 0): their
 // logits are recomputed in fp32 from the 16-bit sink keys, their PV weights
 // are zero in the MMA, and P * sink_v is added to the accumulator directly.
@@ -37,6 +43,20 @@ namespace {
 
 constexpr int BS = 16;
 constexpr int NW = 4;
+// Blocks a warp loads before attending them: INT4 blocks are 2 KiB per
+// (block, head), two keep ~4 KiB of codes in flight per warp; FP8 blocks are
+// 4 KiB and two would not fit the 128-register budget.
+template <int QMODE>
+constexpr int kBlocksPerStep = 1;
+// INT4 runs 5 CTAs per SM (96 registers) with the query fragments re-read
+// from shared memory per block; FP8 needs its registers for the 4 KiB of
+// codes per block and keeps 4 CTAs with the query fragments in registers.
+// (Measured on the 32 x 16k workload: INT4 259 -> 242 us; FP8 unchanged or
+// slower with the INT4 settings.)
+template <int QMODE>
+constexpr int kCtasPerSm = QMODE == PKV_QMODE_INT4_ASYM ? 5 : 4;
+template <int QMODE>
+constexpr bool kQueryInShared = QMODE == PKV_QMODE_INT4_ASYM;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct QDecodeArgs {
@@ -67,11 +87,23 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
 
 __device__ __forceinline__ uint32_t f16pair(float lo, float hi) { return Half16<__half>::pack(lo, hi); }
 
-// INT4 nibble pair at bit `shift` of both 16-bit halves -> fp16 {lo - 8, hi - 8}
-__device__ __forceinline__ uint32_t nib2(uint32_t w, int shift) {
-    const uint32_t x = ((w >> shift) & 0x000F000Fu) | 0x64006400u;
-    const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), __half2half2(__ushort_as_half(0x6408)));
-    return *reinterpret_cast<const uint32_t*>(&h);
+// INT4 nibbles as fp16 subnormals: masking a 32-bit word with 0x000F000F
+// leaves the nibbles at bits 0 and 16 as the fp16 pair {n_lo, n_hi} x 2^-24,
+// exactly; the mask 0x00F000F0 leaves the next nibbles as {16 n_lo, 16 n_hi}
+// x 2^-24.  One logic op per pair, no float arithmetic: the 2^-24 (and the 16
+// of the odd nibbles) are taken out after the products.
+__device__ __forceinline__ uint32_t nib_even(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t nib_odd(uint32_t w) { return w & 0x00F000F0u; }
+constexpr float kTwo24 = 16777216.f;         // 2^24
+constexpr float kInvTwo24 = 5.9604645e-08f;  // 2^-24
+
+// 16-byte shared load, kept in place (not hoisted out of the block loop).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
 }
 
 // two e4m3 codes in the low 16 bits of w -> fp16 pair (low byte -> low half)
@@ -87,8 +119,8 @@ __device__ __forceinline__ float tofloat(T x) {
     return Half16<T>::to_float(x);
 }
 
-template <typename T, int D, int QMODE, bool SPLIT>
-__global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeArgs a) {
+template <typename T, int D, int QMODE, bool SPLIT, int U>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant_kernel(QDecodeArgs a) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
     constexpr int KSTEPS = D / 16;             // k-steps of QK^T
     constexpr int MT = D / 16;                 // m-tiles of PV
@@ -114,6 +146,9 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
     const int blk_end = min(blk_begin + a.part_blocks, nblk);
 
     // ---- query fragments (fp16) in the permuted k order of the code layout
+    // staged in this warp's shared slice (k-steps 2t, 2t + 1 of lane l at
+    // sq[warp][t][l]) and re-read per block, to leave registers for the codes
+    __shared__ uint4 sq[NW][KSTEPS / 2][32];
     uint32_t qf[KSTEPS][2];
     float qsum = 0.f;  // sum over this lane's columns of query head g
     {
@@ -134,10 +169,12 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
                     x[j] = __half2float(__float2half_rn(x[j]));
                     qsum += x[j];
                 }
+                // the odd nibbles enter the MMA 16x larger: their query
+                // columns go in divided by 16 (a power of two)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     qf[2 * k + e][0] = f16pair(x[2 * e], x[2 * e + 4]);
-                    qf[2 * k + e][1] = f16pair(x[2 * e + 1], x[2 * e + 5]);
+                    qf[2 * k + e][1] = f16pair(x[2 * e + 1] * 0.0625f, x[2 * e + 5] * 0.0625f);
                 }
             }
         } else {
@@ -157,6 +194,11 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
     }
     // full per-head sums: reduce over the 4 lanes of head g, then fetch the
     // sums of this lane's PV/S columns (heads 2c, 2c+1)
+#pragma unroll
+    for (int t = 0; t < KSTEPS / 2; ++t)
+        sq[warp][t][lane] = make_uint4(qf[2 * t][0], qf[2 * t][1], qf[2 * t + 1][0], qf[2 * t + 1][1]);
+    __syncwarp();
+    const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(&sq[warp][0][lane]));
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
     const float qsum0 = __shfl_sync(0xffffffffu, qsum, (2 * c) * 4);
@@ -171,96 +213,104 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
     const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
     const int vr0 = 2 * c, vr1 = 2 * c + 1, vr2 = 8 + 2 * c, vr3 = 9 + 2 * c;
 
-    for (int lb = blk_begin + warp; lb < blk_end; lb += NW) {
-        const int phys = trow[lb];
-        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
-            if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
-            continue;
-        }
+    // One block's codes and per-token (scale, zero) for this lane.
+    struct QBlk {
+        uint32_t kw0[KW], kw1[KW], vw[4][VW];
+        __half2 ks, vs, kz, vz;  // low: token g, high: token g + 8
+    };
+    auto load = [&](int phys, QBlk& B) {
         const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;  // (block, head)
         const uint8_t* kc = a.k_codes + bh * (BS * CB);
         const uint8_t* vc = a.v_codes + bh * (BS * CB);
 
         // ---- loads: K rows g, g+8; V rows 2c, 2c+1, 8+2c, 9+2c; scales
-        uint32_t kw0[KW], kw1[KW], vw[4][VW];
         if constexpr (INT4) {
             if constexpr (KW == 4) {
                 const uint4 r0 = ldg_stream(kc + g * CB + 16 * c);
                 const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 16 * c);
-                kw0[0] = r0.x; kw0[1] = r0.y; kw0[2] = r0.z; kw0[3] = r0.w;
-                kw1[0] = r1.x; kw1[1] = r1.y; kw1[2] = r1.z; kw1[3] = r1.w;
+                B.kw0[0] = r0.x; B.kw0[1] = r0.y; B.kw0[2] = r0.z; B.kw0[3] = r0.w;
+                B.kw1[0] = r1.x; B.kw1[1] = r1.y; B.kw1[2] = r1.z; B.kw1[3] = r1.w;
             } else {
                 const uint2 r0 = ldg_stream8(kc + g * CB + 8 * c);
                 const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 8 * c);
-                kw0[0] = r0.x; kw0[1] = r0.y;
-                kw1[0] = r1.x; kw1[1] = r1.y;
+                B.kw0[0] = r0.x; B.kw0[1] = r0.y;
+                B.kw1[0] = r1.x; B.kw1[1] = r1.y;
             }
             if constexpr (VW == 2) {
                 const int off = DS / 2 * g;  // bytes: DS columns = DS/2 bytes
                 const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
                 const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
-                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[1][0] = x1.x; vw[1][1] = x1.y;
-                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[3][0] = x3.x; vw[3][1] = x3.y;
+                B.vw[0][0] = x0.x; B.vw[0][1] = x0.y; B.vw[1][0] = x1.x; B.vw[1][1] = x1.y;
+                B.vw[2][0] = x2.x; B.vw[2][1] = x2.y; B.vw[3][0] = x3.x; B.vw[3][1] = x3.y;
             } else {
                 const int off = DS / 2 * g;
-                vw[0][0] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
-                vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
-                vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
-                vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+                B.vw[0][0] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
+                B.vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
+                B.vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
+                B.vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
             }
         } else {
 #pragma unroll
             for (int i = 0; i < D / 64; ++i) {
                 const uint4 r0 = ldg_stream(kc + g * CB + 64 * i + 16 * c);
                 const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 64 * i + 16 * c);
-                kw0[4 * i] = r0.x; kw0[4 * i + 1] = r0.y; kw0[4 * i + 2] = r0.z; kw0[4 * i + 3] = r0.w;
-                kw1[4 * i] = r1.x; kw1[4 * i + 1] = r1.y; kw1[4 * i + 2] = r1.z; kw1[4 * i + 3] = r1.w;
+                B.kw0[4 * i] = r0.x; B.kw0[4 * i + 1] = r0.y; B.kw0[4 * i + 2] = r0.z; B.kw0[4 * i + 3] = r0.w;
+                B.kw1[4 * i] = r1.x; B.kw1[4 * i + 1] = r1.y; B.kw1[4 * i + 2] = r1.z; B.kw1[4 * i + 3] = r1.w;
             }
             const int off = DS * g;  // bytes
             if constexpr (VW == 4) {
                 const uint4 x0 = ldg_stream(vc + vr0 * CB + off), x1 = ldg_stream(vc + vr1 * CB + off);
                 const uint4 x2 = ldg_stream(vc + vr2 * CB + off), x3 = ldg_stream(vc + vr3 * CB + off);
-                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[0][2] = x0.z; vw[0][3] = x0.w;
-                vw[1][0] = x1.x; vw[1][1] = x1.y; vw[1][2] = x1.z; vw[1][3] = x1.w;
-                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[2][2] = x2.z; vw[2][3] = x2.w;
-                vw[3][0] = x3.x; vw[3][1] = x3.y; vw[3][2] = x3.z; vw[3][3] = x3.w;
+                B.vw[0][0] = x0.x; B.vw[0][1] = x0.y; B.vw[0][2] = x0.z; B.vw[0][3] = x0.w;
+                B.vw[1][0] = x1.x; B.vw[1][1] = x1.y; B.vw[1][2] = x1.z; B.vw[1][3] = x1.w;
+                B.vw[2][0] = x2.x; B.vw[2][1] = x2.y; B.vw[2][2] = x2.z; B.vw[2][3] = x2.w;
+                B.vw[3][0] = x3.x; B.vw[3][1] = x3.y; B.vw[3][2] = x3.z; B.vw[3][3] = x3.w;
             } else {
                 const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
                 const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
-                vw[0][0] = x0.x; vw[0][1] = x0.y; vw[1][0] = x1.x; vw[1][1] = x1.y;
-                vw[2][0] = x2.x; vw[2][1] = x2.y; vw[3][0] = x3.x; vw[3][1] = x3.y;
+                B.vw[0][0] = x0.x; B.vw[0][1] = x0.y; B.vw[1][0] = x1.x; B.vw[1][1] = x1.y;
+                B.vw[2][0] = x2.x; B.vw[2][1] = x2.y; B.vw[3][0] = x3.x; B.vw[3][1] = x3.y;
             }
         }
         const __half* ksc = a.k_scale + bh * BS;
         const __half* vsc = a.v_scale + bh * BS;
-        const float ks0 = __half2float(ksc[g]), ks1 = __half2float(ksc[g + 8]);
-        const float vs0 = __half2float(vsc[g]), vs1 = __half2float(vsc[g + 8]);
-        float kz0 = 0.f, kz1 = 0.f, vz0 = 0.f, vz1 = 0.f;
+        B.ks = __halves2half2(ksc[g], ksc[g + 8]);
+        B.vs = __halves2half2(vsc[g], vsc[g + 8]);
         if constexpr (INT4) {
-            kz0 = __half2float(a.k_zero[bh * BS + g]);
-            kz1 = __half2float(a.k_zero[bh * BS + g + 8]);
-            vz0 = __half2float(a.v_zero[bh * BS + g]);
-            vz1 = __half2float(a.v_zero[bh * BS + g + 8]);
+            B.kz = __halves2half2(a.k_zero[bh * BS + g], a.k_zero[bh * BS + g + 8]);
+            B.vz = __halves2half2(a.v_zero[bh * BS + g], a.v_zero[bh * BS + g + 8]);
         }
-
+    };
+    auto attend = [&](int lb, QBlk& B) {
+        const float ks0 = __low2float(B.ks), ks1 = __high2float(B.ks);
+        const float vs0 = __low2float(B.vs), vs1 = __high2float(B.vs);
+        const float kz0 = INT4 ? __low2float(B.kz) : 0.f, kz1 = INT4 ? __high2float(B.kz) : 0.f;
+        const float vz0 = INT4 ? __low2float(B.vz) : 0.f, vz1 = INT4 ? __high2float(B.vz) : 0.f;
         // ---- S_raw^T = C Q^T over the code values
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (INT4) {
 #pragma unroll
             for (int k = 0; k < KW; ++k) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    mma_f16(s, nib2(kw0[k], 8 * e), nib2(kw1[k], 8 * e), nib2(kw0[k], 8 * e + 4),
-                            nib2(kw1[k], 8 * e + 4), qf[2 * k + e][0], qf[2 * k + e][1]);
-                }
+                // k-step 2k: nibbles {0, 4} and {1, 5}; 2k + 1: {2, 6}, {3, 7}
+                const uint4 q2 = kQueryInShared<QMODE> ? lds128(qs + k * 512)
+                                      : make_uint4(qf[2 * k][0], qf[2 * k][1], qf[2 * k + 1][0], qf[2 * k + 1][1]);
+                const uint32_t u0 = B.kw0[k] >> 8, u1 = B.kw1[k] >> 8;
+                mma_f16(s, nib_even(B.kw0[k]), nib_even(B.kw1[k]), nib_odd(B.kw0[k]), nib_odd(B.kw1[k]),
+                        q2.x, q2.y);
+                mma_f16(s, nib_even(u0), nib_even(u1), nib_odd(u0), nib_odd(u1), q2.z, q2.w);
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < KSTEPS; ++j) {
+            for (int t = 0; t < KSTEPS / 2; ++t) {
                 // k-step j = 4i + e uses word e of load i (= word j): codes
                 // {0, 1} are the low k pair, codes {2, 3} the high k pair
-                mma_f16(s, e4m3x2(kw0[j]), e4m3x2(kw1[j]), e4m3x2(kw0[j] >> 16),
-                        e4m3x2(kw1[j] >> 16), qf[j][0], qf[j][1]);
+                const int j0 = 2 * t, j1 = 2 * t + 1;
+                const uint4 q2 = kQueryInShared<QMODE> ? lds128(qs + t * 512)
+                                      : make_uint4(qf[j0][0], qf[j0][1], qf[j1][0], qf[j1][1]);
+                mma_f16(s, e4m3x2(B.kw0[j0]), e4m3x2(B.kw1[j0]), e4m3x2(B.kw0[j0] >> 16),
+                        e4m3x2(B.kw1[j0] >> 16), q2.x, q2.y);
+                mma_f16(s, e4m3x2(B.kw0[j1]), e4m3x2(B.kw1[j1]), e4m3x2(B.kw0[j1] >> 16),
+                        e4m3x2(B.kw1[j1] >> 16), q2.z, q2.w);
             }
         }
         const int t0 = lb * BS;
@@ -268,10 +318,12 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
         const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
         float x0, x1, x2, x3;
         if constexpr (INT4) {
-            x0 = ks0 * (s[0] + (8.f - kz0) * qsum0) * a.scale_log2;
-            x1 = ks0 * (s[1] + (8.f - kz0) * qsum1) * a.scale_log2;
-            x2 = ks1 * (s[2] + (8.f - kz1) * qsum0) * a.scale_log2;
-            x3 = ks1 * (s[3] + (8.f - kz1) * qsum1) * a.scale_log2;
+            // S = s (sum_d q_d c_d - z sum_d q_d); the MMA gave 2^-24 sum q c
+            const float f0 = ks0 * a.scale_log2, f1 = ks1 * a.scale_log2;
+            x0 = f0 * (s[0] * kTwo24 - kz0 * qsum0);
+            x1 = f0 * (s[1] * kTwo24 - kz0 * qsum1);
+            x2 = f1 * (s[2] * kTwo24 - kz1 * qsum0);
+            x3 = f1 * (s[3] * kTwo24 - kz1 * qsum1);
         } else {
             x0 = ks0 * s[0] * a.scale_log2;
             x1 = ks0 * s[1] * a.scale_log2;
@@ -319,22 +371,26 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
             bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
         }
         const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-        const float p0 = ex2(x0 - mn0), p1 = ex2(x1 - mn1);
-        const float p2 = ex2(x2 - mn0), p3 = ex2(x3 - mn1);
-        l0 = l0 * al0 + (p0 + p2);
-        l1 = l1 * al1 + (p1 + p3);
-        m0 = mn0;
-        m1 = mn1;
-        corr0 *= al0;
-        corr1 *= al1;
+        if (mn0 != m0 || mn1 != m1) {  // warp-uniform: the max is warp-wide
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            l0 *= al0;
+            l1 *= al1;
+            corr0 *= al0;
+            corr1 *= al1;
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            m0 = mn0;
+            m1 = mn1;
         }
+        const float p0 = ex2(x0 - m0), p1 = ex2(x1 - m1);
+        const float p2 = ex2(x2 - m0), p3 = ex2(x3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         // PV weights W = P * s (zero for masked and sink tokens)
         const bool w0 = ok0 && !sk0, w1 = ok1 && !sk1;
         const float W0 = w0 ? p0 * vs0 : 0.f, W1 = w0 ? p1 * vs0 : 0.f;
@@ -345,12 +401,12 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
             const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
             const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
             if (w0) {
-                corr0 += __low2float(h0) * (vz0 - 8.f);
-                corr1 += __high2float(h0) * (vz0 - 8.f);
+                corr0 += __low2float(h0) * vz0;
+                corr1 += __high2float(h0) * vz0;
             }
             if (w1) {
-                corr0 += __low2float(h1) * (vz1 - 8.f);
-                corr1 += __high2float(h1) * (vz1 - 8.f);
+                corr0 += __low2float(h1) * vz1;
+                corr1 += __high2float(h1) * vz1;
             }
         }
         const uint32_t pb0 = movmatrix_trans(pk0);
@@ -359,10 +415,10 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
         if (t0 + BS > ctx) {  // partial last block: clear codes of missing tokens
 #pragma unroll
             for (int j = 0; j < VW; ++j) {
-                if (t0 + vr0 >= ctx) vw[0][j] = 0;
-                if (t0 + vr1 >= ctx) vw[1][j] = 0;
-                if (t0 + vr2 >= ctx) vw[2][j] = 0;
-                if (t0 + vr3 >= ctx) vw[3][j] = 0;
+                if (t0 + vr0 >= ctx) B.vw[0][j] = 0;
+                if (t0 + vr1 >= ctx) B.vw[1][j] = 0;
+                if (t0 + vr2 >= ctx) B.vw[2][j] = 0;
+                if (t0 + vr3 >= ctx) B.vw[3][j] = 0;
             }
         }
 
@@ -375,16 +431,17 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
                 const int e = mt + hf * MT;
 #pragma unroll
                 for (int pr = 0; pr < 2; ++pr) {  // token pair (2c, 2c+1) / (8+2c, 9+2c)
-                    const uint32_t* A = vw[2 * pr];
-                    const uint32_t* B = vw[2 * pr + 1];
+                    const uint32_t* R0 = B.vw[2 * pr];
+                    const uint32_t* R1 = B.vw[2 * pr + 1];
                     uint32_t v;
                     if constexpr (INT4) {
                         const int word = e >> 3, sub = (e >> 2) & 1, nib = e & 3;
-                        const uint32_t X = __byte_perm(A[word], B[word], sub ? 0x7632u : 0x5410u);
-                        v = nib2(X, 4 * nib);
+                        const uint32_t X = __byte_perm(R0[word], R1[word], sub ? 0x7632u : 0x5410u);
+                        const uint32_t Y = nib >= 2 ? X >> 8 : X;
+                        v = (nib & 1) ? nib_odd(Y) : nib_even(Y);
                     } else {
                         const int word = e >> 2, sub = e & 3;
-                        const uint32_t X = __byte_perm(A[word], B[word], (sub >> 1) ? 0x7362u : 0x5140u);
+                        const uint32_t X = __byte_perm(R0[word], R1[word], (sub >> 1) ? 0x7362u : 0x5140u);
                         v = e4m3x2((sub & 1) ? (X >> 16) : X);
                     }
                     av[hf + 2 * pr] = v;
@@ -403,13 +460,40 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
                 const T* vrow = svb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D + g * DS;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
-                    const float vl = tofloat(vrow[mt]), vh = tofloat(vrow[mt + MT]);
+                    // in the accumulator's units (INT4: 2^-24, odd columns 2^-20)
+                    const float u = INT4 ? ((mt & 1) ? 16.f * kInvTwo24 : kInvTwo24) : 1.f;
+                    const float vl = tofloat(vrow[mt]) * u, vh = tofloat(vrow[mt + MT]) * u;
                     o[mt][0] += pa * vl;
                     o[mt][1] += pb * vl;
                     o[mt][2] += pa * vh;
                     o[mt][3] += pb * vh;
                 }
             }
+        }
+    };
+
+    // Warp w takes U consecutive blocks per step -- blk_begin + U (w + NW i)
+    // + u -- all loaded before any is attended, so U blocks of codes are in
+    // flight per warp.  Lane j holds the physical id of the warp's j-th
+    // upcoming block (32 at a time).
+    int tab = 0;
+    for (int i = 0, lb0 = blk_begin + U * warp; lb0 < blk_end; ++i, lb0 += U * NW) {
+        if (((i * U) & 31) == 0) {
+            const int idx = lb0 + (lane / U) * U * NW + lane % U;
+            tab = idx < blk_end ? trow[idx] : -1;
+        }
+        QBlk B[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int phys = __shfl_sync(0xffffffffu, tab, (i * U + u) & 31);
+            ok[u] = lb0 + u < blk_end && static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
+            if (lb0 + u < blk_end && !ok[u] && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            if (ok[u]) load(phys, B[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (ok[u]) attend(lb0 + u, B[u]);
         }
     }
 
@@ -431,11 +515,14 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
+        // INT4: back from the accumulator's units (columns e = mt, mt + MT
+        // share mt's parity), then O = sum W c - sum W z
+        const float u = INT4 ? ((mt & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
         const int dl = g * DS + mt, dh = g * DS + mt + MT;
-        sm_o[warp][2 * c][dl] = o[mt][0] - corr0;
-        sm_o[warp][2 * c + 1][dl] = o[mt][1] - corr1;
-        sm_o[warp][2 * c][dh] = o[mt][2] - corr0;
-        sm_o[warp][2 * c + 1][dh] = o[mt][3] - corr1;
+        sm_o[warp][2 * c][dl] = o[mt][0] * u - corr0;
+        sm_o[warp][2 * c + 1][dl] = o[mt][1] * u - corr1;
+        sm_o[warp][2 * c][dh] = o[mt][2] * u - corr0;
+        sm_o[warp][2 * c + 1][dh] = o[mt][3] * u - corr1;
     }
     __syncthreads();
 
@@ -470,7 +557,7 @@ __global__ void __launch_bounds__(NW * 32, 4) paged_decode_quant_kernel(QDecodeA
 template <typename T, int D, int QMODE, bool SPLIT>
 void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
     dim3 grid(SPLIT ? parts : 1, hkv, batch);
-    paged_decode_quant_kernel<T, D, QMODE, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+    paged_decode_quant_kernel<T, D, QMODE, SPLIT, kBlocksPerStep<QMODE>><<<grid, NW * 32, 0, st>>>(a);
 }
 
 template <bool SPLIT>
