@@ -185,15 +185,16 @@ int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
  *     may be balanced (batch <= 1024 and batch * num_q_heads * max_blocks >=
  *     32 * 16 * SMs), the larger of that and the balanced split's need:
  *     (nwt * 8 + batch * num_q_heads) * (head_dim + 2) * 4 bytes,
- *     nwt = min(16 * SMs, batch * num_q_heads * max_blocks / 2)
- *     launched warps (SMs of the current device, 152 if none). */
+ *     nwt = min(20 * SMs, batch * num_q_heads * max_blocks / 2), the most
+ *     warps a balanced kernel launches (SMs of the current device, 152 if
+ *     none). */
 int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                int32_t max_blocks, int32_t block_size, int32_t partition_size,
                                size_t* out);
 
 /* The partition size of an automatic split that is not balanced (see
- * pkv_paged_attention_decode), of the quantised decode with partition_size
- * 0, and of _partials / _merge with partition_size 0: the largest of 512,
+ * pkv_paged_attention_decode; the quantised decode follows the same rule),
+ * and of _partials / _merge with partition_size 0: the largest of 512,
  * 256, 128, 64 tokens for which batch * num_q_heads * ceil(max_blocks *
  * block_size / size) >= 12 * (SM count of the current device, 152 if none),
  * else 64.  Small batches get finer splits so the GPU has enough partition

@@ -1,0 +1,140 @@
+// Balanced split-K ("stream-K" over block-heads), shared by the 16-bit and
+// the quantised decode kernels.
+//
+// The work of one decode call is the ordered list of (sequence, KV head,
+// logical block) items -- sequence-major, then KV head, then block --
+// W = Hkv * sum_b nblk_b items.  Warp i of nwt = min(launched warps,
+// W / min_items) takes the contiguous range [i W / nwt, (i + 1) W / nwt), so
+// every warp streams the same number of blocks whatever the mix of context
+// lengths: no wave quantisation, no short last partitions, one prologue per
+// warp.  A range falls into runs of one (sequence, KV head); a warp writes
+// one fp32 partial (m, l, o) per run it touches, at slot i + b * Hkv + kvh
+// (rows slot * G + h of the partial arrays): the warps touching one run are
+// consecutive and every range is non-empty, so slots never collide, and
+// fewer than nwt + batch * Hkv slots are used.
+#pragma once
+
+#include "common.cuh"
+
+namespace pkv {
+
+constexpr int kSplitBS = 16;  // tokens per block
+
+// Batches up to this size may use the balanced split (every warp scans the
+// context lengths once).
+constexpr int kBalancedMaxBatch = 1024;
+// Fewest (sequence, KV head, block) items a warp of the balanced split takes.
+constexpr int kBalancedMinItems = 2;
+// The automatic split is balanced when the tables could hold this many items
+// per launched warp: below it fixed partitions measured as fast or faster
+// (the balanced split's per-warp scan, partial rows and merge cost more than
+// the wave quantisation they remove).
+constexpr int kBalancedItemsPerWarp = 32;
+
+// SM count of the current device (152 when it cannot be queried), cached.
+int num_sms();
+// Warps a balanced split launches: warps_per_sm per SM (all resident at
+// once), fewer for small problems.
+int balanced_warps(int64_t max_items, int warps_per_sm);
+// The most warps per SM any balanced kernel launches (the workspace bound).
+constexpr int kBalancedMaxWarpsPerSm = 20;
+// Whether an automatic split may be balanced for at most max_items items.
+bool balanced_candidate(int64_t batch, int64_t max_items);
+// Whether an automatic split over these tables is balanced.
+bool use_balanced(int64_t batch, int64_t hkv, int64_t max_blocks);
+// Workspace bytes of a balanced split: nwt * G + batch * hq partial rows.
+size_t balanced_bytes(int32_t batch, int32_t hq, int32_t G, int32_t D, int32_t nwt);
+// The merge of a balanced split (decode.cu), launched behind the split
+// kernel with programmatic dependent launch; out has the 16-bit dtype.
+int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int max_blocks,
+                          int nwt, const float* ws_o, const float* ws_ml, void* out, int dtype,
+                          cudaStream_t st);
+
+__device__ __forceinline__ int blocks_of(int ctx, int cap) {
+    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+    return (ctx + kSplitBS - 1) / kSplitBS;
+}
+
+// First warp of a balanced split whose range holds item x: the largest i
+// with floor(i W / nwt) <= x.
+__device__ __forceinline__ int64_t first_warp(int64_t x, int64_t W, int64_t nwt) {
+    return ((x + 1) * nwt - 1) / W;
+}
+
+// One warp's range, walked run by run.  The host keeps
+// batch * Hkv * max_blocks below 2^30, so item indices fit in int.
+struct WarpSplit {
+    const int32_t* ctx_lens;
+    int cap, hkv;
+    int pos, E;    // remaining items [pos, E)
+    int b, nb, cs; // current sequence, its block count, its first item
+    // current run segment: sequence b, KV head kvh, blocks [lb0, lb1)
+    int ctx, kvh, lb0, lb1;
+
+    // Sets up warp i's range; false when it has none.  Every lane of the warp
+    // calls it (warp-collective).  bad: some context length was outside
+    // [0, max_blocks * 16].
+    __device__ __forceinline__ bool begin(const int32_t* lens, int batch, int max_blocks, int hkv_,
+                                          int nwt_launch, int min_items, int i, bool& bad) {
+        const int lane = threadIdx.x & 31;
+        ctx_lens = lens;
+        cap = max_blocks * kSplitBS;
+        hkv = hkv_;
+        int mine = 0;
+        bad = false;
+        for (int j = lane; j < batch; j += 32) {
+            const int x = lens[j];
+            bad |= x < 0 || x > cap;
+            mine += blocks_of(x, cap);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
+        bad = __any_sync(0xffffffffu, bad);
+        const int W = mine * hkv;
+        const int nwt = max(min(W / min_items, nwt_launch), 1);
+        if (W == 0 || i >= nwt) return false;
+        pos = static_cast<int>(static_cast<int64_t>(i) * W / nwt);
+        E = static_cast<int>(static_cast<int64_t>(i + 1) * W / nwt);
+        // the sequence holding item pos
+        b = nb = cs = 0;
+        int run = 0;
+        for (int base = 0; base < batch; base += 32) {
+            const int j = base + lane;
+            const int nbj = j < batch ? blocks_of(lens[j], cap) : 0;
+            int incl = nbj;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += y;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, j < batch && pos < (run + incl) * hkv);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                b = base + src;
+                nb = __shfl_sync(0xffffffffu, nbj, src);
+                cs = (run + __shfl_sync(0xffffffffu, incl - nbj, src)) * hkv;
+                break;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        return true;
+    }
+
+    // Advances to the next run segment of the range; false at its end.
+    __device__ __forceinline__ bool next() {
+        if (pos >= E) return false;
+        while (pos >= cs + nb * hkv) {  // next non-empty sequence
+            cs += nb * hkv;
+            ++b;
+            nb = blocks_of(ctx_lens[b], cap);
+        }
+        ctx = min(max(ctx_lens[b], 0), cap);
+        kvh = (pos - cs) / nb;
+        lb0 = pos - cs - kvh * nb;
+        lb1 = min(nb, lb0 + (E - pos));
+        pos += lb1 - lb0;
+        return true;
+    }
+};
+
+}  // namespace pkv

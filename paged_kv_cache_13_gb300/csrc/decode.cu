@@ -46,8 +46,9 @@
 //   are zeroed in registers (an unwritten slot may hold NaN bit patterns).
 
 #include <atomic>
+#include <type_traits>
 
-#include "common.cuh"
+#include "balanced.cuh"
 
 namespace pkv {
 namespace {
@@ -487,27 +488,9 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
     });
 }
 
-__device__ __forceinline__ int blocks_of(int ctx, int cap) {
-    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    return (ctx + BS - 1) / BS;
-}
-
-// First warp of a balanced split whose range holds item x: the largest i
-// with floor(i W / nwt) <= x.
-__device__ __forceinline__ int64_t first_warp(int64_t x, int64_t W, int64_t nwt) {
-    return ((x + 1) * nwt - 1) / W;
-}
-
-// Balanced split-K ("stream-K" over block-heads).  The work of one call is
-// the ordered list of (sequence, KV head, logical block) items, sequence-
-// major, then KV head, then block: W = Hkv * sum_b nblk_b items.  Warp i of
-// nwt = min(launched warps, W / min_items) takes the contiguous range
-// [i W / nwt, (i + 1) W / nwt), so every warp streams the same number of
-// blocks whatever the mix of context lengths: no wave quantisation, no short
-// last partitions, one prologue per warp, and no barrier anywhere.  A warp
-// writes one fp32 partial (m, l, o) per (sequence, KV head) run it touches,
-// at slot i + b * Hkv + kvh: the warps touching one run are consecutive and
-// every range is non-empty, so slots never collide.
+// Balanced split-K kernel for the 16-bit cache (the split itself:
+// balanced.cuh).  Warp i walks its range run by run; within a run it
+// attends its blocks in order, then writes the run's partial.  No barrier.
 template <typename T, int D, bool APPEND>
 __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
     paged_decode_balanced_kernel(DecodeArgs a, int batch, int nwt_launch, int min_items) {
@@ -520,63 +503,15 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
     __shared__ __align__(16) float sm_o[kNW][8][D];
     __shared__ uint4 sm_q[kNW][KC][32];
 
-    // every warp counts the items (the host keeps batch * Hkv * max_blocks
-    // below 2^30)
-    const int cap = a.max_blocks * BS;
-    int mine = 0;
-    bool bad = false;
-    for (int j = lane; j < batch; j += 32) {
-        const int x = a.ctx_lens[j];
-        bad |= x < 0 || x > cap;
-        mine += blocks_of(x, cap);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, off);
-    const int W = mine * a.hkv;
-    const int nwt = max(min(W / min_items, nwt_launch), 1);
     const int i = blockIdx.x * kNW + warp;
-
+    WarpSplit ws_;
+    bool bad = false;
+    const bool any = ws_.begin(a.ctx_lens, batch, a.max_blocks, a.hkv, nwt_launch, min_items, i, bad);
     if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
-    if (W == 0 || i >= nwt) return;
-    const int S = static_cast<int>(static_cast<int64_t>(i) * W / nwt);
-    const int E = static_cast<int>(static_cast<int64_t>(i + 1) * W / nwt);
+    if (!any) return;
 
-    // the sequence holding item S: its first item (cs) and block count (nb)
-    int b = 0, nb = 0, cs = 0;
-    {
-        int run = 0;
-        for (int base = 0; base < batch; base += 32) {
-            const int j = base + lane;
-            const int nbj = j < batch ? blocks_of(a.ctx_lens[j], cap) : 0;
-            int incl = nbj;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off) incl += y;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, j < batch && S < (run + incl) * a.hkv);
-            if (hit) {
-                const int src = __ffs(hit) - 1;
-                b = base + src;
-                nb = __shfl_sync(0xffffffffu, nbj, src);
-                cs = (run + __shfl_sync(0xffffffffu, incl - nbj, src)) * a.hkv;
-                break;
-            }
-            run += __shfl_sync(0xffffffffu, incl, 31);
-        }
-    }
-
-    for (int pos = S; pos < E;) {
-        while (pos >= cs + nb * a.hkv) {  // next non-empty sequence
-            cs += nb * a.hkv;
-            ++b;
-            nb = blocks_of(a.ctx_lens[b], cap);
-        }
-        const int ctx = min(max(a.ctx_lens[b], 0), cap);
-        const int kvh = (pos - cs) / nb;
-        const int lb0 = pos - cs - kvh * nb;
-        const int lb1 = min(nb, lb0 + (E - pos));
-        pos += lb1 - lb0;
+    while (ws_.next()) {
+        const int b = ws_.b, nb = ws_.nb, ctx = ws_.ctx, kvh = ws_.kvh, lb0 = ws_.lb0, lb1 = ws_.lb1;
         const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
 
         // fused append: the new row is at ctx - 1, in the run's last block
@@ -797,16 +732,6 @@ struct Shape {
     bool balanced;  // automatic split: balanced over warps instead of fixed partitions
 };
 
-// Batches up to this size use the balanced split when the partition size is
-// automatic (every warp scans the context lengths once).
-constexpr int kBalancedMaxBatch = 1024;
-// Fewest (sequence, KV head, block) items a warp of the balanced split takes.
-constexpr int kBalancedMinItems = 2;
-// The automatic split is balanced when the tables could hold this many items
-// per launched warp: below it the fixed partitions measured as fast or faster
-// (the balanced split's per-warp scan, partial rows and merge cost more than
-// the wave-quantisation they remove).
-constexpr int kBalancedItemsPerWarp = 32;
 
 }  // namespace
 
@@ -838,28 +763,24 @@ int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
     return 64;
 }
 
-// Warps a balanced split launches: 4 CTAs of 4 warps per SM, all resident at
-// once, but no more than the largest possible item count allows at
+// No more warps than the largest possible item count allows at
 // kBalancedMinItems each, so small problems launch (and need room for) fewer.
-int balanced_warps(int64_t max_items) {
-    const int64_t full = num_sms() * 16LL;
+int balanced_warps(int64_t max_items, int warps_per_sm) {
+    const int64_t full = static_cast<int64_t>(num_sms()) * warps_per_sm;
     const int64_t n = max_items / kBalancedMinItems < full ? max_items / kBalancedMinItems : full;
     return n < 1 ? 1 : static_cast<int>(n);
 }
 
-// Whether an automatic split may be balanced for this many items at most
-// (the tables' capacity), and whether it is (else fixed partitions).
 bool balanced_candidate(int64_t batch, int64_t max_items) {
     return batch <= kBalancedMaxBatch &&
            max_items >= static_cast<int64_t>(kBalancedItemsPerWarp) * num_sms() * 16;
 }
+
 bool use_balanced(int64_t batch, int64_t hkv, int64_t max_blocks) {
     const int64_t items = batch * hkv * max_blocks;
     return balanced_candidate(batch, items) && items < (1LL << 30);
 }
 
-// Bytes of a balanced split's workspace: nwt * G + batch * hq partial rows
-// of D + 2 floats (o, then (m, l)).
 size_t balanced_bytes(int32_t batch, int32_t hq, int32_t G, int32_t D, int32_t nwt) {
     const size_t rows = static_cast<size_t>(nwt) * G + static_cast<size_t>(batch) * hq;
     return rows * (D + 2) * sizeof(float);
@@ -922,10 +843,10 @@ int launch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items,
 }
 
 template <typename T, int D, int PG>
-int launch_merge_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items,
-                          cudaStream_t st) {
+int launch_merge_balanced_t(const int32_t* ctx_lens, int batch, int hq, int hkv, int max_blocks, int nwt,
+                            const float* ws_o, const float* ws_ml, void* out, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(s.hq, s.batch);
+    cfg.gridDim = dim3(hq, batch);
     cfg.blockDim = dim3(D * PG);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
@@ -934,34 +855,31 @@ int launch_merge_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_balanced_kernel<T, D, PG>, a.ctx_lens, s.batch,
-                                             s.hq, s.hkv, s.max_blocks, nwt, min_items,
-                                             static_cast<const float*>(a.ws_o),
-                                             static_cast<const float*>(a.ws_ml), static_cast<T*>(a.out));
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_balanced_kernel<T, D, PG>, ctx_lens, batch, hq, hkv,
+                                             max_blocks, nwt, kBalancedMinItems, ws_o, ws_ml,
+                                             static_cast<T*>(out));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Balanced split: the warp-range kernel, then its merge.  Runs of one
-// (sequence, KV head) span about nwt / (batch * Hkv) warp ranges at the
-// longest; beyond 16 the merge folds with 4 partial groups per CTA.
+// Balanced split: the warp-range kernel, then its merge.
 template <typename T, int D, bool APPEND>
-int run_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, cudaStream_t st) {
-    int r = launch_balanced<T, D, APPEND>(a, s, nwt, min_items, st);
+int run_balanced(const DecodeArgs& a, const Shape& s, int nwt, cudaStream_t st) {
+    paged_decode_balanced_kernel<T, D, APPEND>
+        <<<(nwt + kNW - 1) / kNW, kNW * 32, 0, st>>>(a, s.batch, nwt, kBalancedMinItems);
+    const int r = launch_status();
     if (r != PKV_OK) return r;
-    const bool many = nwt > 16LL * s.batch * s.hkv;
-    return many ? launch_merge_balanced<T, D, 4>(a, s, nwt, min_items, st)
-                : launch_merge_balanced<T, D, 1>(a, s, nwt, min_items, st);
+    return launch_balanced_merge(a.ctx_lens, s.batch, s.hq, s.hkv, D, s.max_blocks, nwt, a.ws_o, a.ws_ml,
+                                 a.out, std::is_same<T, __half>::value ? PKV_DTYPE_F16 : PKV_DTYPE_BF16, st);
 }
 
 template <bool APPEND>
-int dispatch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, int dtype,
-                      cudaStream_t st) {
+int dispatch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int dtype, cudaStream_t st) {
     if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128) return run_balanced<__nv_bfloat16, 128, APPEND>(a, s, nwt, min_items, st);
-        return run_balanced<__nv_bfloat16, 64, APPEND>(a, s, nwt, min_items, st);
+        if (s.D == 128) return run_balanced<__nv_bfloat16, 128, APPEND>(a, s, nwt, st);
+        return run_balanced<__nv_bfloat16, 64, APPEND>(a, s, nwt, st);
     }
-    if (s.D == 128) return run_balanced<__half, 128, APPEND>(a, s, nwt, min_items, st);
-    return run_balanced<__half, 64, APPEND>(a, s, nwt, min_items, st);
+    if (s.D == 128) return run_balanced<__half, 128, APPEND>(a, s, nwt, st);
+    return run_balanced<__half, 64, APPEND>(a, s, nwt, st);
 }
 
 // The merge grid is launched with programmatic stream serialization: it may
@@ -1050,14 +968,15 @@ int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_
         return dispatch<kSingle, APPEND>(a, s, dtype, cs);
     }
     if (s.balanced) {
-        const int nwt = balanced_warps(static_cast<int64_t>(s.batch) * s.hkv * s.max_blocks);
+        // 4 CTAs of 4 warps per SM
+        const int nwt = balanced_warps(static_cast<int64_t>(s.batch) * s.hkv * s.max_blocks, 4 * kNW);
         const int G = s.hq / s.hkv;
         if (!ws || ws_bytes < balanced_bytes(s.batch, s.hq, G, s.D, nwt)) return PKV_ERR_WORKSPACE;
         if (!aligned16(ws)) return PKV_ERR_MISALIGNED;
         const size_t rows = static_cast<size_t>(nwt) * G + static_cast<size_t>(s.batch) * s.hq;
         a.ws_o = static_cast<float*>(ws);
         a.ws_ml = a.ws_o + rows * s.D;
-        return dispatch_balanced<APPEND>(a, s, nwt, kBalancedMinItems, dtype, cs);
+        return dispatch_balanced<APPEND>(a, s, nwt, dtype, cs);
     }
     int st = set_workspace(&a, s, ws, ws_bytes);
     if (st != PKV_OK) return st;
@@ -1066,6 +985,27 @@ int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_
 }
 
 }  // namespace
+
+// Runs of one (sequence, KV head) span about nwt / (batch * Hkv) warp ranges
+// at the longest; beyond 16 the merge folds with 4 partial groups per CTA.
+int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int max_blocks,
+                          int nwt, const float* ws_o, const float* ws_ml, void* out, int dtype,
+                          cudaStream_t st) {
+    const bool many = nwt > 16LL * batch * hkv;
+#define PKV_BMERGE(TT, DD)                                                                             \
+    return many ? launch_merge_balanced_t<TT, DD, 4>(ctx_lens, batch, hq, hkv, max_blocks, nwt, ws_o, \
+                                                     ws_ml, out, st)                                 \
+                : launch_merge_balanced_t<TT, DD, 1>(ctx_lens, batch, hq, hkv, max_blocks, nwt, ws_o, \
+                                                     ws_ml, out, st)
+    if (dtype == PKV_DTYPE_BF16) {
+        if (D == 128) PKV_BMERGE(__nv_bfloat16, 128);
+        PKV_BMERGE(__nv_bfloat16, 64);
+    }
+    if (D == 128) PKV_BMERGE(__half, 128);
+    PKV_BMERGE(__half, 64);
+#undef PKV_BMERGE
+}
+
 }  // namespace pkv
 
 extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
@@ -1089,7 +1029,7 @@ extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
         // room for a balanced split (16-bit cache) with Hkv anywhere in
         // [1, Hq] and a GQA group up to 8; the quantised decode still splits
         // into the automatic partitions
-        const int nwt = pkv::balanced_warps(max_items);
+        const int nwt = pkv::balanced_warps(max_items, pkv::kBalancedMaxWarpsPerSm);
         const size_t bal = pkv::balanced_bytes(batch, num_q_heads, 8, head_dim, nwt);
         *out = bal > fixed ? bal : fixed;
         return PKV_OK;

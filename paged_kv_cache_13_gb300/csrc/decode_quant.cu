@@ -36,18 +36,13 @@
 // logits are recomputed in fp32 from the 16-bit sink keys, their PV weights
 // are zero in the MMA, and P * sink_v is added to the accumulator directly.
 
-#include "common.cuh"
+#include "balanced.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int BS = 16;
 constexpr int NW = 4;
-// Blocks a warp loads before attending them: INT4 blocks are 2 KiB per
-// (block, head), two keep ~4 KiB of codes in flight per warp; FP8 blocks are
-// 4 KiB and two would not fit the 128-register budget.
-template <int QMODE>
-constexpr int kBlocksPerStep = 1;
 // INT4 runs 5 CTAs per SM (96 registers) with the query fragments re-read
 // from shared memory per block; FP8 needs its registers for the 4 KiB of
 // codes per block and keeps 4 CTAs with the query fragments in registers.
@@ -119,8 +114,29 @@ __device__ __forceinline__ float tofloat(T x) {
     return Half16<T>::to_float(x);
 }
 
-template <typename T, int D, int QMODE, bool SPLIT, int U>
-__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant_kernel(QDecodeArgs a) {
+// Online-softmax state of one warp over the blocks it attended, for the
+// query heads 2c, 2c+1 of its lanes: per-lane partial sums l and (INT4) the
+// zero-point correction sum_t W_t z_t, and the PV accumulator in the MMA's
+// units (INT4: 2^-24, odd columns 2^-20).
+template <int MT>
+struct QState {
+    float m0, m1, l0, l1, corr0, corr1;
+    float o[MT][4];
+    __device__ __forceinline__ void init() {
+        m0 = m1 = neg_inf();
+        l0 = l1 = corr0 = corr1 = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+};
+
+// One warp's pass over the blocks lb_first, lb_first + stride, ... < lb_end
+// of sequence b, KV head kvh (context ctx): query fragments, then every block
+// loaded into registers and attended into st (reset first).  sq is the
+// lane's slot of the warp's shared query slice (row t at sq[t * 32]).
+template <typename T, int D, int QMODE>
+__device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh, int ctx, int lb_first,
+                                           int lb_end, int stride, uint4* sq, QState<D / 16>& st) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
     constexpr int KSTEPS = D / 16;             // k-steps of QK^T
     constexpr int MT = D / 16;                 // m-tiles of PV
@@ -128,27 +144,12 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     constexpr int KW = INT4 ? D / 32 : D / 16; // 32-bit K-code words per lane per row
     constexpr int VW = INT4 ? D / 64 : D / 32; // 32-bit V-code words per lane per row
     constexpr int DS = D / 8;                  // head-dim columns per lane group in PV
-
-    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-
-    int ctx = a.ctx_lens[b];
-    const int cap = a.max_blocks * BS;
-    if (ctx < 0 || ctx > cap) {
-        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    const int nblk = (ctx + BS - 1) / BS;
-    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
-    if (p >= (nparts > 0 ? nparts : 1)) return;
-    const int blk_begin = p * a.part_blocks;
-    const int blk_end = min(blk_begin + a.part_blocks, nblk);
 
     // ---- query fragments (fp16) in the permuted k order of the code layout
     // staged in this warp's shared slice (k-steps 2t, 2t + 1 of lane l at
     // sq[warp][t][l]) and re-read per block, to leave registers for the codes
-    __shared__ uint4 sq[NW][KSTEPS / 2][32];
     uint32_t qf[KSTEPS][2];
     float qsum = 0.f;  // sum over this lane's columns of query head g
     {
@@ -194,21 +195,27 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     }
     // full per-head sums: reduce over the 4 lanes of head g, then fetch the
     // sums of this lane's PV/S columns (heads 2c, 2c+1)
+    __syncwarp();  // the previous pass no longer reads the slice
+    if constexpr (kQueryInShared<QMODE>) {
 #pragma unroll
-    for (int t = 0; t < KSTEPS / 2; ++t)
-        sq[warp][t][lane] = make_uint4(qf[2 * t][0], qf[2 * t][1], qf[2 * t + 1][0], qf[2 * t + 1][1]);
-    __syncwarp();
-    const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(&sq[warp][0][lane]));
+        for (int t = 0; t < KSTEPS / 2; ++t)
+            sq[t * 32] = make_uint4(qf[2 * t][0], qf[2 * t][1], qf[2 * t + 1][0], qf[2 * t + 1][1]);
+        __syncwarp();
+    }
+    const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(sq));
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
     const float qsum0 = __shfl_sync(0xffffffffu, qsum, (2 * c) * 4);
     const float qsum1 = __shfl_sync(0xffffffffu, qsum, (2 * c + 1) * 4);
 
-    float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
-    float corr0 = 0.f, corr1 = 0.f;  // INT4: sum_t W_t (z_t - 8) per head
-    float o[MT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float& m0 = st.m0;
+    float& m1 = st.m1;
+    float& l0 = st.l0;
+    float& l1 = st.l1;
+    float& corr0 = st.corr0;
+    float& corr1 = st.corr1;
+    auto& o = st.o;
+    st.init();
 
     const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
     const int vr0 = 2 * c, vr1 = 2 * c + 1, vr2 = 8 + 2 * c, vr3 = 9 + 2 * c;
@@ -472,38 +479,80 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
         }
     };
 
-    // Warp w takes U consecutive blocks per step -- blk_begin + U (w + NW i)
-    // + u -- all loaded before any is attended, so U blocks of codes are in
-    // flight per warp.  Lane j holds the physical id of the warp's j-th
-    // upcoming block (32 at a time).
+    // Lane j holds the physical id of the pass's j-th upcoming block (32 at
+    // a time), so a block's loads never wait behind a table load.
     int tab = 0;
-    for (int i = 0, lb0 = blk_begin + U * warp; lb0 < blk_end; ++i, lb0 += U * NW) {
-        if (((i * U) & 31) == 0) {
-            const int idx = lb0 + (lane / U) * U * NW + lane % U;
-            tab = idx < blk_end ? trow[idx] : -1;
+    for (int i = 0, lb = lb_first; lb < lb_end; ++i, lb += stride) {
+        if ((i & 31) == 0) {
+            const int idx = lb + stride * lane;
+            tab = idx < lb_end ? trow[idx] : -1;
         }
-        QBlk B[U];
-        bool ok[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int phys = __shfl_sync(0xffffffffu, tab, (i * U + u) & 31);
-            ok[u] = lb0 + u < blk_end && static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
-            if (lb0 + u < blk_end && !ok[u] && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
-            if (ok[u]) load(phys, B[u]);
+        const int phys = __shfl_sync(0xffffffffu, tab, i & 31);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            continue;
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (ok[u]) attend(lb0 + u, B[u]);
-        }
+        QBlk B;
+        load(phys, B);
+        attend(lb, B);
     }
+}
 
+// Lane-final values of a pass: l and the correction summed over the 8 token
+// lanes, and the output column values sum_t W_t (c - z) in true units.
+template <int D, int QMODE>
+__device__ __forceinline__ void quant_finish(QState<D / 16>& st) {
+    constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
+    constexpr int MT = D / 16;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        corr0 += __shfl_xor_sync(0xffffffffu, corr0, off);
-        corr1 += __shfl_xor_sync(0xffffffffu, corr1, off);
+        st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+        st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+        st.corr0 += __shfl_xor_sync(0xffffffffu, st.corr0, off);
+        st.corr1 += __shfl_xor_sync(0xffffffffu, st.corr1, off);
     }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        // INT4: back from the accumulator's units (columns e = mt, mt + MT
+        // share mt's parity), then O = sum W c - sum W z
+        const float u = INT4 ? ((mt & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
+        st.o[mt][0] = st.o[mt][0] * u - st.corr0;
+        st.o[mt][1] = st.o[mt][1] * u - st.corr1;
+        st.o[mt][2] = st.o[mt][2] * u - st.corr0;
+        st.o[mt][3] = st.o[mt][3] * u - st.corr1;
+    }
+}
+
+// Partition kernel: one CTA of NW warps per (partition, KV head, sequence);
+// the warps take the partition's blocks round-robin and merge through
+// shared memory.
+template <typename T, int D, int QMODE, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant_kernel(QDecodeArgs a) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int MT = D / 16;
+    constexpr int DS = D / 8;
+    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+
+    int ctx = a.ctx_lens[b];
+    const int cap = a.max_blocks * BS;
+    if (ctx < 0 || ctx > cap) {
+        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+        ctx = ctx < 0 ? 0 : cap;
+    }
+    const int nblk = (ctx + BS - 1) / BS;
+    const int nparts = (nblk + a.part_blocks - 1) / a.part_blocks;
+    if (p >= (nparts > 0 ? nparts : 1)) return;
+    const int blk_begin = p * a.part_blocks;
+    const int blk_end = min(blk_begin + a.part_blocks, nblk);
+
+    __shared__ uint4 sq[NW][KSTEPS / 2][32];
+    QState<MT> st;
+    quant_pass<T, D, QMODE>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
+    quant_finish<D, QMODE>(st);
+    const float m0 = st.m0, m1 = st.m1, l0 = st.l0, l1 = st.l1;
+    auto& o = st.o;
 
     __shared__ float sm_ml[NW][8][2];
     __shared__ float sm_o[NW][8][D];
@@ -515,14 +564,11 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        // INT4: back from the accumulator's units (columns e = mt, mt + MT
-        // share mt's parity), then O = sum W c - sum W z
-        const float u = INT4 ? ((mt & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
         const int dl = g * DS + mt, dh = g * DS + mt + MT;
-        sm_o[warp][2 * c][dl] = o[mt][0] * u - corr0;
-        sm_o[warp][2 * c + 1][dl] = o[mt][1] * u - corr1;
-        sm_o[warp][2 * c][dh] = o[mt][2] * u - corr0;
-        sm_o[warp][2 * c + 1][dh] = o[mt][3] * u - corr1;
+        sm_o[warp][2 * c][dl] = o[mt][0];
+        sm_o[warp][2 * c + 1][dl] = o[mt][1];
+        sm_o[warp][2 * c][dh] = o[mt][2];
+        sm_o[warp][2 * c + 1][dh] = o[mt][3];
     }
     __syncthreads();
 
@@ -554,10 +600,94 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     }
 }
 
+// Balanced split for the quantised cache (the split itself: balanced.cuh):
+// warp i walks its range run by run, one pass per run segment, and writes
+// the run's partial.  No barrier.
+template <typename T, int D, int QMODE>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>)
+    paged_decode_quant_balanced_kernel(QDecodeArgs a, int batch, int nwt_launch) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int MT = D / 16;
+    constexpr int DS = D / 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    // the merge grid may be scheduled now; it waits for this grid to finish
+    asm volatile("griddepcontrol.launch_dependents;");
+    __shared__ uint4 sq[NW][KSTEPS / 2][32];
+    __shared__ __align__(16) float sm_o[NW][8][D];
+
+    const int i = blockIdx.x * NW + warp;
+    WarpSplit sp;
+    bool bad = false;
+    const bool any = sp.begin(a.ctx_lens, batch, a.max_blocks, a.hkv, nwt_launch, kBalancedMinItems, i, bad);
+    if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+    if (!any) return;
+    while (sp.next()) {
+        QState<MT> st;
+        quant_pass<T, D, QMODE>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
+        quant_finish<D, QMODE>(st);
+        // partial (m, l, o) of this run: o staged through shared memory so
+        // the G x D rows go out in 16-byte stores
+        __syncwarp();
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int dl = g * DS + mt, dh = g * DS + mt + MT;
+            sm_o[warp][2 * c][dl] = st.o[mt][0];
+            sm_o[warp][2 * c + 1][dl] = st.o[mt][1];
+            sm_o[warp][2 * c][dh] = st.o[mt][2];
+            sm_o[warp][2 * c + 1][dh] = st.o[mt][3];
+        }
+        __syncwarp();
+        const int64_t slot = i + static_cast<int64_t>(sp.b) * a.hkv + sp.kvh;
+        float4* po = reinterpret_cast<float4*>(a.ws_o + slot * a.G * D);
+        const float4* so = reinterpret_cast<const float4*>(&sm_o[warp][0][0]);
+        for (int x = lane; x < a.G * D / 4; x += 32) po[x] = so[x];
+        if (g == 0) {
+            float* pml = a.ws_ml + slot * a.G * 2;
+            if (2 * c < a.G) {
+                pml[4 * c] = st.m0;
+                pml[4 * c + 1] = st.l0;
+            }
+            if (2 * c + 1 < a.G) {
+                pml[4 * c + 2] = st.m1;
+                pml[4 * c + 3] = st.l1;
+            }
+        }
+    }
+}
+
+template <typename T, int D, int QMODE>
+void launch_balanced(const QDecodeArgs& a, int batch, int nwt, cudaStream_t st) {
+    paged_decode_quant_balanced_kernel<T, D, QMODE><<<(nwt + NW - 1) / NW, NW * 32, 0, st>>>(a, batch, nwt);
+}
+
+int run_balanced(const QDecodeArgs& a, int D, int qmode, int dtype, int batch, int nwt, cudaStream_t st) {
+#define PKV_QBLAUNCH(TT, DD, QM) launch_balanced<TT, DD, QM>(a, batch, nwt, st)
+    if (dtype == PKV_DTYPE_BF16) {
+        if (qmode == PKV_QMODE_INT4_ASYM) {
+            if (D == 128) PKV_QBLAUNCH(__nv_bfloat16, 128, PKV_QMODE_INT4_ASYM);
+            else PKV_QBLAUNCH(__nv_bfloat16, 64, PKV_QMODE_INT4_ASYM);
+        } else {
+            if (D == 128) PKV_QBLAUNCH(__nv_bfloat16, 128, PKV_QMODE_FP8_E4M3);
+            else PKV_QBLAUNCH(__nv_bfloat16, 64, PKV_QMODE_FP8_E4M3);
+        }
+    } else {
+        if (qmode == PKV_QMODE_INT4_ASYM) {
+            if (D == 128) PKV_QBLAUNCH(__half, 128, PKV_QMODE_INT4_ASYM);
+            else PKV_QBLAUNCH(__half, 64, PKV_QMODE_INT4_ASYM);
+        } else {
+            if (D == 128) PKV_QBLAUNCH(__half, 128, PKV_QMODE_FP8_E4M3);
+            else PKV_QBLAUNCH(__half, 64, PKV_QMODE_FP8_E4M3);
+        }
+    }
+#undef PKV_QBLAUNCH
+    return launch_status();
+}
+
 template <typename T, int D, int QMODE, bool SPLIT>
 void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
     dim3 grid(SPLIT ? parts : 1, hkv, batch);
-    paged_decode_quant_kernel<T, D, QMODE, SPLIT, kBlocksPerStep<QMODE>><<<grid, NW * 32, 0, st>>>(a);
+    paged_decode_quant_kernel<T, D, QMODE, SPLIT><<<grid, NW * 32, 0, st>>>(a);
 }
 
 template <bool SPLIT>
@@ -646,6 +776,22 @@ extern "C" int pkv_paged_attention_decode_quant(
     a.ws_ml = nullptr;
     a.status = st;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (partition_size == 0 && a.max_parts > 1 && pkv::use_balanced(batch, num_kv_heads, max_blocks)) {
+        // balanced split, all CTAs resident: kCtasPerSm CTAs of NW warps per SM
+        const int per_sm = pkv::NW * (qmode == PKV_QMODE_INT4_ASYM ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM>
+                                                               : pkv::kCtasPerSm<PKV_QMODE_FP8_E4M3>);
+        const int nwt = pkv::balanced_warps(static_cast<int64_t>(batch) * num_kv_heads * max_blocks, per_sm);
+        const size_t rows = static_cast<size_t>(nwt) * a.G + static_cast<size_t>(batch) * num_q_heads;
+        if (!workspace || workspace_bytes < pkv::balanced_bytes(batch, num_q_heads, a.G, head_dim, nwt))
+            return PKV_ERR_WORKSPACE;
+        if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
+        a.ws_o = static_cast<float*>(workspace);
+        a.ws_ml = a.ws_o + rows * head_dim;
+        int r = pkv::run_balanced(a, head_dim, qmode, dtype, batch, nwt, cs);
+        if (r != PKV_OK) return r;
+        return pkv::launch_balanced_merge(context_lens, batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                          nwt, a.ws_o, a.ws_ml, out, dtype, cs);
+    }
     if (a.max_parts <= 1) {
         a.part_blocks = max_blocks > 0 ? max_blocks : 1;
         return pkv::run<false>(a, head_dim, qmode, dtype, 1, num_kv_heads, batch, cs);

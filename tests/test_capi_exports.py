@@ -83,13 +83,13 @@ def _sms():
 
 
 def test_workspace_bytes_automatic(pkv):
-    # automatic split on tables of >= 32 items per launched warp (16 warps
-    # per SM; items = batch x Hq x max_blocks bounds batch x Hkv x blocks):
-    # room for the balanced split (partial rows for a GQA group of up to 8 per
-    # warp, one row per (sequence, query head)) and for the automatic
-    # partitions, whichever is more
-    nwt = 16 * _sms()
-    assert 4 * 32 * 4096 >= 32 * nwt
+    # automatic split on tables of >= 32 items per 16 warps per SM (items =
+    # batch x Hq x max_blocks bounds batch x Hkv x blocks): room for the
+    # balanced split (partial rows for a GQA group of up to 8 per warp, up to
+    # 20 warps per SM, one row per (sequence, query head)) and for the
+    # automatic partitions, whichever is more
+    nwt = 20 * _sms()
+    assert 4 * 32 * 4096 >= 32 * 16 * _sms()
     balanced = (nwt * 8 + 4 * 32) * 130 * 4
     fixed = 4 * 32 * 128 * 130 * 4
     assert pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0) == max(balanced, fixed)
@@ -100,7 +100,7 @@ def test_workspace_bytes_automatic(pkv):
     assert pkv.pkv_decode_workspace_bytes(1025, 32, 128, 64, 16, 0) == \
         pkv.pkv_decode_workspace_bytes(1025, 32, 128, 64, 16, 512)
     # small tables: the automatic partitions only (64 tokens here)
-    assert 3 * 8 * 19 < 32 * nwt
+    assert 3 * 8 * 19 < 32 * 16 * _sms()
     assert pkv.pkv_decode_workspace_bytes(3, 8, 128, 19, 16, 0) == 3 * 8 * 5 * 130 * 4
     # one partition covers everything: single pass, no workspace
     assert pkv.pkv_decode_workspace_bytes(3, 8, 64, 3, 16, 0) == 0

@@ -147,3 +147,51 @@ def test_fused_append_rejects_wrong_slot(pkv, cuda_dev):
     blk, off = divmod(int(slots[i]), 16)
     assert (c.k_pool[blk, :, off] == 0).all()
     assert pkv.pkv_device_status() == 0
+
+
+def _decode_quant(pkv, c, lens=None):
+    w = c.w
+    B = len(c.decoded)
+    out = torch.full((B, w["hq"], w["d"]), 7.0, dtype=w["torch_dtype"], device=c.q.device)
+    n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, 0)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device=c.q.device)
+    pkv.pkv_paged_attention_decode_quant(c.q, c.cache, c.n_sink, c.tables, c.lens if lens is None else lens,
+                                         w["scale"], out, c.quant, c.group_size, ws, 0)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+def _short_quant_workload(n=640, hi=320, **over):
+    rng = np.random.default_rng(12)
+    lens = [int(x) for x in rng.integers(1, hi + 1, size=n)]
+    base = dict(lens=lens, num_blocks=sum(-(-L // 16) for L in lens) + n + 64)
+    base.update(over)
+    return syn.workload("quant", **base)
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_quant_many_short_sequences_with_sinks(pkv, cuda_dev, qmode):
+    """Hundreds of 1..320-token sequences (many shorter than the 4 sinks):
+    runs start and end inside warp ranges, and the sink block of each run is
+    taken by whichever warp's range holds it."""
+    w = _short_quant_workload()
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    assert _is_balanced(c)
+    got = _decode_quant(pkv, c)
+    assert pkv.pkv_device_status() == 0
+    assert_close(got, expected(c), what="%s, 640 short sequences" % qmode)
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_quant_zero_contexts_and_head64_group8(pkv, cuda_dev, qmode):
+    w = _short_quant_workload(n=700, hi=300, hq=64, hkv=8, d=64, dtype="fp16", group_size=64)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    assert _is_balanced(c)
+    zero = [0, 5, 6, 699]
+    lens = c.lens.clone()
+    lens[zero] = 0
+    got = _decode_quant(pkv, c, lens)
+    assert pkv.pkv_device_status() == 0
+    assert (got[zero] == 0).all()
+    keep = [i for i in range(len(c.decoded)) if i not in zero]
+    assert_close(got[keep], expected(c, keep), what="%s, G 8, D 64" % qmode)
