@@ -43,8 +43,18 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; sequences/s per layer"
 KV_BYTES_PER_TOKEN = 2 * 8 * 128 * 2  # K and V, 8 KV heads, head dim 128, bf16
 NOMINAL_HBM_GBS = 8000.0
-DECODE_SOURCES = ["paged_kv_cache_13_gb300/csrc/decode.cu", "paged_kv_cache_13_gb300/csrc/common.cuh"]
-TRAFFIC_FILE = "profiles/paged_decode_bf16_llama3_8b_b64_traffic.txt"
+_CSRC = "paged_kv_cache_13_gb300/csrc/"
+# workload -> (committed ncu traffic summary of its decode kernel, the sources
+# that kernel is built from); the traffic is reported only while they hash
+# to the summary's source_sha256_16
+TRAFFIC = {
+    "llama3_8b_b64": ("profiles/paged_decode_bf16_llama3_8b_b64_traffic.txt",
+                      [_CSRC + "decode.cu", _CSRC + "common.cuh", _CSRC + "balanced.cuh"]),
+    "quant_int4": ("profiles/paged_decode_quant_int4_32x16k_traffic.txt",
+                   [_CSRC + "decode_quant.cu", _CSRC + "common.cuh", _CSRC + "balanced.cuh"]),
+    "quant_fp8": ("profiles/paged_decode_quant_fp8_32x16k_traffic.txt",
+                  [_CSRC + "decode_quant.cu", _CSRC + "common.cuh", _CSRC + "balanced.cuh"]),
+}
 
 # name -> (synthetic workload, overrides, cache mode)
 WORKLOADS = {
@@ -121,18 +131,22 @@ def measured_peak():
         return 6800.0, "fallback"
 
 
-def source_digest():
+def source_digest(sources):
     h = hashlib.sha256()
-    for rel in DECODE_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kv_bytes_per_launch):
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, scaled to this launch; None if the kernel changed since."""
-    p = os.path.join(ROOT, TRAFFIC_FILE)
+def recorded_traffic(workload, kv_bytes_per_launch):
+    """DRAM bytes per launch of the workload's decode kernel from the
+    committed ncu summary, scaled to this launch; None if there is none or
+    the kernel changed since."""
+    if workload not in TRAFFIC:
+        return None
+    rel, sources = TRAFFIC[workload]
+    p = os.path.join(ROOT, rel)
     if not os.path.exists(p):
         return None
     vals = {}
@@ -141,7 +155,7 @@ def recorded_traffic(kv_bytes_per_launch):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-    if vals.get("source_sha256_16") != source_digest():
+    if vals.get("source_sha256_16") != source_digest(sources):
         return None
     try:
         per_kv_byte = float(vals["dram_bytes_per_launch"]) / float(vals["kv_bytes_per_launch"])
@@ -702,7 +716,7 @@ def main():
                           if peak_kind == "measured" else "fallback"),
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": recorded_traffic(res["kv_bytes"]) if args.workload == "llama3_8b_b64" else None,
+            "traffic": recorded_traffic(args.workload, res["kv_bytes"]),
             "algorithmic_bytes_per_launch": res["kv_bytes"],
             "avg_launch_ms": res["call_ms"],
         },
