@@ -428,11 +428,39 @@ def run_device(args, rank, world, dist):
 
     # ---------- end to end through the public API, host buffers
     e2e = run_e2e(pkv, torch, cache, e2e_steps, dist, device)
+    prefix = prefix_cache_timing(pkv, cache) if "prompt" in cache.w else None
 
     return dict(ms_per_step=ms_per_step, call_ms=call_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
+                prefix=prefix,
                 B=cache.B, launches=cache.launches_per_step() * args.steps,
                 unique_blocks=cache.unique_blocks, partition_size=cache.partition_size,
                 split_desc=cache.split_desc)
+
+
+def prefix_cache_timing(pkv, cache, iters=2000):
+    """Host prefix cache on the prefix workload's pool: the prompt holder's
+    blocks are registered under seeded token ids, then each iteration maps a
+    new request (the prompt plus 64 tokens of its own) onto them and releases
+    it -- the lookup a request pays before its prefill.  The cache is cleared
+    afterwards, so the decode state is unchanged."""
+    w = cache.w
+    tokens = np.random.default_rng(np.random.SeedSequence([w["seed"], 99])).integers(
+        0, 128256, size=w["prompt"] + 64).astype(np.int32)
+    holder = 0  # the prompt's own sequence (created first)
+    t0 = time.perf_counter()
+    entries = pkv.pkv_prefix_register(cache.pool, holder, tokens[:w["prompt"]])
+    reg_us = (time.perf_counter() - t0) * 1e6
+    matched = 0
+    t0 = time.perf_counter()
+    for _ in range(iters):
+        seq, matched = pkv.pkv_prefix_match(cache.pool, tokens)
+        pkv.pkv_seq_free(cache.pool, seq)
+    match_us = (time.perf_counter() - t0) * 1e6 / iters
+    pkv.pkv_prefix_clear(cache.pool)
+    return {"register_us": round(reg_us, 2), "match_and_release_us": round(match_us, 2),
+            "prompt_tokens": int(w["prompt"]), "request_tokens": int(tokens.shape[0]),
+            "matched_tokens": int(matched), "entries": int(entries), "iterations": iters,
+            "note": "host C++ through the C ABI (ctypes call overhead included), one thread"}
 
 
 def run_e2e(pkv, torch, cache, steps, dist, device):
@@ -733,6 +761,8 @@ def main():
     }
     if args.workload == "prefix_cow":
         line["unique_kv_bytes_per_step"] = res["unique_blocks"] * 16 * KV_BYTES_PER_TOKEN
+    if res.get("prefix"):
+        line["prefix_cache"] = res["prefix"]
     print(json.dumps(line))
 
 

@@ -171,6 +171,43 @@ int pkv_build_block_tables(const pkv_pool* pool, const int64_t* seqs, int32_t n,
  * n < 0 disables. */
 int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
 
+/* ========================================================= prefix cache */
+
+/* Prefix cache ("Capítulo 8 — Gerenciamento de KV Cache de Próxima Geração",
+ * §8.3): prompts are cut into block_size-token chunks; a chunk already
+ * computed under the same preceding chunks maps the cached physical block
+ * into a new request's table, so its prefill is skipped.  An entry is one
+ * full block keyed by (previous entry, its block_size token ids), compared
+ * exactly (a 64-bit hash only buckets candidates).  The cache holds one
+ * reference on every entry's block.  Token ids are opaque int32 values. */
+
+/* Registers the full blocks of seq holding tokens[0 .. n_tokens) (the first
+ * floor(n_tokens / block_size) blocks of its table; n_tokens <= its length).
+ * Chunks already cached are skipped (the chain continues through them).
+ * n_new (nullable): entries added. */
+int pkv_prefix_register(pkv_pool* pool, int64_t seq, const int32_t* tokens, int32_t n_tokens,
+                        int32_t* n_new);
+
+/* Creates a sequence whose table is the longest chain of cached full blocks
+ * matching tokens (each block's refcount + 1) and whose length is
+ * matched_tokens (a multiple of block_size, <= n_tokens, 0 on a miss).  The
+ * caller prefills tokens[matched_tokens ..] with pkv_seq_append. */
+int pkv_prefix_match(pkv_pool* pool, const int32_t* tokens, int32_t n_tokens, int64_t* seq_out,
+                     int32_t* matched_tokens);
+
+/* Drops up to n_blocks entries, least recently matched or registered first,
+ * among leaves (no cached chunk extends them) whose block no sequence holds;
+ * their blocks return to the free stack.  n_freed (nullable): entries
+ * dropped. */
+int pkv_prefix_evict(pkv_pool* pool, int32_t n_blocks, int32_t* n_freed);
+
+/* Drops every entry, releasing the cache's references in registration
+ * order. */
+int pkv_prefix_clear(pkv_pool* pool);
+
+/* Entries held, pkv_prefix_match calls, and blocks those calls matched. */
+int pkv_prefix_stats(const pkv_pool* pool, int64_t* entries, int64_t* lookups, int64_t* hit_blocks);
+
 /* ================================================================ sizes */
 
 /* Bytes of the split-K workspace pkv_paged_attention_decode* needs for this

@@ -178,3 +178,97 @@ class KVCacheManager:
         for sid in sids:
             s.update(self.tables[sid])
         return len(s)
+
+
+class PrefixCache:
+    """Global cache of computed full blocks over one ``KVCacheManager``.
+
+    "Capítulo 8 — Gerenciamento de KV Cache de Próxima Geração", §8.3: the
+    prompt is cut into block-sized chunks; a chunk whose block is already in
+    the cache is mapped into the new request's table and its prefill
+    skipped; otherwise the prefill runs and the resulting block is
+    registered.  A chunk's identity here is the whole token prefix up to and
+    including it (the tuple of token ids itself, so equal chunks after
+    different prefixes are different entries and nothing can collide).  The
+    cache holds one reference on each entry's block.  Eviction (the pages
+    give no policy): least recently used first, among entries no other
+    entry extends and whose block no sequence holds.
+    """
+
+    def __init__(self, manager):
+        self.m = manager
+        self.entries = {}    # prefix tuple -> [block, last_use]
+        self.clock = 0
+        self.lookups = 0
+        self.hit_blocks = 0
+        self._order = {}     # prefix tuple -> creation index (tie-break)
+        self._created = 0
+
+    def register(self, sid, tokens):
+        """Registers the full blocks of ``sid`` holding ``tokens``; returns
+        the number of entries added."""
+        bs = self.m.block_size
+        tokens = [int(t) for t in tokens]
+        if len(tokens) > self.m.length(sid):
+            raise ValueError("more tokens than the sequence holds")
+        table = self.m.table(sid)
+        added = 0
+        for i in range(len(tokens) // bs):
+            key = tuple(tokens[:(i + 1) * bs])
+            if key in self.entries:
+                continue
+            self.clock += 1
+            self.entries[key] = [table[i], self.clock]
+            self._order[key] = self._created
+            self._created += 1
+            self.m.pool.incref(table[i])
+            added += 1
+        return added
+
+    def match(self, tokens):
+        """New sequence whose table is the longest cached chain of full
+        blocks matching ``tokens``; returns ``(sid, matched_tokens)``."""
+        bs = self.m.block_size
+        tokens = [int(t) for t in tokens]
+        self.clock += 1
+        blocks = []
+        for i in range(len(tokens) // bs):
+            key = tuple(tokens[:(i + 1) * bs])
+            if key not in self.entries:
+                break
+            self.entries[key][1] = self.clock
+            blocks.append(self.entries[key][0])
+        sid = self.m.create()
+        for b in blocks:
+            self.m.pool.incref(b)
+        self.m.tables[sid] = blocks
+        self.m.lens[sid] = len(blocks) * bs
+        self.lookups += 1
+        self.hit_blocks += len(blocks)
+        return sid, len(blocks) * bs
+
+    def _is_leaf(self, key):
+        bs = self.m.block_size
+        return not any(len(k) == len(key) + bs and k[:len(key)] == key for k in self.entries)
+
+    def evict(self, n_blocks):
+        """Drops up to ``n_blocks`` entries; returns how many were dropped."""
+        freed = 0
+        while freed < n_blocks:
+            cands = [k for k, (b, _) in self.entries.items()
+                     if self.m.pool.ref[b] == 1 and self._is_leaf(k)]
+            if not cands:
+                break
+            victim = min(cands, key=lambda k: (self.entries[k][1], self._order[k]))
+            b = self.entries.pop(victim)[0]
+            del self._order[victim]
+            self.m.pool.decref(b)
+            freed += 1
+        return freed
+
+    def clear(self):
+        """Drops every entry, releasing the blocks in registration order."""
+        for b, _ in self.entries.values():
+            self.m.pool.decref(b)
+        self.entries.clear()
+        self._order.clear()

@@ -65,6 +65,11 @@ _SIGS = {
     "pkv_seq_block_table": ([_vp, _i64, _vp, _i32], _int),
     "pkv_build_block_tables": ([_vp, _vp, _i32, _vp, _i32, _vp], _int),
     "pkv_debug_fail_after": ([_vp, _i64], _int),
+    "pkv_prefix_register": ([_vp, _i64, _vp, _i32, _p_i32], _int),
+    "pkv_prefix_match": ([_vp, _vp, _i32, _p_i64, _p_i32], _int),
+    "pkv_prefix_evict": ([_vp, _i32, _p_i32], _int),
+    "pkv_prefix_clear": ([_vp], _int),
+    "pkv_prefix_stats": ([_vp, _p_i64, _p_i64, _p_i64], _int),
     "pkv_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _int),
     "pkv_decode_auto_partition_size": ([_i32, _i32, _i32, _i32, _p_i32], _int),
     "pkv_kv_append": ([_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _int, _vp], _int),
@@ -271,6 +276,40 @@ def pkv_build_block_tables(pool, seqs, max_blocks, tables_out=None, lens_out=Non
 
 def pkv_debug_fail_after(pool, n_allocs):
     _check(lib.pkv_debug_fail_after(pool, n_allocs), "pkv_debug_fail_after")
+
+
+def pkv_prefix_register(pool, seq, tokens):
+    """Registers seq's full blocks holding tokens; returns entries added."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    n = _i32()
+    _check(lib.pkv_prefix_register(pool, seq, _ptr(tokens), tokens.shape[0], ctypes.byref(n)),
+           "pkv_prefix_register")
+    return n.value
+
+
+def pkv_prefix_match(pool, tokens):
+    """New sequence mapped onto the longest cached prefix: (seq, matched tokens)."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    seq, m = _i64(), _i32()
+    _check(lib.pkv_prefix_match(pool, _ptr(tokens), tokens.shape[0], ctypes.byref(seq),
+                                ctypes.byref(m)), "pkv_prefix_match")
+    return seq.value, m.value
+
+
+def pkv_prefix_evict(pool, n_blocks):
+    return _out_i32("pkv_prefix_evict", pool, n_blocks)
+
+
+def pkv_prefix_clear(pool):
+    _check(lib.pkv_prefix_clear(pool), "pkv_prefix_clear")
+
+
+def pkv_prefix_stats(pool):
+    """(entries, lookups, matched blocks)."""
+    e, l, h = _i64(), _i64(), _i64()
+    _check(lib.pkv_prefix_stats(pool, ctypes.byref(e), ctypes.byref(l), ctypes.byref(h)),
+           "pkv_prefix_stats")
+    return e.value, l.value, h.value
 
 
 def pkv_decode_workspace_bytes(batch, num_q_heads, head_dim, max_blocks, block_size=16,

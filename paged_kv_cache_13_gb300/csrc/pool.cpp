@@ -9,7 +9,19 @@
 // shared tail ("The 8GB VRAM Breakthrough", §3 "Copy-on-Write (CoW) Prefix
 // Sharing").  Appends count every block they need before touching anything,
 // so a failure leaves the state unchanged.
+//
+// Prefix cache ("Capítulo 8 — Gerenciamento de KV Cache de Próxima Geração",
+// §8.3: hash the prompt in block-sized chunks; a chunk already in the global
+// cache of computed blocks is mapped into the new request's table and its
+// prefill skipped; otherwise the prefill runs and the block is registered).
+// An entry is one full block, keyed by its parent entry (the entry of the
+// previous block, so equal chunks at different prefixes differ) and its
+// block_size token ids; the 64-bit hash only buckets candidates, which are
+// then compared exactly.  The cache holds one reference on each entry's
+// block, so cached blocks outlive the sequences that computed them until
+// evicted (least recently used first, leaves only, blocks no one else holds).
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -25,6 +37,28 @@ struct Seq {
     int64_t len = 0;
 };
 
+struct PrefixEntry {
+    int32_t block = -1;           // physical block (one reference held by the cache)
+    int64_t parent = -1;          // entry of the previous block, -1 for the first
+    std::vector<int32_t> tokens;  // the block's token ids
+    uint64_t last_use = 0;        // LRU clock
+    int32_t children = 0;         // entries whose parent is this one
+};
+
+// 64-bit hash of the parent id and the chunk's token ids: FNV-1a over
+// 32-bit words (buckets only: candidates are compared exactly).
+uint64_t chunk_hash(int64_t parent, const int32_t* tokens, int32_t n) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&h](uint32_t x) {
+        h ^= x;
+        h *= 1099511628211ull;
+    };
+    mix(static_cast<uint32_t>(static_cast<uint64_t>(parent)));
+    mix(static_cast<uint32_t>(static_cast<uint64_t>(parent) >> 32));
+    for (int32_t i = 0; i < n; ++i) mix(static_cast<uint32_t>(tokens[i]));
+    return h ^ (h >> 29);
+}
+
 }  // namespace
 
 struct pkv_pool {
@@ -35,6 +69,39 @@ struct pkv_pool {
     std::unordered_map<int64_t, Seq> seqs;
     int64_t next_seq = 0;
     int64_t fail_after = -1;  // allocations left before injected failures
+
+    // prefix cache
+    std::unordered_map<int64_t, PrefixEntry> entries;
+    std::unordered_multimap<uint64_t, int64_t> index;  // chunk hash -> entry
+    int64_t next_entry = 0;
+    uint64_t clock = 0;
+    int64_t lookups = 0, hit_blocks = 0;
+
+    // The entry for (parent, chunk), or -1.
+    int64_t find_entry(int64_t parent, const int32_t* tokens) const {
+        auto range = index.equal_range(chunk_hash(parent, tokens, block_size));
+        for (auto it = range.first; it != range.second; ++it) {
+            const PrefixEntry& e = entries.at(it->second);
+            if (e.parent == parent &&
+                std::memcmp(e.tokens.data(), tokens, sizeof(int32_t) * block_size) == 0)
+                return it->second;
+        }
+        return -1;
+    }
+
+    void drop_entry(int64_t id) {
+        PrefixEntry& e = entries.at(id);
+        auto range = index.equal_range(chunk_hash(e.parent, e.tokens.data(), block_size));
+        for (auto it = range.first; it != range.second; ++it) {
+            if (it->second == id) {
+                index.erase(it);
+                break;
+            }
+        }
+        if (e.parent >= 0) --entries.at(e.parent).children;
+        decref(e.block);
+        entries.erase(id);
+    }
 
     // Blocks that can actually be allocated right now (injection included).
     int64_t allocatable() const {
@@ -322,6 +389,115 @@ int pkv_build_block_tables(const pkv_pool* pool, const int64_t* seqs, int32_t n,
         for (int32_t j = static_cast<int32_t>(nb); j < max_blocks; ++j) row[j] = -1;
         context_lens[i] = static_cast<int32_t>(s.len);
     }
+    return PKV_OK;
+}
+
+int pkv_prefix_register(pkv_pool* pool, int64_t seq, const int32_t* tokens, int32_t n_tokens,
+                        int32_t* n_new) {
+    if (!pool) return PKV_ERR_BAD_HANDLE;
+    if (n_tokens < 0 || (n_tokens > 0 && !tokens)) return PKV_ERR_INVALID_ARG;
+    auto it = pool->seqs.find(seq);
+    if (it == pool->seqs.end()) return PKV_ERR_BAD_SEQ;
+    const Seq& s = it->second;
+    if (n_tokens > s.len) return PKV_ERR_INVALID_ARG;
+    const int32_t bs = pool->block_size;
+    const int32_t full = n_tokens / bs;
+    int32_t added = 0;
+    int64_t parent = -1;
+    for (int32_t i = 0; i < full; ++i) {
+        const int32_t* chunk = tokens + static_cast<int64_t>(i) * bs;
+        int64_t id = pool->find_entry(parent, chunk);
+        if (id < 0) {
+            // a new full block: the cache takes a reference on the sequence's block
+            id = pool->next_entry++;
+            PrefixEntry e;
+            e.block = s.table[i];
+            e.parent = parent;
+            e.tokens.assign(chunk, chunk + bs);
+            e.last_use = ++pool->clock;
+            ++pool->ref[e.block];
+            if (parent >= 0) ++pool->entries.at(parent).children;
+            pool->index.emplace(chunk_hash(parent, chunk, bs), id);
+            pool->entries.emplace(id, std::move(e));
+            ++added;
+        }
+        parent = id;
+    }
+    if (n_new) *n_new = added;
+    return PKV_OK;
+}
+
+int pkv_prefix_match(pkv_pool* pool, const int32_t* tokens, int32_t n_tokens, int64_t* seq_out,
+                     int32_t* matched_tokens) {
+    if (!pool) return PKV_ERR_BAD_HANDLE;
+    if (!seq_out || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PKV_ERR_INVALID_ARG;
+    const int32_t bs = pool->block_size;
+    Seq s;
+    int64_t parent = -1;
+    const uint64_t now = ++pool->clock;
+    for (int32_t i = 0; i < n_tokens / bs; ++i) {
+        const int64_t id = pool->find_entry(parent, tokens + static_cast<int64_t>(i) * bs);
+        if (id < 0) break;
+        PrefixEntry& e = pool->entries.at(id);
+        e.last_use = now;
+        s.table.push_back(e.block);
+        parent = id;
+    }
+    for (int32_t b : s.table) ++pool->ref[b];
+    s.len = static_cast<int64_t>(s.table.size()) * bs;
+    ++pool->lookups;
+    pool->hit_blocks += static_cast<int64_t>(s.table.size());
+    const int64_t id = pool->next_seq++;
+    if (matched_tokens) *matched_tokens = static_cast<int32_t>(s.len);
+    pool->seqs.emplace(id, std::move(s));
+    *seq_out = id;
+    return PKV_OK;
+}
+
+int pkv_prefix_evict(pkv_pool* pool, int32_t n_blocks, int32_t* n_freed) {
+    if (!pool) return PKV_ERR_BAD_HANDLE;
+    if (n_blocks < 0) return PKV_ERR_INVALID_ARG;
+    int32_t freed = 0;
+    while (freed < n_blocks) {
+        // least recently used leaf whose block only the cache holds
+        int64_t victim = -1;
+        uint64_t oldest = 0;
+        for (const auto& kv : pool->entries) {
+            const PrefixEntry& e = kv.second;
+            if (e.children != 0 || pool->ref[e.block] != 1) continue;
+            if (victim < 0 || e.last_use < oldest || (e.last_use == oldest && kv.first < victim)) {
+                victim = kv.first;
+                oldest = e.last_use;
+            }
+        }
+        if (victim < 0) break;
+        pool->drop_entry(victim);
+        ++freed;
+    }
+    if (n_freed) *n_freed = freed;
+    return PKV_OK;
+}
+
+int pkv_prefix_clear(pkv_pool* pool) {
+    if (!pool) return PKV_ERR_BAD_HANDLE;
+    // release in registration order (the blocks return to the free stack in
+    // a defined order)
+    std::vector<int64_t> ids;
+    ids.reserve(pool->entries.size());
+    for (const auto& kv : pool->entries) ids.push_back(kv.first);
+    std::sort(ids.begin(), ids.end());
+    for (int64_t id : ids) pool->decref(pool->entries.at(id).block);
+    pool->entries.clear();
+    pool->index.clear();
+    return PKV_OK;
+}
+
+int pkv_prefix_stats(const pkv_pool* pool, int64_t* entries, int64_t* lookups, int64_t* hit_blocks) {
+    if (!pool) return PKV_ERR_BAD_HANDLE;
+    if (!entries || !lookups || !hit_blocks) return PKV_ERR_INVALID_ARG;
+    *entries = static_cast<int64_t>(pool->entries.size());
+    *lookups = pool->lookups;
+    *hit_blocks = pool->hit_blocks;
     return PKV_OK;
 }
 
