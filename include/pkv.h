@@ -320,6 +320,32 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
                                      const void* workspace, size_t workspace_bytes, void* out,
                                      int dtype, void* stream);
 
+/* Multi-query paged attention: several new query tokens per sequence, each
+ * attending causally to the cache up to its own position -- the target
+ * model's one parallel pass over the gamma + 1 draft tokens of speculative
+ * decoding ("The 8GB VRAM Breakthrough", §6), or one slice of a chunked
+ * prefill (§5, "Chunked Prefill").
+ *   q: [T, num_q_heads, head_dim] (dtype), T = q_start[batch]; the queries
+ *     of sequence b are rows q_start[b] .. q_start[b+1] - 1 (device int32
+ *     [batch + 1], non-decreasing; L_b = q_start[b+1] - q_start[b] <=
+ *     max_q_len, which sizes the grid).
+ *   The L_b new tokens are the last L_b of the context_lens[b] tokens in the
+ *   pool (written before the call, e.g. by pkv_kv_append), so query i of
+ *   sequence b sits at position p = context_lens[b] - L_b + i and
+ *   out[q_start[b] + i, h] = sum_{t <= p} softmax_t(scale <q, K_t>) V_t
+ *   over KV head h / (num_q_heads / num_kv_heads).  out: [T, num_q_heads,
+ *   head_dim] (dtype).  L_b = 1 is pkv_paged_attention_decode.
+ *   context_lens[b] < L_b sets PKV_STATUS_BAD_CONTEXT; rows at negative
+ *   positions get zeros.  No workspace; one pass per (8 or 16 query rows,
+ *   KV head, sequence).
+ * Supported: block_size 16, head_dim 64 or 128, 1 <= G <= 8. */
+int pkv_paged_attention_multi_query(const void* q, const int32_t* q_start, const void* k_pool,
+                                    const void* v_pool, const int32_t* block_tables,
+                                    const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                    int32_t block_size, int32_t max_blocks, int32_t max_q_len,
+                                    float scale, void* out, int dtype, void* stream);
+
 /* Allocation-free decode.  The source pages have no counterpart for this
  * entry point: it exists for callers that cannot provide a device workspace
  * -- code running while a stream is captured into a CUDA graph (allocation

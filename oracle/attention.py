@@ -111,3 +111,54 @@ def sequence_attention(q_seq, k_seq, v_seq, scale):
         g = h // G
         out[h] = attention_reference(q_seq[h], k_seq[:, g, :], v_seq[:, g, :], scale)
     return out
+
+
+def multi_query_attention(q_rows, k_seq, v_seq, scale):
+    """Causal attention of L new query tokens of one sequence.
+
+    The L queries are the last L of the sequence's ctx tokens ("The 8GB VRAM
+    Breakthrough", §6: the target model's one parallel pass over the
+    gamma + 1 draft tokens; §5: a slice of a chunked prefill), so query i
+    sits at position p = ctx - L + i and attends to tokens 0..p.
+    q_rows: [L, Hq, D]; k_seq, v_seq: [ctx, Hkv, D] in logical order.
+    Returns float64 [L, Hq, D]; a query at a negative position (ctx < L)
+    gets zeros.
+    """
+    q_rows = np.asarray(q_rows, dtype=np.float64)
+    L, Hq, D = q_rows.shape
+    ctx, Hkv = k_seq.shape[0], k_seq.shape[1]
+    G = Hq // Hkv
+    out = np.zeros((L, Hq, D), dtype=np.float64)
+    for i in range(L):
+        p = ctx - L + i
+        if p < 0:
+            continue
+        for h in range(Hq):
+            g = h // G
+            out[i, h] = attention_reference(q_rows[i, h], k_seq[:p + 1, g, :], v_seq[:p + 1, g, :], scale)
+    return out
+
+
+def paged_multi_query_attention(q, q_start, k_pool, v_pool, block_tables, context_lens, scale,
+                                block_size=16):
+    """Multi-query attention through block tables.
+
+    q: [T, Hq, D] with sequence b's queries at rows q_start[b] .. q_start[b+1]-1;
+    pools [num_blocks, Hkv, block_size, D]; context_lens include the new
+    tokens.  Returns float64 [T, Hq, D].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    T, Hq, D = q.shape
+    Hkv = k_pool.shape[1]
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    for b in range(len(context_lens)):
+        lo, hi = int(q_start[b]), int(q_start[b + 1])
+        if hi == lo:
+            continue
+        ctx = int(context_lens[b])
+        k = np.stack([gather_tokens(k_pool, block_tables[b], ctx, g, block_size) for g in range(Hkv)], axis=1) \
+            if ctx else np.zeros((0, Hkv, D))
+        v = np.stack([gather_tokens(v_pool, block_tables[b], ctx, g, block_size) for g in range(Hkv)], axis=1) \
+            if ctx else np.zeros((0, Hkv, D))
+        out[lo:hi] = multi_query_attention(q[lo:hi], k, v, scale)
+    return out

@@ -73,6 +73,9 @@ _SIGS = {
     "pkv_decode_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)], _int),
     "pkv_decode_auto_partition_size": ([_i32, _i32, _i32, _i32, _p_i32], _int),
     "pkv_kv_append": ([_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _int, _vp], _int),
+    "pkv_paged_attention_multi_query": (
+        [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
+         _int, _vp], _int),
     "pkv_paged_attention_decode": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
          _i32, _int, _vp], _int),
@@ -345,6 +348,20 @@ def pkv_paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, sc
         _ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens), B, Hq, Hkv, D,
         NB, BS, mb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, partition_size,
         _dtype_code(q), _stream(stream)), "pkv_paged_attention_decode")
+
+
+def pkv_paged_attention_multi_query(q, q_start, k_pool, v_pool, block_tables, context_lens, scale,
+                                    out, max_q_len, stream=None):
+    """q, out [T, Hq, D]; q_start int32 [B + 1] (sequence b's queries are rows
+    q_start[b] .. q_start[b+1]-1, the last of its context_lens[b] tokens)."""
+    T, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_pool.shape
+    B = q_start.shape[0] - 1
+    mb = block_tables.shape[1]
+    _check(lib.pkv_paged_attention_multi_query(
+        _ptr(q), _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
+        B, Hq, Hkv, D, NB, BS, mb, int(max_q_len), float(scale), _ptr(out), _dtype_code(q),
+        _stream(stream)), "pkv_paged_attention_multi_query")
 
 
 def pkv_paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,

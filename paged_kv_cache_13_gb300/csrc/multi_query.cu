@@ -1,0 +1,404 @@
+// Multi-query paged attention: several new query tokens per sequence, each
+// attending causally to the cache up to its own position.
+//
+// What it computes: sequence b holds ctx_b tokens in the pool (its block
+// table), the last L_b of which are this call's new tokens, at positions
+// ctx_b - L_b .. ctx_b - 1.  Query token i of b (row q_start[b] + i of q)
+// sits at position p = ctx_b - L_b + i and
+//   out[q_start[b] + i, h] = sum_{t <= p} softmax_t(scale <q, K_t>) V_t
+// with K_t, V_t of KV head h / G gathered through the table.  This is the
+// attention of the target model's one parallel pass over the gamma + 1
+// draft tokens of speculative decoding ("The 8GB VRAM Breakthrough", §6
+// "Speculative Decoding: Breaking the Bandwidth Wall") and of a 512-token
+// chunk of a chunked prefill (§5, "Chunked Prefill"); with L_b = 1 it is the
+// decode attention of decode.cu.
+//
+// Design: the layout of the decode kernels -- K and V fragments loaded
+// straight from the pool into mma.sync registers, tokens as M of QK^T and
+// the head dim as M of PV -- with the N dimension holding (query token,
+// query head) rows instead of heads: a CTA takes a tile of 8 NT rows of one
+// (sequence, KV head), NT n-tiles of 8, so every K/V fragment loaded is used
+// by all rows of the tile.  Its 4 warps take the blocks up to the tile's
+// last position round-robin, each with its own online softmax per row, and
+// merge through shared memory.  Rows beyond a token's position are masked
+// per element; blocks past the tile's last position are not read.
+
+#include "common.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int BS = 16;
+constexpr int NW = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.f;  // see the softmax in attend()
+
+struct MQArgs {
+    const void* q;
+    const int32_t* q_start;
+    const void* k_pool;
+    const void* v_pool;
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    int hq, hkv, G, num_blocks, max_blocks;
+    float scale_log2;
+    void* out;
+    int* status;
+};
+
+template <typename T>
+constexpr bool kSplitP = false;
+template <>
+constexpr bool kSplitP<__nv_bfloat16> = true;
+
+__device__ __forceinline__ float lo_float(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float hi_float(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+// Element e (0 .. D/8-1) of lane group g in the PV fragment layout sits at
+// head-dim column 64 * (e / 8) + 8 * g + e % 8.
+__device__ __forceinline__ int pv_col(int e, int g) { return 64 * (e >> 3) + 8 * g + (e & 7); }
+
+// Online-softmax state of one warp: lane (g, c) holds rows 8 nt + 2c and
+// 8 nt + 2c + 1 of every n-tile nt.
+template <int MT, int NT>
+struct MQState {
+    float m[NT][2], l[NT][2];
+    float o[MT][NT][4];
+};
+
+// Attend one 16-token block (physical id phys, logical index lb).  qs: the
+// lane's shared address of the tile's query fragments (n-tile nt, k-chunk i
+// at qs + (nt * KC + i) * 512); pos: the positions of the lane's rows (-1
+// for rows beyond the sequence's tokens).
+template <typename T, int D, int NT>
+__device__ __forceinline__ void attend(const MQArgs& a, int kvh, int lb, int phys, int ctx, uint32_t qs,
+                                       const int (&pos)[NT][2], MQState<D / 16, NT>& w, int g, int c) {
+    using H = Half16<T>;
+    constexpr int KC = D / 32;
+    constexpr int VC = D / 64;
+    constexpr int MT = D / 16;
+    const int64_t base = (static_cast<int64_t>(phys) * a.hkv + kvh) * (BS * D);
+    const T* kb = static_cast<const T*>(a.k_pool) + base;
+    const T* vb = static_cast<const T*>(a.v_pool) + base;
+
+    // K rows g, g + 8 at [32i + 8c, +8); V rows 2c, 2c+1, 8+2c, 9+2c at [64j + 8g, +8)
+    uint4 kr0[KC], kr1[KC], vr[4][VC];
+#pragma unroll
+    for (int i = 0; i < KC; ++i) {
+        kr0[i] = ldg_stream(kb + g * D + 32 * i + 8 * c);
+        kr1[i] = ldg_stream(kb + (g + 8) * D + 32 * i + 8 * c);
+    }
+#pragma unroll
+    for (int j = 0; j < VC; ++j) {
+        vr[0][j] = ldg_stream(vb + (2 * c) * D + 64 * j + 8 * g);
+        vr[1][j] = ldg_stream(vb + (2 * c + 1) * D + 64 * j + 8 * g);
+        vr[2][j] = ldg_stream(vb + (8 + 2 * c) * D + 64 * j + 8 * g);
+        vr[3][j] = ldg_stream(vb + (9 + 2 * c) * D + 64 * j + 8 * g);
+    }
+
+    const int tok0 = lb * BS + g, tok1 = tok0 + 8;
+    uint32_t pb0[NT], pb1[NT], pr0[NT], pr1[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        // ---- S^T = K Q^T for the 8 rows of n-tile nt (permuted k order)
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < KC; ++i) {
+            const uint4 qf = lds128(qs + (nt * KC + i) * 512);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                H::mma(s, word(kr0[i], 2 * e), word(kr1[i], 2 * e), word(kr0[i], 2 * e + 1),
+                       word(kr1[i], 2 * e + 1), word(qf, 2 * e), word(qf, 2 * e + 1));
+            }
+        }
+        // causal mask: token t is seen by a row at position p >= t
+        const float x0 = tok0 <= pos[nt][0] ? s[0] * a.scale_log2 : neg_inf();
+        const float x1 = tok0 <= pos[nt][1] ? s[1] * a.scale_log2 : neg_inf();
+        const float x2 = tok1 <= pos[nt][0] ? s[2] * a.scale_log2 : neg_inf();
+        const float x3 = tok1 <= pos[nt][1] ? s[3] * a.scale_log2 : neg_inf();
+
+        // ---- online softmax (base 2), rows 2c (x0, x2) and 2c + 1 (x1, x3):
+        // the reference max is raised only when a logit exceeds it by more
+        // than kSlack (weights then stay <= 2^kSlack); otherwise no warp-wide
+        // max and no rescale.
+        const float bx0 = fmaxf(x0, x2), bx1 = fmaxf(x1, x3);
+        if (__any_sync(0xffffffffu, bx0 > w.m[nt][0] + kSlack || bx1 > w.m[nt][1] + kSlack)) {
+            float bm0 = bx0, bm1 = bx1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(w.m[nt][0], bm0), mn1 = fmaxf(w.m[nt][1], bm1);
+            // a row still without any visible token keeps m = -inf
+            const float al0 = mn0 == neg_inf() ? 1.f : ex2(w.m[nt][0] - mn0);
+            const float al1 = mn1 == neg_inf() ? 1.f : ex2(w.m[nt][1] - mn1);
+            w.l[nt][0] *= al0;
+            w.l[nt][1] *= al1;
+            w.m[nt][0] = mn0;
+            w.m[nt][1] = mn1;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                w.o[mt][nt][0] *= al0;
+                w.o[mt][nt][1] *= al1;
+                w.o[mt][nt][2] *= al0;
+                w.o[mt][nt][3] *= al1;
+            }
+        }
+        // masked logits give 0 even while the row's m is still -inf
+        const float r0 = w.m[nt][0] == neg_inf() ? 0.f : w.m[nt][0];
+        const float r1 = w.m[nt][1] == neg_inf() ? 0.f : w.m[nt][1];
+        const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1);
+        const float p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+        w.l[nt][0] += p0 + p2;
+        w.l[nt][1] += p1 + p3;
+        // P^T B-fragments (two 8x8 transposes); bf16 P also as its residual
+        const uint32_t h01 = H::pack(p0, p1), h23 = H::pack(p2, p3);
+        pb0[nt] = movmatrix_trans(h01);
+        pb1[nt] = movmatrix_trans(h23);
+        if constexpr (kSplitP<T>) {
+            pr0[nt] = movmatrix_trans(H::pack(p0 - lo_float(h01), p1 - hi_float(h01)));
+            pr1[nt] = movmatrix_trans(H::pack(p2 - lo_float(h23), p3 - hi_float(h23)));
+        }
+    }
+
+    // ---- O^T += V^T P^T; every V fragment serves all NT n-tiles.  Masked
+    // tokens have P = 0, but slots past the context may hold any bits (NaN
+    // included, and 0 * NaN would poison o): their V rows are cleared.
+    if (lb * BS + BS > ctx) {
+        const int t0 = lb * BS;
+#pragma unroll
+        for (int j = 0; j < VC; ++j) {
+            if (t0 + 2 * c >= ctx) vr[0][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 2 * c + 1 >= ctx) vr[1][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 8 + 2 * c >= ctx) vr[2][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 9 + 2 * c >= ctx) vr[3][j] = make_uint4(0, 0, 0, 0);
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        constexpr int HALF = D / 16;
+        const int elo = mt, ehi = mt + HALF;
+        const int jl = elo >> 3, wl = (elo & 7) >> 1, hl = elo & 1;
+        const int jh = ehi >> 3, wh = (ehi & 7) >> 1, hh = ehi & 1;
+        const uint32_t sl = hl ? 0x7632u : 0x5410u;
+        const uint32_t sh = hh ? 0x7632u : 0x5410u;
+        const uint32_t a0 = __byte_perm(word(vr[0][jl], wl), word(vr[1][jl], wl), sl);
+        const uint32_t a1 = __byte_perm(word(vr[0][jh], wh), word(vr[1][jh], wh), sh);
+        const uint32_t a2 = __byte_perm(word(vr[2][jl], wl), word(vr[3][jl], wl), sl);
+        const uint32_t a3 = __byte_perm(word(vr[2][jh], wh), word(vr[3][jh], wh), sh);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            H::mma(w.o[mt][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+            if constexpr (kSplitP<T>) H::mma(w.o[mt][nt], a0, a1, a2, a3, pr0[nt], pr1[nt]);
+        }
+    }
+}
+
+// One CTA per (row tile, KV head, sequence).  Row r of the tile (0 .. 8 NT - 1)
+// is row tile * 8 NT + r of the sequence's (query token, query head) rows,
+// token i = row / G, head kvh * G + row % G.
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(NW * 32, NT == 1 ? 4 : 3) multi_query_kernel(MQArgs a) {
+    using H = Half16<T>;
+    constexpr int KC = D / 32;
+    constexpr int MT = D / 16;
+    constexpr int R = 8 * NT;
+    const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+
+    const int q0 = a.q_start[b], L = a.q_start[b + 1] - q0;
+    const int row0 = tile * R;
+    if (L <= 0 || row0 >= L * a.G) return;
+    int ctx = a.ctx_lens[b];
+    const int cap = a.max_blocks * BS;
+    if (ctx < L || ctx > cap) {
+        if (threadIdx.x == 0 && tile == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+        ctx = ctx > cap ? cap : ctx;
+    }
+    const int first_pos = ctx - L;  // position of query token 0 (negative if ctx < L)
+
+    // query fragments of the tile, shared by the 4 warps: n-tile nt, column g
+    // (row 8 nt + g), k-chunk i at sq[nt][i][lane]
+    __shared__ uint4 sq[NT][KC][32];
+    for (int x = threadIdx.x; x < NT * KC * 32; x += NW * 32) {
+        const int nt = x / (KC * 32), i = (x / 32) % KC, ln = x % 32;
+        const int row = row0 + 8 * nt + (ln >> 2), cc = ln & 3;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < L * a.G) {
+            const int tok = row / a.G, h = row - tok * a.G;
+            const T* qrow = static_cast<const T*>(a.q) +
+                            ((static_cast<int64_t>(q0) + tok) * a.hq + kvh * a.G + h) * D;
+            v = *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * cc);
+        }
+        sq[nt][i][ln] = v;
+    }
+    __syncthreads();
+    const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(&sq[0][0][lane]));
+
+    // positions of this lane's rows (8 nt + 2c, 8 nt + 2c + 1), -1 if none
+    int pos[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int row = row0 + 8 * nt + 2 * c + k;
+            const int p = row < L * a.G ? first_pos + row / a.G : -1;
+            pos[nt][k] = p < 0 ? -1 : p;
+        }
+    }
+    // blocks up to the tile's last position (its last valid row's token)
+    const int last = first_pos + (min(row0 + R, L * a.G) - 1) / a.G;
+    const int nblk = last >= 0 ? last / BS + 1 : 0;
+
+    MQState<MT, NT> w;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        w.m[nt][0] = w.m[nt][1] = neg_inf();
+        w.l[nt][0] = w.l[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) w.o[mt][nt][0] = w.o[mt][nt][1] = w.o[mt][nt][2] = w.o[mt][nt][3] = 0.f;
+    }
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    int tab = 0, k = 0;
+    for (int lb = warp; lb < nblk; lb += NW, ++k) {
+        if ((k & 31) == 0) {  // physical ids of this warp's next 32 blocks
+            const int idx = lb + NW * lane;
+            tab = idx < nblk ? trow[idx] : 0;
+        }
+        const int phys = __shfl_sync(0xffffffffu, tab, k & 31);
+        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+            if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            continue;
+        }
+        attend<T, D, NT>(a, kvh, lb, phys, ctx, qs, pos, w, g, c);
+    }
+
+    // ---- merge the NW warps through shared memory, write the tile's rows
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            w.l[nt][0] += __shfl_xor_sync(0xffffffffu, w.l[nt][0], off);
+            w.l[nt][1] += __shfl_xor_sync(0xffffffffu, w.l[nt][1], off);
+        }
+    }
+    __shared__ float sm_ml[NW][R][2];
+    __shared__ float sm_o[NW][R][D];
+    if (g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sm_ml[warp][8 * nt + 2 * c][0] = w.m[nt][0];
+            sm_ml[warp][8 * nt + 2 * c][1] = w.l[nt][0];
+            sm_ml[warp][8 * nt + 2 * c + 1][0] = w.m[nt][1];
+            sm_ml[warp][8 * nt + 2 * c + 1][1] = w.l[nt][1];
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int dl = pv_col(mt, g), dh = pv_col(mt + D / 16, g);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sm_o[warp][8 * nt + 2 * c][dl] = w.o[mt][nt][0];
+            sm_o[warp][8 * nt + 2 * c + 1][dl] = w.o[mt][nt][1];
+            sm_o[warp][8 * nt + 2 * c][dh] = w.o[mt][nt][2];
+            sm_o[warp][8 * nt + 2 * c + 1][dh] = w.o[mt][nt][3];
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < R * D; idx += NW * 32) {
+        const int r = idx / D, d = idx - r * D;
+        const int row = row0 + r;
+        if (row >= L * a.G) continue;
+        float M = neg_inf();
+#pragma unroll
+        for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, sm_ml[ww][r][0]);
+        float acc = 0.f, Ls = 0.f;
+        if (M != neg_inf()) {
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) {
+                const float sc = ex2(sm_ml[ww][r][0] - M);
+                acc += sc * sm_o[ww][r][d];
+                Ls += sc * sm_ml[ww][r][1];
+            }
+        }
+        const int tok = row / a.G, h = row - tok * a.G;
+        const int64_t orow = (static_cast<int64_t>(q0) + tok) * a.hq + kvh * a.G + h;
+        static_cast<T*>(a.out)[orow * D + d] = H::from_float(Ls > 0.f ? acc / Ls : 0.f);
+    }
+}
+
+template <typename T, int D, int NT>
+void launch(const MQArgs& a, int tiles, int batch, cudaStream_t st) {
+    dim3 grid(tiles, a.hkv, batch);
+    multi_query_kernel<T, D, NT><<<grid, NW * 32, 0, st>>>(a);
+}
+
+template <typename T, int D>
+void launch_nt(const MQArgs& a, int rows, int batch, cudaStream_t st) {
+    if (rows <= 8) launch<T, D, 1>(a, 1, batch, st);
+    else launch<T, D, 2>(a, (rows + 15) / 16, batch, st);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_attention_multi_query(
+    const void* q, const int32_t* q_start, const void* k_pool, const void* v_pool,
+    const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+    int32_t max_blocks, int32_t max_q_len, float scale, void* out, int dtype, void* stream) {
+    if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || max_blocks < 0 || max_q_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) || num_q_heads / num_kv_heads > 8 ||
+        batch > 65535 || num_kv_heads > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t rows = static_cast<int64_t>(max_q_len) * (num_q_heads / num_kv_heads);
+    if (rows > 16LL * 65535) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0 || max_q_len == 0) return PKV_OK;
+    if (!q || !q_start || !k_pool || !v_pool || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_pool) || !pkv::aligned16(v_pool) || !pkv::aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(q_start) & 3u) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+        (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+        return PKV_ERR_MISALIGNED;
+    int* st = pkv::status_word();
+    if (!st) return PKV_ERR_CUDA;
+    pkv::MQArgs a;
+    a.q = q;
+    a.q_start = q_start;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
+    a.tables = block_tables;
+    a.ctx_lens = context_lens;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.G = num_q_heads / num_kv_heads;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.scale_log2 = scale * pkv::kLog2e;
+    a.out = out;
+    a.status = st;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const int r = static_cast<int>(rows);
+    if (dtype == PKV_DTYPE_BF16) {
+        if (head_dim == 128) pkv::launch_nt<__nv_bfloat16, 128>(a, r, batch, cs);
+        else pkv::launch_nt<__nv_bfloat16, 64>(a, r, batch, cs);
+    } else {
+        if (head_dim == 128) pkv::launch_nt<__half, 128>(a, r, batch, cs);
+        else pkv::launch_nt<__half, 64>(a, r, batch, cs);
+    }
+    return pkv::launch_status();
+}

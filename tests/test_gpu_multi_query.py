@@ -1,0 +1,129 @@
+"""GPU parity of multi-query paged attention (speculative verify of gamma + 1
+tokens, chunked-prefill slices) against the float64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic as syn
+from cache_builder import assert_close, build, logical_rows
+from oracle import attention as oatt
+
+pytestmark = pytest.mark.gpu
+
+
+def _queries(w, qlens, seed):
+    rng = np.random.default_rng(seed)
+    T = int(sum(qlens))
+    q32 = rng.standard_normal((T, w["hq"], w["d"]), dtype=np.float32)
+    q = torch.from_numpy(q32).to(w["torch_dtype"])
+    q_start = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    return q, q_start
+
+
+def _run(pkv, c, qlens, seed=0, lens=None):
+    w = c.w
+    q, q_start = _queries(w, qlens, seed)
+    dev = c.q.device
+    out = torch.full(q.shape, 7.0, dtype=q.dtype, device=dev)
+    pkv.pkv_paged_attention_multi_query(q.to(dev), torch.from_numpy(q_start).to(dev), c.k_pool, c.v_pool,
+                                        c.tables, c.lens if lens is None else lens, w["scale"], out,
+                                        max(max(qlens), 1))
+    torch.cuda.synchronize()
+    return q, q_start, out.float().cpu().numpy()
+
+
+def _expected(c, q, q_start, seqs, ctx_override=None):
+    qn = q.float().numpy()
+    want = {}
+    for b in seqs:
+        k, v = logical_rows(c, b)
+        if ctx_override is not None:
+            k, v = k[:ctx_override[b]], v[:ctx_override[b]]
+        want[b] = oatt.multi_query_attention(qn[q_start[b]:q_start[b + 1]], k, v, c.w["scale"])
+    return want
+
+
+def _check(c, q, q_start, got, seqs=None, ctx_override=None, what=""):
+    seqs = range(len(q_start) - 1) if seqs is None else seqs
+    want = _expected(c, q, q_start, seqs, ctx_override)
+    for b, wb in want.items():
+        if wb.shape[0]:
+            assert_close(got[q_start[b]:q_start[b + 1]], wb, what="%s seq %d" % (what, b))
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 6, 8, 16, 17, 40])
+def test_uniform_query_lengths(pkv, cuda_dev, L):
+    w = syn.workload("llama3_8b_b64", batch=5, len_lo=40, len_hi=900, num_blocks=1024)
+    c = build(pkv, w, cuda_dev)
+    q, q_start, got = _run(pkv, c, [L] * 5, seed=L)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="L %d" % L)
+
+
+def test_ragged_query_lengths_with_empty(pkv, cuda_dev):
+    w = syn.workload("llama3_8b_b64", batch=7, len_lo=20, len_hi=600, num_blocks=1024)
+    c = build(pkv, w, cuda_dev)
+    qlens = [6, 0, 1, 19, 3, 0, 12]
+    q, q_start, got = _run(pkv, c, qlens, seed=3)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="ragged")
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype", [(8, 8, 128, "bf16"), (64, 8, 64, "fp16"), (16, 2, 64, "bf16"),
+                                            (8, 2, 128, "fp16")])
+def test_groups_dims_dtypes(pkv, cuda_dev, hq, hkv, d, dtype):
+    w = syn.workload("llama3_8b_b64", batch=4, len_lo=30, len_hi=400, num_blocks=512, hq=hq, hkv=hkv,
+                     d=d, dtype=dtype)
+    c = build(pkv, w, cuda_dev)
+    q, q_start, got = _run(pkv, c, [5, 1, 9, 2], seed=hq)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="G %d D %d %s" % (hq // hkv, d, dtype))
+
+
+def test_whole_prefill_and_short_contexts(pkv, cuda_dev):
+    """L = ctx: the whole sequence is new (a prefill from an empty cache),
+    including contexts of 1, 15, 16 and 17 tokens."""
+    w = syn.workload("llama3_8b_b64", lens=[1, 15, 16, 17, 100, 130], num_blocks=256)
+    c = build(pkv, w, cuda_dev)
+    lens = syn.context_lengths(w)
+    q, q_start, got = _run(pkv, c, lens, seed=11)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="whole prefill")
+
+
+def test_more_queries_than_context_sets_status(pkv, cuda_dev):
+    w = syn.workload("llama3_8b_b64", lens=[5, 40], num_blocks=64)
+    c = build(pkv, w, cuda_dev)
+    pkv.pkv_device_status()
+    q, q_start, got = _run(pkv, c, [8, 3], seed=12)
+    assert pkv.pkv_device_status() & pkv.PKV_STATUS_BAD_CONTEXT
+    assert (got[:3] == 0).all()  # queries 0..2 of sequence 0 sit at negative positions
+    _check(c, q, q_start, got, seqs=[1], what="valid sequence")
+    assert pkv.pkv_device_status() == 0
+
+
+def test_one_query_agrees_with_decode(pkv, cuda_dev):
+    w = syn.workload("llama3_8b_b64", batch=6, num_blocks=2048)
+    c = build(pkv, w, cuda_dev)
+    B = len(c.decoded)
+    q = c.q
+    out = torch.empty_like(q)
+    q_start = torch.arange(B + 1, dtype=torch.int32, device=cuda_dev)
+    pkv.pkv_paged_attention_multi_query(q, q_start, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"], out, 1)
+    dec = torch.empty_like(q)
+    ws = torch.empty(max(pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, 0), 16),
+                     dtype=torch.uint8, device=cuda_dev)
+    pkv.pkv_paged_attention_decode(q, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"], dec, ws, 0)
+    torch.cuda.synchronize()
+    assert_close(out.float().cpu().numpy(), dec.float().cpu().numpy().astype(np.float64), what="vs decode")
+
+
+def test_speculative_verify_full_layer_sampled(pkv, cuda_dev):
+    """The 64-sequence layer with gamma + 1 = 6 query tokens per sequence
+    (the pages' gamma = 5): sampled sequences against the oracle."""
+    w = syn.workload("llama3_8b_b64")
+    c = build(pkv, w, cuda_dev)
+    q, q_start, got = _run(pkv, c, [6] * len(c.decoded), seed=5)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, seqs=[0, 17, 63], what="verify")
