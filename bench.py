@@ -63,7 +63,12 @@ WORKLOADS = {
     "quant_int4": ("quant", {}, "int4"),
     "quant_fp8": ("quant", {}, "fp8"),
     "prefix_cow": ("prefix_cow", {}, None),
+    "verify_b64_g5": ("llama3_8b_b64", {}, None),
+    "prefill_chunk512": ("llama3_8b_b64", {"lens": [4096] * 8, "num_blocks": 4096}, None),
 }
+
+# multi-query workloads: query tokens per sequence (the last ones of its context)
+MQ_LEN = {"verify_b64_g5": 6, "prefill_chunk512": 512}
 
 DESCRIPTIONS = {
     "llama3_8b_b64": "one Llama-3-8B-shaped layer, 64 sequences, context uniform in [512, 4096] "
@@ -80,6 +85,12 @@ DESCRIPTIONS = {
                  "values N(0,1) with 1% outliers at +-8",
     "prefix_cow": "8 sequences forked from a shared 2,000-token prompt, each extended by a "
                   "seeded tail of 1..300 tokens, 32 q / 8 KV heads, head dim 128, bf16",
+    "verify_b64_g5": "speculative verify on the 64-sequence Llama-3-8B-shaped layer: the target's "
+                     "one pass over gamma + 1 = 6 tokens per sequence (the pages' gamma = 5), each "
+                     "attending causally over its context (512..4096 tokens), 32/8/128 bf16",
+    "prefill_chunk512": "one 512-token chunked-prefill slice per sequence (the pages' "
+                        "--chunked-prefill-size 512) at positions 3,584..4,095 of 8 sequences, "
+                        "causal, 32/8/128 bf16",
 }
 
 
@@ -437,6 +448,128 @@ def run_device(args, rank, world, dist):
                 split_desc=cache.split_desc)
 
 
+def run_mq(args, rank, world, dist):
+    """Multi-query workloads: every step rewrites the L new tokens' K/V rows
+    of every sequence (pkv_kv_append) and runs pkv_paged_attention_multi_query
+    with L queries per sequence at the last L positions of its context."""
+    import torch
+    import paged_kv_cache_13_gb300 as pkv
+    import synthetic as syn
+
+    dev_index = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev_index)
+    device = torch.device("cuda", dev_index)
+    name, L = args.workload, MQ_LEN[args.workload]
+    cache = Cache(pkv, torch, device, name, 0, 8)
+    w, B = cache.w, cache.B
+    Hq, Hkv, D = w["hq"], w["hkv"], w["d"]
+    # the pool holds every context token
+    pkv.pkv_kv_append(cache.new_k, cache.new_v, cache.slots, cache.k_pool, cache.v_pool)
+    tables = cache.tables.cpu().numpy()
+    ctx = cache.ctx_host
+    ks, vs, slots = [], [], []
+    for b in range(B):
+        k, v = syn.sequence_kv(w, b)
+        lo = int(ctx[b]) - L
+        ks.append(k[lo:])
+        vs.append(v[lo:])
+        for pos in range(lo, int(ctx[b])):
+            slots.append(int(tables[b, pos // 16]) * 16 + pos % 16)
+    mq_k = torch.cat(ks).to(device)
+    mq_v = torch.cat(vs).to(device)
+    mq_slots = torch.tensor(slots, dtype=torch.int64, device=device)
+    rng = np.random.default_rng(np.random.SeedSequence([w["seed"], 77]))
+    q = torch.from_numpy(rng.standard_normal((B * L, Hq, D), dtype=np.float32)).to(w["torch_dtype"]).to(device)
+    q_start = torch.arange(0, B * L + 1, L, dtype=torch.int32, device=device)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q, oo=out):
+        pkv.pkv_kv_append(mq_k, mq_v, mq_slots, cache.k_pool, cache.v_pool)
+        pkv.pkv_paged_attention_multi_query(qq, q_start, cache.k_pool, cache.v_pool, cache.tables,
+                                            cache.lens, w["scale"], oo, L)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev_index)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert pkv.pkv_device_status() == 0
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dist, device)
+    ms = elapsed_ms / args.steps
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    # end to end: q from pinned host memory, out back to pinned host memory
+    e2e_steps = max(1, min(args.steps, 200))
+    hq_ = q.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq = torch.empty_like(q)
+    torch.cuda.synchronize()
+    te = time.perf_counter()
+    for _ in range(e2e_steps):
+        dq.copy_(hq_, non_blocking=True)
+        step(dq, out)
+        ho.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - te, dist, device) / e2e_steps
+
+    kv_bytes = cache.kv_bytes()
+    positions = [int(ctx[b]) - L + i for b in range(B) for i in range(L)]
+    flops = sum(4.0 * (p + 1) * D * Hq for p in positions)  # QK^T and PV, causal
+    qo_bytes = 2 * q.numel() * q.element_size()
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    tflops_peak = float(peaks.get("bf16_tflops", 1900.0))
+    cfg = {"workload": "%s: %s; step = pkv_kv_append of the %d new rows per sequence + "
+                       "pkv_paged_attention_multi_query" % (name, DESCRIPTIONS[name], L),
+           "batch": B, "query_tokens_per_sequence": L, "kv_bytes_per_step": kv_bytes,
+           "causal_flops_per_step": flops,
+           "l2": "inputs larger than L2 (%.0f MB of KV per step), no flush" % (kv_bytes / 1e6)
+           if kv_bytes > 129e6 else "KV working set %.0f MB fits the 129 MB L2" % (kv_bytes / 1e6)}
+    common = {"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+              "data": "synthetic", "config": cfg, "gpu_launches": 2 * args.steps, "clocks": clk,
+              "queries_per_s": round(B * L * world / (ms * 1e-3), 1), "cpu_baseline": None}
+    if name == "prefill_chunk512":
+        value = flops * world / (ms * 1e-3) / 1e12
+        achieved = flops / (call_ms * 1e-3) / 1e12
+        line = dict(metric="chunked-prefill attention TFLOP/s (causal QK^T + PV FLOPs)",
+                    value=round(value, 2), unit="TFLOP/s", **common)
+        line["roofline"] = {"bound": "tensor", "kernel": "multi_query_kernel<bf16, 128, 2> (mma.sync)",
+                            "achieved": round(achieved, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+                            "peak_kind": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS, burst)",
+                            "frac": round(achieved / tflops_peak, 4), "traffic": None,
+                            "algorithmic_flops_per_launch": flops, "avg_launch_ms": call_ms}
+        line["e2e"] = {"value": round(flops * world / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
+    else:
+        value = kv_bytes * world / (ms * 1e-3) / 1e9
+        achieved = kv_bytes / (call_ms * 1e-3) / 1e9
+        line = dict(metric=METRIC, value=round(value, 1), unit="GB/s", **common)
+        line["roofline"] = {"bound": "hbm", "kernel": "multi_query_kernel<bf16, 128, 2>",
+                            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                            "peak_kind": "measured (MEASURED_PEAKS.json hbm_gbs, copy, burst)",
+                            "frac": round(achieved / hbm, 4), "traffic": None,
+                            "algorithmic_bytes_per_launch": kv_bytes + qo_bytes, "avg_launch_ms": call_ms}
+        line["e2e"] = {"value": round(kv_bytes * world / e2e_s / 1e9, 1), "unit": "GB/s",
+                       "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": out.numel() * 2}
+    return line
+
+
 def prefix_cache_timing(pkv, cache, iters=2000):
     """Host prefix cache on the prefix workload's pool: the prompt holder's
     blocks are registered under seeded token ids, then each iteration maps a
@@ -702,6 +835,13 @@ def main():
         import torch.distributed as dist_mod
         dist_mod.init_process_group("nccl")
         dist = dist_mod
+    if args.workload in MQ_LEN:
+        line = run_mq(args, rank, world, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(line))
+        return
     res = run_device(args, rank, world, dist)
     if dist is not None:
         dist.destroy_process_group()
