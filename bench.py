@@ -62,6 +62,7 @@ WORKLOADS = {
     "long_splitk": ("long_splitk", {}, None),
     "quant_int4": ("quant", {}, "int4"),
     "quant_fp8": ("quant", {}, "fp8"),
+    "quant_int4_g64": ("quant", {"group_size": 64, "n_sink": 8}, "int4"),
     "prefix_cow": ("prefix_cow", {}, None),
     "verify_b64_g5": ("llama3_8b_b64", {}, None),
     "prefill_chunk512": ("llama3_8b_b64", {"lens": [4096] * 8, "num_blocks": 4096}, None),
@@ -83,6 +84,10 @@ DESCRIPTIONS = {
     "quant_fp8": "32 sequences x 16,384 tokens, 32 q / 8 KV heads, head dim 128, bf16 queries, "
                  "FP8 E4M3 cache with an fp16 scale per (token, head), 4 bf16 sink tokens, "
                  "values N(0,1) with 1% outliers at +-8",
+    "quant_int4_g64": "32 sequences x 16,384 tokens in the pages' INT4 layout: groups of 64 along "
+                      "the head dim (two fp16 scale/zero pairs per token and head, 36 B per 64 "
+                      "elements), 8 bf16 sink tokens, 32 q / 8 KV heads, head dim 128, values "
+                      "N(0,1) with 1% outliers at +-8",
     "prefix_cow": "8 sequences forked from a shared 2,000-token prompt, each extended by a "
                   "seeded tail of 1..300 tokens, 32 q / 8 KV heads, head dim 128, bf16",
     "verify_b64_g5": "speculative verify on the 64-sequence Llama-3-8B-shaped layer: the target's "
@@ -255,18 +260,20 @@ class Cache:
             self.pools = [self.k_pool, self.v_pool]
         else:
             cb = D // 2 if qmode == "int4" else D
+            self.group_size = w.get("group_size", D) if qmode == "int4" else D
+            ng = D // self.group_size
             u8, f16 = torch.uint8, torch.float16
             self.cache = {
                 "k_codes": torch.empty((NB, Hkv, BS, cb), dtype=u8, device=device),
                 "v_codes": torch.empty((NB, Hkv, BS, cb), dtype=u8, device=device),
-                "k_scale": torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device),
-                "v_scale": torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device),
+                "k_scale": torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device),
+                "v_scale": torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device),
                 "sink_k": torch.zeros((B, max(self.n_sink, 1), Hkv, D), dtype=dt, device=device),
                 "sink_v": torch.zeros((B, max(self.n_sink, 1), Hkv, D), dtype=dt, device=device),
             }
             if qmode == "int4":
-                self.cache["k_zero"] = torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device)
-                self.cache["v_zero"] = torch.empty((NB, Hkv, BS, 1), dtype=f16, device=device)
+                self.cache["k_zero"] = torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device)
+                self.cache["v_zero"] = torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device)
             self.pools = [self.cache[k] for k in ("k_codes", "k_scale", "k_zero", "v_codes",
                                                   "v_scale", "v_zero") if k in self.cache]
         row_of = {h: i for i, h in enumerate(decoded)}
@@ -350,12 +357,12 @@ class Cache:
             positions = torch.from_numpy(np.asarray(positions, dtype=np.int32)).to(self.dev)
         sidx = torch.full((k.shape[0],), seq_row, dtype=torch.int32, device=self.dev)
         self.pkv.pkv_kv_append_quant(k, v, slots, positions, sidx, self.cache, self.n_sink,
-                                     self.qmode)
+                                     self.qmode, self.group_size)
 
     def bytes_per_token(self):
         Hkv, D = self.w["hkv"], self.w["d"]
         if self.qmode == "int4":
-            return 2 * Hkv * (D // 2 + 4)
+            return 2 * Hkv * (D // 2 + 4 * (D // self.group_size))
         if self.qmode == "fp8":
             return 2 * Hkv * (D + 2)
         return 2 * Hkv * D * 2
@@ -387,9 +394,9 @@ class Cache:
             return
         positions = self.positions if positions is None else positions
         pkv.pkv_kv_append_quant(k_new, v_new, slots, positions, self.seq_idx, self.cache,
-                                self.n_sink, self.qmode, 0, stream)
+                                self.n_sink, self.qmode, self.group_size, stream)
         pkv.pkv_paged_attention_decode_quant(q, self.cache, self.n_sink, tables, lens,
-                                             self.w["scale"], out, self.qmode, 0, ws,
+                                             self.w["scale"], out, self.qmode, self.group_size, ws,
                                              self.partition_size, stream)
 
     def launches_per_step(self):
@@ -735,17 +742,19 @@ def oracle_sample(name, S):
     else:
         ns = w["n_sink"]
         cb = D // 2 if qmode == "int4" else D
+        gsz = w.get("group_size", D) if qmode == "int4" else D
+        ng = D // gsz
         cache = {"k_codes": np.zeros((nb, Hkv, 16, cb), np.uint8),
                  "v_codes": np.zeros((nb, Hkv, 16, cb), np.uint8),
-                 "k_scale": np.zeros((nb, Hkv, 16, 1), np.float16),
-                 "v_scale": np.zeros((nb, Hkv, 16, 1), np.float16),
-                 "k_zero": np.zeros((nb, Hkv, 16, 1), np.float16),
-                 "v_zero": np.zeros((nb, Hkv, 16, 1), np.float16),
+                 "k_scale": np.zeros((nb, Hkv, 16, ng), np.float16),
+                 "v_scale": np.zeros((nb, Hkv, 16, ng), np.float16),
+                 "k_zero": np.zeros((nb, Hkv, 16, ng), np.float16),
+                 "v_zero": np.zeros((nb, Hkv, 16, ng), np.float16),
                  "sink_k": np.zeros((S, ns, Hkv, D)), "sink_v": np.zeros((S, ns, Hkv, D))}
         for i in range(S):
             # the oracle's vectorised quantiser, written at the slots
-            _, kc, ksc, kz = kvcache.quantize_sequence(ks[i], qmode, D)
-            _, vc, vsc, vz = kvcache.quantize_sequence(vs[i], qmode, D)
+            _, kc, ksc, kz = kvcache.quantize_sequence(ks[i], qmode, gsz)
+            _, vc, vsc, vz = kvcache.quantize_sequence(vs[i], qmode, gsz)
             for t, slot in enumerate(all_slots[i]):
                 blk, off = divmod(int(slot), 16)
                 cache["k_codes"][blk, :, off] = kc[t]
@@ -759,8 +768,8 @@ def oracle_sample(name, S):
             cache["sink_v"][i] = vs[i][:ns]
 
         def decode():
-            kvcache.paged_attention_decode_quant(q, cache, tables, ctx, w["scale"], ns, qmode, D)
-        per_tok = 2 * Hkv * (D // 2 + 4) if qmode == "int4" else 2 * Hkv * (D + 2)
+            kvcache.paged_attention_decode_quant(q, cache, tables, ctx, w["scale"], ns, qmode, gsz)
+        per_tok = 2 * Hkv * (D // 2 + 4 * ng) if qmode == "int4" else 2 * Hkv * (D + 2)
         kvb = int(np.sum(ctx)) * per_tok + int(np.sum(np.minimum(ctx, ns))) * 2 * Hkv * D * 2
     return decode, kvb, S, int(np.sum(ctx))
 
@@ -779,7 +788,7 @@ def cpu_worker(name, min_seconds, S):
 
 
 CPU_SAMPLE_SEQS = {"llama3_8b_b64": 16, "long_splitk": 1, "quant_int4": 1, "quant_fp8": 1,
-                   "prefix_cow": 8}
+                   "quant_int4_g64": 1, "prefix_cow": 8}
 
 
 def cpu_baseline(name, min_seconds):

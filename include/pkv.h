@@ -410,8 +410,10 @@ int pkv_kv_append_quant(const void* k, const void* v, const int64_t* slot_mappin
  * with K_t, V_t the dequantised values ((q - z) * s for INT4, e4m3 * s for
  * FP8), except that positions t < n_sink read sink_k/sink_v[b, t, kv_head]
  * (16-bit, row b of the sink buffers belongs to batch entry b).  q and out
- * are 16-bit (dtype).  Supported: block_size 16, head_dim 128 or 64,
- * group_size == head_dim for INT4, n_sink <= block_size, 1 <= G <= 8. */
+ * are 16-bit (dtype).  Supported: block_size 16, head_dim 128 or 64;
+ * INT4 group_size == head_dim, or 64 at head_dim 128 (the pages' layout:
+ * two (scale, zero) pairs per token and head); n_sink <= block_size (the
+ * pages keep 8); 1 <= G <= 8. */
 int pkv_paged_attention_decode_quant(const void* q, const void* k_codes, const void* k_scale,
                                      const void* k_zero, const void* v_codes, const void* v_scale,
                                      const void* v_zero, const void* sink_k, const void* sink_v,

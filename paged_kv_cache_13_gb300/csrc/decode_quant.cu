@@ -44,12 +44,14 @@ namespace {
 constexpr int BS = 16;
 constexpr int NW = 4;
 // INT4 runs 5 CTAs per SM (96 registers) with the query fragments re-read
-// from shared memory per block; FP8 needs its registers for the 4 KiB of
-// codes per block and keeps 4 CTAs with the query fragments in registers.
+// from shared memory per block (4 with two column groups, whose per-group
+// sums, scales and weights need the registers); FP8 needs its registers for
+// the 4 KiB of codes per block and keeps 4 CTAs with the query fragments in
+// registers.
 // (Measured on the 32 x 16k workload: INT4 259 -> 242 us; FP8 unchanged or
 // slower with the INT4 settings.)
-template <int QMODE>
-constexpr int kCtasPerSm = QMODE == PKV_QMODE_INT4_ASYM ? 5 : 4;
+template <int QMODE, int NG = 1>
+constexpr int kCtasPerSm = QMODE == PKV_QMODE_INT4_ASYM && NG == 1 ? 5 : 4;
 template <int QMODE>
 constexpr bool kQueryInShared = QMODE == PKV_QMODE_INT4_ASYM;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -118,25 +120,43 @@ __device__ __forceinline__ float tofloat(T x) {
 // query heads 2c, 2c+1 of its lanes: per-lane partial sums l and (INT4) the
 // zero-point correction sum_t W_t z_t, and the PV accumulator in the MMA's
 // units (INT4: 2^-24, odd columns 2^-20).
-template <int MT>
+template <int MT, int NG>
 struct QState {
-    float m0, m1, l0, l1, corr0, corr1;
+    float m0, m1, l0, l1;
+    float corr[NG][2];  // per column group, heads 2c / 2c + 1
     float o[MT][4];
     __device__ __forceinline__ void init() {
         m0 = m1 = neg_inf();
-        l0 = l1 = corr0 = corr1 = 0.f;
+        l0 = l1 = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) corr[gi][0] = corr[gi][1] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     }
 };
 
+// PV element e (0 .. D/8 - 1) of m-tile mt, half hf (M rows g / g + 8).  One
+// column group (NG = 1): e = mt, mt + MT.  Two groups of 64 columns (NG = 2):
+// e = 8 (mt / 4) + mt % 4 + 4 hf, so both halves of an m-tile lie in one
+// group and take that group's weights.  Both halves have the same parity.
+template <int NG, int MT>
+__host__ __device__ constexpr int pv_e(int mt, int hf) {
+    return NG == 1 ? mt + hf * MT : 8 * (mt / 4) + mt % 4 + 4 * hf;
+}
+// Head-dim column of element e of lane group g: NG = 1, the lane's DS
+// consecutive columns; NG = 2, 8 columns in each 64-column group.
+template <int NG, int D>
+__device__ __forceinline__ int pv_column(int e, int g) {
+    return NG == 1 ? g * (D / 8) + e : (e >> 3) * 64 + 8 * g + (e & 7);
+}
+
 // One warp's pass over the blocks lb_first, lb_first + stride, ... < lb_end
 // of sequence b, KV head kvh (context ctx): query fragments, then every block
 // loaded into registers and attended into st (reset first).  sq is the
 // lane's slot of the warp's shared query slice (row t at sq[t * 32]).
-template <typename T, int D, int QMODE>
+template <typename T, int D, int QMODE, int NG>
 __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh, int ctx, int lb_first,
-                                           int lb_end, int stride, uint4* sq, QState<D / 16>& st) {
+                                           int lb_end, int stride, uint4* sq, QState<D / 16, NG>& st) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
     constexpr int KSTEPS = D / 16;             // k-steps of QK^T
     constexpr int MT = D / 16;                 // m-tiles of PV
@@ -144,6 +164,12 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     constexpr int KW = INT4 ? D / 32 : D / 16; // 32-bit K-code words per lane per row
     constexpr int VW = INT4 ? D / 64 : D / 32; // 32-bit V-code words per lane per row
     constexpr int DS = D / 8;                  // head-dim columns per lane group in PV
+    // INT4 column groups (one (scale, zero) each): GS columns, KPG K words
+    // and VPG V words per lane and row in each
+    constexpr int GS = D / NG;
+    constexpr int KPG = KW / NG;
+    constexpr int VPG = VW / NG;
+    static_assert(NG == 1 || (INT4 && D == 128 && NG == 2), "groups: one per head, or 64 columns at D 128");
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
 
@@ -151,24 +177,28 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     // staged in this warp's shared slice (k-steps 2t, 2t + 1 of lane l at
     // sq[warp][t][l]) and re-read per block, to leave registers for the codes
     uint32_t qf[KSTEPS][2];
-    float qsum = 0.f;  // sum over this lane's columns of query head g
+    float qsum[NG];  // sums over this lane's columns of query head g, per group
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) qsum[gi] = 0.f;
     {
         const T* qrow = static_cast<const T*>(a.q) +
                         (static_cast<int64_t>(b) * a.hq + kvh * a.G + (g < a.G ? g : 0)) * D;
         const bool valid = g < a.G;
         if constexpr (INT4) {
-            // lane c owns columns [c*D/4, (c+1)*D/4); word k covers 8 of them
-            const int base = c * (D / 4);
+            // K word k of lane c covers the 8 columns starting at
+            // (k / KPG) GS + (GS / 4) c + 8 (k % KPG): lane c holds a quarter
+            // of every column group
 #pragma unroll
             for (int k = 0; k < KW; ++k) {
+                const int col = (k / KPG) * GS + (GS / 4) * c + 8 * (k % KPG);
                 float x[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] = valid ? tofloat(qrow[base + 8 * k + j]) : 0.f;
+                for (int j = 0; j < 8; ++j) x[j] = valid ? tofloat(qrow[col + j]) : 0.f;
                 // fp16 rounding of the query, as fed to the MMA
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     x[j] = __half2float(__float2half_rn(x[j]));
-                    qsum += x[j];
+                    qsum[k / KPG] += x[j];
                 }
                 // the odd nibbles enter the MMA 16x larger: their query
                 // columns go in divided by 16 (a power of two)
@@ -203,17 +233,21 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         __syncwarp();
     }
     const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(sq));
-    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
-    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-    const float qsum0 = __shfl_sync(0xffffffffu, qsum, (2 * c) * 4);
-    const float qsum1 = __shfl_sync(0xffffffffu, qsum, (2 * c + 1) * 4);
+    float qs0[NG], qs1[NG];  // group sums of heads 2c, 2c + 1
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+        float x = qsum[gi];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        qs0[gi] = __shfl_sync(0xffffffffu, x, (2 * c) * 4);
+        qs1[gi] = __shfl_sync(0xffffffffu, x, (2 * c + 1) * 4);
+    }
 
     float& m0 = st.m0;
     float& m1 = st.m1;
     float& l0 = st.l0;
     float& l1 = st.l1;
-    float& corr0 = st.corr0;
-    float& corr1 = st.corr1;
+    auto& corr = st.corr;
     auto& o = st.o;
     st.init();
 
@@ -223,7 +257,7 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     // One block's codes and per-token (scale, zero) for this lane.
     struct QBlk {
         uint32_t kw0[KW], kw1[KW], vw[4][VW];
-        __half2 ks, vs, kz, vz;  // low: token g, high: token g + 8
+        __half2 ks[NG], vs[NG], kz[NG], vz[NG];  // per group; low: token g, high: token g + 8
     };
     auto load = [&](int phys, QBlk& B) {
         const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;  // (block, head)
@@ -231,7 +265,21 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         const uint8_t* vc = a.v_codes + bh * (BS * CB);
 
         // ---- loads: K rows g, g+8; V rows 2c, 2c+1, 8+2c, 9+2c; scales
-        if constexpr (INT4) {
+        if constexpr (INT4 && NG == 2) {
+            // per group: K words at byte 32 grp + 8 c, V word at byte 32 grp + 4 g
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+                const uint2 r0 = ldg_stream8(kc + g * CB + 32 * gi + 8 * c);
+                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 32 * gi + 8 * c);
+                B.kw0[2 * gi] = r0.x; B.kw0[2 * gi + 1] = r0.y;
+                B.kw1[2 * gi] = r1.x; B.kw1[2 * gi + 1] = r1.y;
+                const int off = 32 * gi + 4 * g;
+                B.vw[0][gi] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
+                B.vw[1][gi] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
+                B.vw[2][gi] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
+                B.vw[3][gi] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+            }
+        } else if constexpr (INT4) {
             if constexpr (KW == 4) {
                 const uint4 r0 = ldg_stream(kc + g * CB + 16 * c);
                 const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 16 * c);
@@ -279,22 +327,24 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
                 B.vw[2][0] = x2.x; B.vw[2][1] = x2.y; B.vw[3][0] = x3.x; B.vw[3][1] = x3.y;
             }
         }
-        const __half* ksc = a.k_scale + bh * BS;
-        const __half* vsc = a.v_scale + bh * BS;
-        B.ks = __halves2half2(ksc[g], ksc[g + 8]);
-        B.vs = __halves2half2(vsc[g], vsc[g + 8]);
-        if constexpr (INT4) {
-            B.kz = __halves2half2(a.k_zero[bh * BS + g], a.k_zero[bh * BS + g + 8]);
-            B.vz = __halves2half2(a.v_zero[bh * BS + g], a.v_zero[bh * BS + g + 8]);
+        // scale / zero [block, head, token, group]
+        const int64_t s0 = (bh * BS + g) * NG, s1 = (bh * BS + g + 8) * NG;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            B.ks[gi] = __halves2half2(a.k_scale[s0 + gi], a.k_scale[s1 + gi]);
+            B.vs[gi] = __halves2half2(a.v_scale[s0 + gi], a.v_scale[s1 + gi]);
+            if constexpr (INT4) {
+                B.kz[gi] = __halves2half2(a.k_zero[s0 + gi], a.k_zero[s1 + gi]);
+                B.vz[gi] = __halves2half2(a.v_zero[s0 + gi], a.v_zero[s1 + gi]);
+            }
         }
     };
     auto attend = [&](int lb, QBlk& B) {
-        const float ks0 = __low2float(B.ks), ks1 = __high2float(B.ks);
-        const float vs0 = __low2float(B.vs), vs1 = __high2float(B.vs);
-        const float kz0 = INT4 ? __low2float(B.kz) : 0.f, kz1 = INT4 ? __high2float(B.kz) : 0.f;
-        const float vz0 = INT4 ? __low2float(B.vz) : 0.f, vz1 = INT4 ? __high2float(B.vz) : 0.f;
-        // ---- S_raw^T = C Q^T over the code values
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S_raw^T = C Q^T over the code values (INT4: one accumulator per group)
+        float sg[NG][4];
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) sg[gi][0] = sg[gi][1] = sg[gi][2] = sg[gi][3] = 0.f;
+        float (&s)[4] = sg[0];
         if constexpr (INT4) {
 #pragma unroll
             for (int k = 0; k < KW; ++k) {
@@ -302,9 +352,10 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
                 const uint4 q2 = kQueryInShared<QMODE> ? lds128(qs + k * 512)
                                       : make_uint4(qf[2 * k][0], qf[2 * k][1], qf[2 * k + 1][0], qf[2 * k + 1][1]);
                 const uint32_t u0 = B.kw0[k] >> 8, u1 = B.kw1[k] >> 8;
-                mma_f16(s, nib_even(B.kw0[k]), nib_even(B.kw1[k]), nib_odd(B.kw0[k]), nib_odd(B.kw1[k]),
+                float (&sk)[4] = sg[k / KPG];
+                mma_f16(sk, nib_even(B.kw0[k]), nib_even(B.kw1[k]), nib_odd(B.kw0[k]), nib_odd(B.kw1[k]),
                         q2.x, q2.y);
-                mma_f16(s, nib_even(u0), nib_even(u1), nib_odd(u0), nib_odd(u1), q2.z, q2.w);
+                mma_f16(sk, nib_even(u0), nib_even(u1), nib_odd(u0), nib_odd(u1), q2.z, q2.w);
             }
         } else {
 #pragma unroll
@@ -325,13 +376,24 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
         float x0, x1, x2, x3;
         if constexpr (INT4) {
-            // S = s (sum_d q_d c_d - z sum_d q_d); the MMA gave 2^-24 sum q c
-            const float f0 = ks0 * a.scale_log2, f1 = ks1 * a.scale_log2;
-            x0 = f0 * (s[0] * kTwo24 - kz0 * qsum0);
-            x1 = f0 * (s[1] * kTwo24 - kz0 * qsum1);
-            x2 = f1 * (s[2] * kTwo24 - kz1 * qsum0);
-            x3 = f1 * (s[3] * kTwo24 - kz1 * qsum1);
+            // S = sum_groups s (sum_d q_d c_d - z sum_d q_d); the MMA gave
+            // 2^-24 sum q c per group
+            x0 = x1 = x2 = x3 = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                const float ks0 = __low2float(B.ks[gi]), ks1 = __high2float(B.ks[gi]);
+                const float kz0 = __low2float(B.kz[gi]), kz1 = __high2float(B.kz[gi]);
+                x0 += ks0 * (sg[gi][0] * kTwo24 - kz0 * qs0[gi]);
+                x1 += ks0 * (sg[gi][1] * kTwo24 - kz0 * qs1[gi]);
+                x2 += ks1 * (sg[gi][2] * kTwo24 - kz1 * qs0[gi]);
+                x3 += ks1 * (sg[gi][3] * kTwo24 - kz1 * qs1[gi]);
+            }
+            x0 *= a.scale_log2;
+            x1 *= a.scale_log2;
+            x2 *= a.scale_log2;
+            x3 *= a.scale_log2;
         } else {
+            const float ks0 = __low2float(B.ks[0]), ks1 = __high2float(B.ks[0]);
             x0 = ks0 * s[0] * a.scale_log2;
             x1 = ks0 * s[1] * a.scale_log2;
             x2 = ks1 * s[2] * a.scale_log2;
@@ -382,8 +444,11 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
             const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
             l0 *= al0;
             l1 *= al1;
-            corr0 *= al0;
-            corr1 *= al1;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                corr[gi][0] *= al0;
+                corr[gi][1] *= al1;
+            }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 o[mt][0] *= al0;
@@ -398,26 +463,32 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         const float p2 = ex2(x2 - m0), p3 = ex2(x3 - m1);
         l0 += p0 + p2;
         l1 += p1 + p3;
-        // PV weights W = P * s (zero for masked and sink tokens)
+        // PV weights W = P * s per group (zero for masked and sink tokens)
         const bool w0 = ok0 && !sk0, w1 = ok1 && !sk1;
-        const float W0 = w0 ? p0 * vs0 : 0.f, W1 = w0 ? p1 * vs0 : 0.f;
-        const float W2 = w1 ? p2 * vs1 : 0.f, W3 = w1 ? p3 * vs1 : 0.f;
-        const uint32_t pk0 = f16pair(W0, W1), pk1 = f16pair(W2, W3);
-        if constexpr (INT4) {
-            // the correction uses the fp16-rounded weights the MMA sees
-            const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
-            const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
-            if (w0) {
-                corr0 += __low2float(h0) * vz0;
-                corr1 += __high2float(h0) * vz0;
+        uint32_t pb0[NG], pb1[NG];
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const float vs0 = __low2float(B.vs[gi]), vs1 = __high2float(B.vs[gi]);
+            const float W0 = w0 ? p0 * vs0 : 0.f, W1 = w0 ? p1 * vs0 : 0.f;
+            const float W2 = w1 ? p2 * vs1 : 0.f, W3 = w1 ? p3 * vs1 : 0.f;
+            const uint32_t pk0 = f16pair(W0, W1), pk1 = f16pair(W2, W3);
+            if constexpr (INT4) {
+                // the correction uses the fp16-rounded weights the MMA sees
+                const float vz0 = __low2float(B.vz[gi]), vz1 = __high2float(B.vz[gi]);
+                const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
+                const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
+                if (w0) {
+                    corr[gi][0] += __low2float(h0) * vz0;
+                    corr[gi][1] += __high2float(h0) * vz0;
+                }
+                if (w1) {
+                    corr[gi][0] += __low2float(h1) * vz1;
+                    corr[gi][1] += __high2float(h1) * vz1;
+                }
             }
-            if (w1) {
-                corr0 += __low2float(h1) * vz1;
-                corr1 += __high2float(h1) * vz1;
-            }
+            pb0[gi] = movmatrix_trans(pk0);
+            pb1[gi] = movmatrix_trans(pk1);
         }
-        const uint32_t pb0 = movmatrix_trans(pk0);
-        const uint32_t pb1 = movmatrix_trans(pk1);
 
         if (t0 + BS > ctx) {  // partial last block: clear codes of missing tokens
 #pragma unroll
@@ -429,13 +500,14 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
             }
         }
 
-        // ---- O^T += C_v^T W^T; lane columns d = g*DS + e, e_lo = mt, e_hi = mt + MT
+        // ---- O^T += C_v^T W^T: m-tile mt takes the lane's elements
+        // e = pv_e<NG>(mt, 0 / 1) (see pv_e), both in one column group
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             uint32_t av[4];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const int e = mt + hf * MT;
+                const int e = INT4 ? pv_e<NG, MT>(mt, hf) : mt + hf * MT;
 #pragma unroll
                 for (int pr = 0; pr < 2; ++pr) {  // token pair (2c, 2c+1) / (8+2c, 9+2c)
                     const uint32_t* R0 = B.vw[2 * pr];
@@ -454,7 +526,8 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
                     av[hf + 2 * pr] = v;
                 }
             }
-            mma_f16(o[mt], av[0], av[1], av[2], av[3], pb0, pb1);
+            const int gi = INT4 ? (pv_e<NG, MT>(mt, 0) >> 3) / VPG : 0;
+            mma_f16(o[mt], av[0], av[1], av[2], av[3], pb0[gi], pb1[gi]);
         }
 
         if (sinks_here) {
@@ -464,12 +537,14 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
                 const int src = (t & 7) * 4 + c;
                 const float pa = __shfl_sync(0xffffffffu, t < 8 ? p0 : p2, src);
                 const float pb = __shfl_sync(0xffffffffu, t < 8 ? p1 : p3, src);
-                const T* vrow = svb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D + g * DS;
+                const T* vrow = svb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     // in the accumulator's units (INT4: 2^-24, odd columns 2^-20)
-                    const float u = INT4 ? ((mt & 1) ? 16.f * kInvTwo24 : kInvTwo24) : 1.f;
-                    const float vl = tofloat(vrow[mt]) * u, vh = tofloat(vrow[mt + MT]) * u;
+                    const int el = INT4 ? pv_e<NG, MT>(mt, 0) : mt, eh = INT4 ? pv_e<NG, MT>(mt, 1) : mt + MT;
+                    const float u = INT4 ? ((el & 1) ? 16.f * kInvTwo24 : kInvTwo24) : 1.f;
+                    const float vl = tofloat(vrow[pv_column<INT4 ? NG : 1, D>(el, g)]) * u;
+                    const float vh = tofloat(vrow[pv_column<INT4 ? NG : 1, D>(eh, g)]) * u;
                     o[mt][0] += pa * vl;
                     o[mt][1] += pb * vl;
                     o[mt][2] += pa * vh;
@@ -498,36 +573,51 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     }
 }
 
-// Lane-final values of a pass: l and the correction summed over the 8 token
-// lanes, and the output column values sum_t W_t (c - z) in true units.
-template <int D, int QMODE>
-__device__ __forceinline__ void quant_finish(QState<D / 16>& st) {
+// Lane-final values of a pass: l and the corrections summed over the 8
+// token lanes, and the output column values sum_t W_t (c - z) in true units.
+template <int D, int QMODE, int NG>
+__device__ __forceinline__ void quant_finish(QState<D / 16, NG>& st) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
     constexpr int MT = D / 16;
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
         st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
         st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
-        st.corr0 += __shfl_xor_sync(0xffffffffu, st.corr0, off);
-        st.corr1 += __shfl_xor_sync(0xffffffffu, st.corr1, off);
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            st.corr[gi][0] += __shfl_xor_sync(0xffffffffu, st.corr[gi][0], off);
+            st.corr[gi][1] += __shfl_xor_sync(0xffffffffu, st.corr[gi][1], off);
+        }
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        // INT4: back from the accumulator's units (columns e = mt, mt + MT
-        // share mt's parity), then O = sum W c - sum W z
-        const float u = INT4 ? ((mt & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
-        st.o[mt][0] = st.o[mt][0] * u - st.corr0;
-        st.o[mt][1] = st.o[mt][1] * u - st.corr1;
-        st.o[mt][2] = st.o[mt][2] * u - st.corr0;
-        st.o[mt][3] = st.o[mt][3] * u - st.corr1;
+        // INT4: back from the accumulator's units (both elements of an m-tile
+        // share their parity and column group), then O = sum W c - sum W z
+        const int el = INT4 ? pv_e<NG, MT>(mt, 0) : mt;
+        const int gi = INT4 ? (el >> 3) / ((D / 64) / NG) : 0;
+        const float u = INT4 ? ((el & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
+        st.o[mt][0] = st.o[mt][0] * u - st.corr[gi][0];
+        st.o[mt][1] = st.o[mt][1] * u - st.corr[gi][1];
+        st.o[mt][2] = st.o[mt][2] * u - st.corr[gi][0];
+        st.o[mt][3] = st.o[mt][3] * u - st.corr[gi][1];
     }
+}
+
+// Shared-memory row index of the lane's output columns of m-tile mt.
+template <int D, int QMODE, int NG>
+__device__ __forceinline__ void out_columns(int mt, int g, int& dl, int& dh) {
+    constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
+    constexpr int MT = D / 16;
+    const int el = INT4 ? pv_e<NG, MT>(mt, 0) : mt, eh = INT4 ? pv_e<NG, MT>(mt, 1) : mt + MT;
+    dl = pv_column<INT4 ? NG : 1, D>(el, g);
+    dh = pv_column<INT4 ? NG : 1, D>(eh, g);
 }
 
 // Partition kernel: one CTA of NW warps per (partition, KV head, sequence);
 // the warps take the partition's blocks round-robin and merge through
 // shared memory.
-template <typename T, int D, int QMODE, bool SPLIT>
-__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant_kernel(QDecodeArgs a) {
+template <typename T, int D, int QMODE, int NG, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_quant_kernel(QDecodeArgs a) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
     constexpr int DS = D / 8;
@@ -548,9 +638,9 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     const int blk_end = min(blk_begin + a.part_blocks, nblk);
 
     __shared__ uint4 sq[NW][KSTEPS / 2][32];
-    QState<MT> st;
-    quant_pass<T, D, QMODE>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
-    quant_finish<D, QMODE>(st);
+    QState<MT, NG> st;
+    quant_pass<T, D, QMODE, NG>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
+    quant_finish<D, QMODE, NG>(st);
     const float m0 = st.m0, m1 = st.m1, l0 = st.l0, l1 = st.l1;
     auto& o = st.o;
 
@@ -564,7 +654,8 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-        const int dl = g * DS + mt, dh = g * DS + mt + MT;
+        int dl, dh;
+        out_columns<D, QMODE, NG>(mt, g, dl, dh);
         sm_o[warp][2 * c][dl] = o[mt][0];
         sm_o[warp][2 * c + 1][dl] = o[mt][1];
         sm_o[warp][2 * c][dh] = o[mt][2];
@@ -603,8 +694,8 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>) paged_decode_quant
 // Balanced split for the quantised cache (the split itself: balanced.cuh):
 // warp i walks its range run by run, one pass per run segment, and writes
 // the run's partial.  No barrier.
-template <typename T, int D, int QMODE>
-__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>)
+template <typename T, int D, int QMODE, int NG>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     paged_decode_quant_balanced_kernel(QDecodeArgs a, int batch, int nwt_launch) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
@@ -623,15 +714,16 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>)
     if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
     if (!any) return;
     while (sp.next()) {
-        QState<MT> st;
-        quant_pass<T, D, QMODE>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
-        quant_finish<D, QMODE>(st);
+        QState<MT, NG> st;
+        quant_pass<T, D, QMODE, NG>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
+        quant_finish<D, QMODE, NG>(st);
         // partial (m, l, o) of this run: o staged through shared memory so
         // the G x D rows go out in 16-byte stores
         __syncwarp();
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int dl = g * DS + mt, dh = g * DS + mt + MT;
+            int dl, dh;
+            out_columns<D, QMODE, NG>(mt, g, dl, dh);
             sm_o[warp][2 * c][dl] = st.o[mt][0];
             sm_o[warp][2 * c + 1][dl] = st.o[mt][1];
             sm_o[warp][2 * c][dh] = st.o[mt][2];
@@ -656,62 +748,42 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE>)
     }
 }
 
-template <typename T, int D, int QMODE>
+template <typename T, int D, int QMODE, int NG>
 void launch_balanced(const QDecodeArgs& a, int batch, int nwt, cudaStream_t st) {
-    paged_decode_quant_balanced_kernel<T, D, QMODE><<<(nwt + NW - 1) / NW, NW * 32, 0, st>>>(a, batch, nwt);
+    paged_decode_quant_balanced_kernel<T, D, QMODE, NG><<<(nwt + NW - 1) / NW, NW * 32, 0, st>>>(a, batch, nwt);
 }
 
-int run_balanced(const QDecodeArgs& a, int D, int qmode, int dtype, int batch, int nwt, cudaStream_t st) {
-#define PKV_QBLAUNCH(TT, DD, QM) launch_balanced<TT, DD, QM>(a, batch, nwt, st)
-    if (dtype == PKV_DTYPE_BF16) {
-        if (qmode == PKV_QMODE_INT4_ASYM) {
-            if (D == 128) PKV_QBLAUNCH(__nv_bfloat16, 128, PKV_QMODE_INT4_ASYM);
-            else PKV_QBLAUNCH(__nv_bfloat16, 64, PKV_QMODE_INT4_ASYM);
-        } else {
-            if (D == 128) PKV_QBLAUNCH(__nv_bfloat16, 128, PKV_QMODE_FP8_E4M3);
-            else PKV_QBLAUNCH(__nv_bfloat16, 64, PKV_QMODE_FP8_E4M3);
-        }
-    } else {
-        if (qmode == PKV_QMODE_INT4_ASYM) {
-            if (D == 128) PKV_QBLAUNCH(__half, 128, PKV_QMODE_INT4_ASYM);
-            else PKV_QBLAUNCH(__half, 64, PKV_QMODE_INT4_ASYM);
-        } else {
-            if (D == 128) PKV_QBLAUNCH(__half, 128, PKV_QMODE_FP8_E4M3);
-            else PKV_QBLAUNCH(__half, 64, PKV_QMODE_FP8_E4M3);
-        }
-    }
-#undef PKV_QBLAUNCH
-    return launch_status();
-}
-
-template <typename T, int D, int QMODE, bool SPLIT>
+template <typename T, int D, int QMODE, int NG, bool SPLIT>
 void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
     dim3 grid(SPLIT ? parts : 1, hkv, batch);
-    paged_decode_quant_kernel<T, D, QMODE, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+    paged_decode_quant_kernel<T, D, QMODE, NG, SPLIT><<<grid, NW * 32, 0, st>>>(a);
 }
 
-template <bool SPLIT>
-int run(const QDecodeArgs& a, int D, int qmode, int dtype, int parts, int hkv, int batch,
-        cudaStream_t st) {
-#define PKV_QLAUNCH(TT, DD, QM) launch<TT, DD, QM, SPLIT>(a, parts, hkv, batch, st)
-    if (dtype == PKV_DTYPE_BF16) {
-        if (qmode == PKV_QMODE_INT4_ASYM) {
-            if (D == 128) PKV_QLAUNCH(__nv_bfloat16, 128, PKV_QMODE_INT4_ASYM);
-            else PKV_QLAUNCH(__nv_bfloat16, 64, PKV_QMODE_INT4_ASYM);
-        } else {
-            if (D == 128) PKV_QLAUNCH(__nv_bfloat16, 128, PKV_QMODE_FP8_E4M3);
-            else PKV_QLAUNCH(__nv_bfloat16, 64, PKV_QMODE_FP8_E4M3);
-        }
-    } else {
-        if (qmode == PKV_QMODE_INT4_ASYM) {
-            if (D == 128) PKV_QLAUNCH(__half, 128, PKV_QMODE_INT4_ASYM);
-            else PKV_QLAUNCH(__half, 64, PKV_QMODE_INT4_ASYM);
-        } else {
-            if (D == 128) PKV_QLAUNCH(__half, 128, PKV_QMODE_FP8_E4M3);
-            else PKV_QLAUNCH(__half, 64, PKV_QMODE_FP8_E4M3);
-        }
-    }
-#undef PKV_QLAUNCH
+// The kernel for (dtype, head dim, mode, column groups); balanced or
+// partitioned (SPLIT: partials, else a single pass).
+template <bool BALANCED, bool SPLIT>
+int dispatch(const QDecodeArgs& a, int D, int qmode, int ng, int dtype, int parts, int hkv, int batch,
+             int nwt, cudaStream_t st) {
+#define PKV_Q(TT, DD, QM, NN)                                                          \
+    do {                                                                                 \
+        if (BALANCED) launch_balanced<TT, DD, QM, NN>(a, batch, nwt, st);              \
+        else launch<TT, DD, QM, NN, SPLIT>(a, parts, hkv, batch, st);                   \
+    } while (0)
+#define PKV_QT(TT)                                                                       \
+    do {                                                                                 \
+        if (qmode == PKV_QMODE_INT4_ASYM) {                                              \
+            if (D == 128 && ng == 2) PKV_Q(TT, 128, PKV_QMODE_INT4_ASYM, 2);             \
+            else if (D == 128) PKV_Q(TT, 128, PKV_QMODE_INT4_ASYM, 1);                   \
+            else PKV_Q(TT, 64, PKV_QMODE_INT4_ASYM, 1);                                  \
+        } else {                                                                         \
+            if (D == 128) PKV_Q(TT, 128, PKV_QMODE_FP8_E4M3, 1);                         \
+            else PKV_Q(TT, 64, PKV_QMODE_FP8_E4M3, 1);                                   \
+        }                                                                                \
+    } while (0)
+    if (dtype == PKV_DTYPE_BF16) PKV_QT(__nv_bfloat16);
+    else PKV_QT(__half);
+#undef PKV_QT
+#undef PKV_Q
     return launch_status();
 }
 
@@ -734,7 +806,11 @@ extern "C" int pkv_paged_attention_decode_quant(
     if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) ||
         num_q_heads / num_kv_heads > 8 || n_sink > pkv::BS || batch > 65535 || num_kv_heads > 65535)
         return PKV_ERR_UNSUPPORTED;
-    if (qmode == PKV_QMODE_INT4_ASYM && group_size != head_dim) return PKV_ERR_UNSUPPORTED;
+    // INT4 groups: one per (token, head), or 64 columns at head dim 128
+    const int ng = qmode == PKV_QMODE_INT4_ASYM && group_size > 0 ? head_dim / group_size : 1;
+    if (qmode == PKV_QMODE_INT4_ASYM &&
+        !(group_size == head_dim || (head_dim == 128 && group_size == 64)))
+        return PKV_ERR_UNSUPPORTED;
     const int32_t ps = partition_size == 0 ? pkv::auto_partition_size(batch, num_q_heads, max_blocks)
                                            : partition_size;
     if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
@@ -778,8 +854,9 @@ extern "C" int pkv_paged_attention_decode_quant(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (partition_size == 0 && a.max_parts > 1 && pkv::use_balanced(batch, num_kv_heads, max_blocks)) {
         // balanced split, all CTAs resident: kCtasPerSm CTAs of NW warps per SM
-        const int per_sm = pkv::NW * (qmode == PKV_QMODE_INT4_ASYM ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM>
-                                                               : pkv::kCtasPerSm<PKV_QMODE_FP8_E4M3>);
+        const int per_sm = pkv::NW * (qmode != PKV_QMODE_INT4_ASYM ? pkv::kCtasPerSm<PKV_QMODE_FP8_E4M3>
+                                      : ng == 2 ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 2>
+                                                : pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 1>);
         const int nwt = pkv::balanced_warps(static_cast<int64_t>(batch) * num_kv_heads * max_blocks, per_sm);
         const size_t rows = static_cast<size_t>(nwt) * a.G + static_cast<size_t>(batch) * num_q_heads;
         if (!workspace || workspace_bytes < pkv::balanced_bytes(batch, num_q_heads, a.G, head_dim, nwt))
@@ -787,21 +864,21 @@ extern "C" int pkv_paged_attention_decode_quant(
         if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
         a.ws_o = static_cast<float*>(workspace);
         a.ws_ml = a.ws_o + rows * head_dim;
-        int r = pkv::run_balanced(a, head_dim, qmode, dtype, batch, nwt, cs);
+        int r = pkv::dispatch<true, true>(a, head_dim, qmode, ng, dtype, 0, num_kv_heads, batch, nwt, cs);
         if (r != PKV_OK) return r;
         return pkv::launch_balanced_merge(context_lens, batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
                                           nwt, a.ws_o, a.ws_ml, out, dtype, cs);
     }
     if (a.max_parts <= 1) {
         a.part_blocks = max_blocks > 0 ? max_blocks : 1;
-        return pkv::run<false>(a, head_dim, qmode, dtype, 1, num_kv_heads, batch, cs);
+        return pkv::dispatch<false, false>(a, head_dim, qmode, ng, dtype, 1, num_kv_heads, batch, 0, cs);
     }
     const size_t need = static_cast<size_t>(batch) * num_q_heads * a.max_parts * (head_dim + 2) * sizeof(float);
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (!pkv::aligned16(workspace)) return PKV_ERR_MISALIGNED;
     a.ws_o = static_cast<float*>(workspace);
     a.ws_ml = a.ws_o + static_cast<size_t>(batch) * num_q_heads * a.max_parts * head_dim;
-    int r = pkv::run<true>(a, head_dim, qmode, dtype, a.max_parts, num_kv_heads, batch, cs);
+    int r = pkv::dispatch<false, true>(a, head_dim, qmode, ng, dtype, a.max_parts, num_kv_heads, batch, 0, cs);
     if (r != PKV_OK) return r;
     return pkv_paged_attention_decode_merge(context_lens, batch, num_q_heads, head_dim, max_blocks,
                                             block_size, ps, workspace, workspace_bytes, out, dtype,

@@ -195,3 +195,12 @@ def test_quant_zero_contexts_and_head64_group8(pkv, cuda_dev, qmode):
     assert (got[zero] == 0).all()
     keep = [i for i in range(len(c.decoded)) if i not in zero]
     assert_close(got[keep], expected(c, keep), what="%s, G 8, D 64" % qmode)
+
+
+def test_quant_int4_group64_many_short_sequences(pkv, cuda_dev):
+    w = _short_quant_workload(group_size=64, n_sink=8)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    assert _is_balanced(c)
+    got = _decode_quant(pkv, c)
+    assert pkv.pkv_device_status() == 0
+    assert_close(got, expected(c), what="int4 g64, 640 short sequences")

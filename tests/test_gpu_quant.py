@@ -148,3 +148,41 @@ def test_quant_prefix_cow_int4(pkv, cuda_dev):
     c = build(pkv, w, cuda_dev, quant="int4")
     assert len(c.all_pairs) == 8
     assert_close(_decode_quant(pkv, c, 0), expected(c), what="prefix int4")
+
+
+# The pages' own INT4 layout: groups of 64 along the head dim (two (scale,
+# zero) pairs per token and head at D = 128) and 8 sink tokens.
+
+@pytest.mark.parametrize("ps", [0, 64, 4096])
+def test_int4_group64_decode(pkv, cuda_dev, ps):
+    w = syn.workload("quant", batch=5, ctx=1000, num_blocks=1024, group_size=64, n_sink=8)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    assert c.group_size == 64
+    assert_close(_decode_quant(pkv, c, ps), expected(c), what="g64 ps %d" % ps)
+
+
+@pytest.mark.parametrize("ctx", [1, 7, 8, 9, 16, 17, 33])
+def test_int4_group64_short_contexts_and_8_sinks(pkv, cuda_dev, ctx):
+    w = syn.workload("quant", batch=3, ctx=ctx, num_blocks=64, group_size=64, n_sink=8)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    want = expected(c)
+    for ps in (0, 16):
+        assert_close(_decode_quant(pkv, c, ps), want, what="g64 ctx %d" % ctx)
+
+
+def test_int4_group64_full_size_sampled(pkv, cuda_dev):
+    """32 sequences x 16,384 tokens in the pages' layout (g = 64, 8 sinks):
+    sampled outputs within the bound (balanced split)."""
+    w = syn.workload("quant", group_size=64, n_sink=8)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    got = _decode_quant(pkv, c, 0)
+    sample = [0, 21, 31]
+    assert_close(got[sample], expected(c, sample), what="g64 full size")
+
+
+def test_int4_group_size_checks(pkv, cuda_dev):
+    """Decode supports g = head dim, and g = 64 at head dim 128."""
+    w = syn.workload("quant", batch=2, ctx=40, num_blocks=64, group_size=32)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    with pytest.raises(pkv.PkvError):
+        _decode_quant(pkv, c, 0)
