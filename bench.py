@@ -63,6 +63,7 @@ WORKLOADS = {
     "quant_int4": ("quant", {}, "int4"),
     "quant_fp8": ("quant", {}, "fp8"),
     "quant_int4_g64": ("quant", {"group_size": 64, "n_sink": 8}, "int4"),
+    "quant_int4_bie": ("quant", {"group_size": 64, "n_sink": 8, "window": 128}, "int4"),
     "prefix_cow": ("prefix_cow", {}, None),
     "verify_b64_g5": ("llama3_8b_b64", {}, None),
     "prefill_chunk512": ("llama3_8b_b64", {"lens": [4096] * 8, "num_blocks": 4096}, None),
@@ -88,6 +89,10 @@ DESCRIPTIONS = {
                       "the head dim (two fp16 scale/zero pairs per token and head, 36 B per 64 "
                       "elements), 8 bf16 sink tokens, 32 q / 8 KV heads, head dim 128, values "
                       "N(0,1) with 1% outliers at +-8",
+    "quant_int4_bie": "the pages' full cache layout on 32 sequences x 16,384 tokens: INT4 groups "
+                      "of 64 along the head dim, 8 bf16 sink tokens, and the last 128 tokens (whole "
+                      "blocks) read from a 16-bit window ring, 32 q / 8 KV heads, head dim 128, "
+                      "values N(0,1) with 1% outliers at +-8",
     "prefix_cow": "8 sequences forked from a shared 2,000-token prompt, each extended by a "
                   "seeded tail of 1..300 tokens, 32 q / 8 KV heads, head dim 128, bf16",
     "verify_b64_g5": "speculative verify on the 64-sequence Llama-3-8B-shaped layer: the target's "
@@ -254,6 +259,7 @@ class Cache:
         B = len(decoded)
         self.B = B
         self.n_sink = w.get("n_sink", 0)
+        self.window = 0
         if qmode is None:
             self.k_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
             self.v_pool = torch.empty((NB, Hkv, BS, D), dtype=dt, device=device)
@@ -274,6 +280,11 @@ class Cache:
             if qmode == "int4":
                 self.cache["k_zero"] = torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device)
                 self.cache["v_zero"] = torch.empty((NB, Hkv, BS, ng), dtype=f16, device=device)
+            self.window = w.get("window", 0)
+            if self.window:
+                R = self.window // BS + 1
+                self.cache["win_k"] = torch.zeros((B, R, Hkv, BS, D), dtype=dt, device=device)
+                self.cache["win_v"] = torch.zeros((B, R, Hkv, BS, D), dtype=dt, device=device)
             self.pools = [self.cache[k] for k in ("k_codes", "k_scale", "k_zero", "v_codes",
                                                   "v_scale", "v_zero") if k in self.cache]
         row_of = {h: i for i, h in enumerate(decoded)}
@@ -357,7 +368,7 @@ class Cache:
             positions = torch.from_numpy(np.asarray(positions, dtype=np.int32)).to(self.dev)
         sidx = torch.full((k.shape[0],), seq_row, dtype=torch.int32, device=self.dev)
         self.pkv.pkv_kv_append_quant(k, v, slots, positions, sidx, self.cache, self.n_sink,
-                                     self.qmode, self.group_size)
+                                     self.qmode, self.group_size, window=self.window)
 
     def bytes_per_token(self):
         Hkv, D = self.w["hkv"], self.w["d"]
@@ -372,7 +383,17 @@ class Cache:
         ctx = self.ctx_host if ctx is None else ctx
         total = int(np.sum(ctx)) * self.bytes_per_token()
         if self.qmode is not None:
-            total += int(np.sum(np.minimum(ctx, self.n_sink))) * 2 * self.w["hkv"] * self.w["d"] * 2
+            # sink and window tokens are read in 16-bit, not as codes; the window
+            # is the last `window` tokens rounded down to a block boundary
+            w16 = np.array([c - max(int(c) - self.window, 0) // 16 * 16 if self.window else 0
+                            for c in ctx])
+            sinks = np.minimum(ctx, self.n_sink)
+            if self.window:
+                ws = ctx - w16
+                sinks = np.minimum(sinks, ws)  # sinks inside the window are read once
+                total -= int(np.sum(w16)) * self.bytes_per_token()
+                total += int(np.sum(w16)) * 2 * self.w["hkv"] * self.w["d"] * 2
+            total += int(np.sum(sinks)) * 2 * self.w["hkv"] * self.w["d"] * 2
         return total
 
     def step(self, q=None, k_new=None, v_new=None, slots=None, tables=None, lens=None, out=None,
@@ -394,10 +415,10 @@ class Cache:
             return
         positions = self.positions if positions is None else positions
         pkv.pkv_kv_append_quant(k_new, v_new, slots, positions, self.seq_idx, self.cache,
-                                self.n_sink, self.qmode, self.group_size, stream)
+                                self.n_sink, self.qmode, self.group_size, stream, window=self.window)
         pkv.pkv_paged_attention_decode_quant(q, self.cache, self.n_sink, tables, lens,
                                              self.w["scale"], out, self.qmode, self.group_size, ws,
-                                             self.partition_size, stream)
+                                             self.partition_size, stream, window=self.window)
 
     def launches_per_step(self):
         return (2 if self.split else 1) + (1 if self.qmode else 0)
@@ -766,11 +787,24 @@ def oracle_sample(name, S):
                     cache["v_zero"][blk, :, off] = vz[t]
             cache["sink_k"][i] = ks[i][:ns]
             cache["sink_v"][i] = vs[i][:ns]
+        win = w.get("window", 0)
+        if win:
+            R = kvcache.ring_blocks(win)
+            cache["win_k"] = np.zeros((S, R, Hkv, 16, D))
+            cache["win_v"] = np.zeros((S, R, Hkv, 16, D))
+            for i in range(S):
+                for t in range(kvcache.window_start(ks[i].shape[0], win), ks[i].shape[0]):
+                    cache["win_k"][i, (t // 16) % R, :, t % 16] = ks[i][t]
+                    cache["win_v"][i, (t // 16) % R, :, t % 16] = vs[i][t]
 
         def decode():
-            kvcache.paged_attention_decode_quant(q, cache, tables, ctx, w["scale"], ns, qmode, gsz)
+            kvcache.paged_attention_decode_quant(q, cache, tables, ctx, w["scale"], ns, qmode, gsz,
+                                                 window=win)
         per_tok = 2 * Hkv * (D // 2 + 4 * ng) if qmode == "int4" else 2 * Hkv * (D + 2)
-        kvb = int(np.sum(ctx)) * per_tok + int(np.sum(np.minimum(ctx, ns))) * 2 * Hkv * D * 2
+        w16 = np.array([c - kvcache.window_start(int(c), win) if win else 0 for c in ctx])
+        sinks = np.minimum(np.minimum(ctx, ns), ctx - w16)
+        kvb = (int(np.sum(ctx - w16)) * per_tok + int(np.sum(w16)) * 2 * Hkv * D * 2
+               + int(np.sum(sinks)) * 2 * Hkv * D * 2)
     return decode, kvb, S, int(np.sum(ctx))
 
 
@@ -788,7 +822,7 @@ def cpu_worker(name, min_seconds, S):
 
 
 CPU_SAMPLE_SEQS = {"llama3_8b_b64": 16, "long_splitk": 1, "quant_int4": 1, "quant_fp8": 1,
-                   "quant_int4_g64": 1, "prefix_cow": 8}
+                   "quant_int4_g64": 1, "quant_int4_bie": 1, "prefix_cow": 8}
 
 
 def cpu_baseline(name, min_seconds):

@@ -397,27 +397,42 @@ int pkv_paged_attention_decode_static_ws(const void* q, const void* k_pool, cons
  * Sinks: if positions[t] < n_sink, the 16-bit row is also copied to
  * sink_k/sink_v[seq_idx[t], positions[t], h, :]; sink buffers are
  * [sink_rows, n_sink, Hkv, head_dim] in dtype (nullable when n_sink == 0).
+ * Local window ("The 8GB VRAM Breakthrough", §5 flowchart: the most recent
+ * tokens go to the high-precision pool): with window > 0 (a multiple of
+ * block_size) every row is also copied to the 16-bit ring win_k/win_v
+ * [sink_rows, window / block_size + 1, Hkv, block_size, head_dim] (dtype)
+ * at ring block (p / block_size) % (window / block_size + 1), offset
+ * p % block_size, p = positions[t]; nullable when window == 0.  Within one
+ * call, a row whose slot the entry one ring span (window + block_size)
+ * further on takes again (same seq_idx, position p + span) is not written;
+ * other layouts in which two rows of one call share a slot leave that slot
+ * undefined, so pass a sequence's tokens as consecutive entries.
  * positions / seq_idx: device int32 [num_tokens]. */
 int pkv_kv_append_quant(const void* k, const void* v, const int64_t* slot_mapping,
                         const int32_t* positions, const int32_t* seq_idx, int32_t num_tokens,
                         void* k_codes, void* k_scale, void* k_zero, void* v_codes,
                         void* v_scale, void* v_zero, void* sink_k, void* sink_v, int32_t n_sink,
-                        int32_t sink_rows, int32_t num_blocks, int32_t num_kv_heads,
+                        int32_t sink_rows, void* win_k, void* win_v, int32_t window,
+                        int32_t num_blocks, int32_t num_kv_heads,
                         int32_t head_dim, int32_t block_size, int32_t group_size, int qmode,
                         int dtype, void* stream);
 
 /* Decode attention over a quantised cache: as pkv_paged_attention_decode
  * with K_t, V_t the dequantised values ((q - z) * s for INT4, e4m3 * s for
  * FP8), except that positions t < n_sink read sink_k/sink_v[b, t, kv_head]
- * (16-bit, row b of the sink buffers belongs to batch entry b).  q and out
- * are 16-bit (dtype).  Supported: block_size 16, head_dim 128 or 64;
+ * (16-bit, row b of the sink buffers belongs to batch entry b), and, with
+ * window > 0, the whole blocks from w0 = block_size * floor(max(ctx -
+ * window, 0) / block_size) on read the 16-bit window ring win_k/win_v[b]
+ * (see pkv_kv_append_quant; between window and window + block_size - 1
+ * tokens).  q and out are 16-bit (dtype).  Supported: block_size 16, head_dim 128 or 64;
  * INT4 group_size == head_dim, or 64 at head_dim 128 (the pages' layout:
  * two (scale, zero) pairs per token and head); n_sink <= block_size (the
  * pages keep 8); 1 <= G <= 8. */
 int pkv_paged_attention_decode_quant(const void* q, const void* k_codes, const void* k_scale,
                                      const void* k_zero, const void* v_codes, const void* v_scale,
                                      const void* v_zero, const void* sink_k, const void* sink_v,
-                                     int32_t n_sink, const int32_t* block_tables,
+                                     int32_t n_sink, const void* win_k, const void* win_v,
+                                     int32_t window, const int32_t* block_tables,
                                      const int32_t* context_lens, int32_t batch,
                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                      int32_t num_blocks, int32_t block_size, int32_t max_blocks,

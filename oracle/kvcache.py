@@ -12,6 +12,16 @@ and attention over a quantised cache (test infrastructure).
   (sink slots included) and the sink tokens are *also* copied into a
   per-sequence 16-bit buffer ``sink[seq, pos, head, :]``; attention reads the
   sink buffer for positions < n_sink and the codes elsewhere.
+* Local window: the most recent tokens also stay in 16-bit ("The 8GB VRAM
+  Breakthrough", §5 flowchart: the "Token Position Router" sends "Sink
+  (0..7) or Local Window (Last 128)" to the high-precision FP16 pool, the
+  middle context body to the quantiser).  Reading used: every token is
+  quantised as above *and* copied to a per-sequence 16-bit ring of
+  ``window / block_size + 1`` blocks (token p in ring block
+  ``(p // bs) % R``, offset ``p % bs``); attention reads 16-bit values for
+  the whole blocks from ``window_start`` on -- the last ``window`` tokens
+  rounded down to a block boundary, so between window and window + bs - 1
+  tokens -- and codes before that.
 * Copy-on-write: cloning a shared block copies the whole physical block
   ("A Ideia de 60 Anos...", section "o bônus que paga o ingresso:
   compartilhar": copy only the affected block, then write).
@@ -68,8 +78,21 @@ def quantize_token(x_heads, qmode, group_size):
     raise ValueError(qmode)
 
 
+def window_start(ctx, window, block_size=16):
+    """First position read from the 16-bit window: the last ``window``
+    tokens rounded down to a block boundary (ctx when there is no window)."""
+    if window <= 0:
+        return ctx
+    return max(0, ctx - window) // block_size * block_size
+
+
+def ring_blocks(window, block_size=16):
+    """Blocks in a sequence's 16-bit window ring."""
+    return window // block_size + 1
+
+
 def kv_append_quant(k, v, slot_mapping, positions, seq_idx, cache, n_sink, qmode,
-                    group_size, block_size=16):
+                    group_size, block_size=16, window=0):
     """Quantised scatter of new tokens plus the 16-bit sink copies.
 
     k, v: [T, Hkv, D] values exact in binary32; cache: dict with
@@ -91,6 +114,10 @@ def kv_append_quant(k, v, slot_mapping, positions, seq_idx, cache, n_sink, qmode
         if pos < n_sink:
             cache["sink_k"][int(seq_idx[t]), pos] = k[t]
             cache["sink_v"][int(seq_idx[t]), pos] = v[t]
+        if window > 0:
+            rb = (pos // block_size) % ring_blocks(window, block_size)
+            cache["win_k"][int(seq_idx[t]), rb, :, pos % block_size] = k[t]
+            cache["win_v"][int(seq_idx[t]), rb, :, pos % block_size] = v[t]
 
 
 def dequantize_cache_row(cache, name, blk, head, off, qmode, group_size):
@@ -108,8 +135,9 @@ def dequantize_cache_row(cache, name, blk, head, off, qmode, group_size):
 
 
 def paged_attention_decode_quant(q, cache, block_tables, context_lens, scale, n_sink, qmode,
-                                 group_size, block_size=16):
-    """Attention over the dequantised cache, sink positions read in 16-bit."""
+                                 group_size, block_size=16, window=0):
+    """Attention over the dequantised cache, sink and window positions read
+    in 16-bit (window ring ``win_k/win_v [B, R, Hkv, block_size, D]``)."""
     q = np.asarray(q, dtype=np.float64)
     B, Hq, D = q.shape
     Hkv = cache["k_codes"].shape[1]
@@ -117,10 +145,16 @@ def paged_attention_decode_quant(q, cache, block_tables, context_lens, scale, n_
     out = np.zeros((B, Hq, D), dtype=np.float64)
     for b in range(B):
         ctx = int(context_lens[b])
+        ws = window_start(ctx, window, block_size)
         for g in range(Hkv):
             K = np.zeros((ctx, D))
             V = np.zeros((ctx, D))
             for t in range(ctx):
+                if t >= ws:
+                    rb = (t // block_size) % ring_blocks(window, block_size)
+                    K[t] = cache["win_k"][b, rb, g, t % block_size]
+                    V[t] = cache["win_v"][b, rb, g, t % block_size]
+                    continue
                 if t < n_sink:
                     K[t] = cache["sink_k"][b, t, g]
                     V[t] = cache["sink_v"][b, t, g]
@@ -154,18 +188,21 @@ def quantize_sequence(x_seq, qmode, group_size):
     raise ValueError(qmode)
 
 
-def sequence_attention_quant(q_seq, k_seq, v_seq, scale, n_sink, qmode, group_size):
+def sequence_attention_quant(q_seq, k_seq, v_seq, scale, n_sink, qmode, group_size, window=0):
     """Decode attention of one sequence over its quantised cache.
 
     The cache holds the oracle's own quantisation of the logical rows; the
-    first n_sink positions use the 16-bit originals.  q_seq: [Hq, D];
-    k_seq, v_seq: [ctx, Hkv, D].
+    first n_sink positions and the positions from window_start on use the
+    16-bit originals.  q_seq: [Hq, D]; k_seq, v_seq: [ctx, Hkv, D].
     """
     k_deq = quantize_sequence(k_seq, qmode, group_size)[0]
     v_deq = quantize_sequence(v_seq, qmode, group_size)[0]
     ns = min(n_sink, k_seq.shape[0])
     k_deq[:ns] = np.asarray(k_seq[:ns], dtype=np.float64)
     v_deq[:ns] = np.asarray(v_seq[:ns], dtype=np.float64)
+    ws = window_start(k_seq.shape[0], window)
+    k_deq[ws:] = np.asarray(k_seq[ws:], dtype=np.float64)
+    v_deq[ws:] = np.asarray(v_seq[ws:], dtype=np.float64)
     q_seq = np.asarray(q_seq, dtype=np.float64)
     Hq, D = q_seq.shape
     Hkv = k_seq.shape[1]

@@ -91,11 +91,11 @@ _SIGS = {
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _i32, _int,
          _vp], _int),
     "pkv_kv_append_quant": (
-        [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
-         _i32, _i32, _i32, _i32, _int, _int, _vp], _int),
+        [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32,
+         _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _int, _int, _vp], _int),
     "pkv_paged_attention_decode_quant": (
-        [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
-         _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32, _int, _int, _vp], _int),
+        [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _vp, _vp, _i32, _i32,
+         _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz, _i32, _int, _int, _vp], _int),
     "pkv_copy_blocks": ([_vp, _vp, _i32, _vp, _i32, _i32, _vp], _int),
     "pkv_device_status": ([_p_i32, _vp], _int),
 }
@@ -416,23 +416,26 @@ def pkv_paged_attention_decode_static_ws(q, k_pool, v_pool, block_tables, contex
 
 
 def pkv_kv_append_quant(k, v, slot_mapping, positions, seq_idx, cache, n_sink, qmode,
-                        group_size=0, stream=None):
-    """cache: dict with k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, sink_k, sink_v."""
+                        group_size=0, stream=None, window=0):
+    """cache: dict with k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, sink_k, sink_v,
+    and win_k, win_v [rows, window / block_size + 1, Hkv, block_size, D] when window > 0."""
     T, Hkv, D = k.shape
     kc = cache["k_codes"]
     NB, _, BS, _ = kc.shape
-    sink_rows = cache["sink_k"].shape[0] if cache.get("sink_k") is not None else 0
+    rows_of = cache.get("sink_k") if cache.get("sink_k") is not None else cache.get("win_k")
+    sink_rows = rows_of.shape[0] if rows_of is not None else 0
     _check(lib.pkv_kv_append_quant(
         _ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(positions), _ptr(seq_idx), T, _ptr(kc),
         _ptr(cache["k_scale"]), _ptr(cache.get("k_zero")), _ptr(cache["v_codes"]),
         _ptr(cache["v_scale"]), _ptr(cache.get("v_zero")), _ptr(cache.get("sink_k")),
-        _ptr(cache.get("sink_v")), n_sink, sink_rows, NB, Hkv, D, BS, group_size or D,
+        _ptr(cache.get("sink_v")), n_sink, sink_rows, _ptr(cache.get("win_k")),
+        _ptr(cache.get("win_v")), window, NB, Hkv, D, BS, group_size or D,
         _qmode_code(qmode), _dtype_code(k), _stream(stream)), "pkv_kv_append_quant")
 
 
 def pkv_paged_attention_decode_quant(q, cache, n_sink, block_tables, context_lens, scale, out,
                                      qmode, group_size=0, workspace=None, partition_size=0,
-                                     stream=None):
+                                     stream=None, window=0):
     B, Hq, D = q.shape
     kc = cache["k_codes"]
     NB, Hkv, BS, _ = kc.shape
@@ -440,7 +443,8 @@ def pkv_paged_attention_decode_quant(q, cache, n_sink, block_tables, context_len
     _check(lib.pkv_paged_attention_decode_quant(
         _ptr(q), _ptr(kc), _ptr(cache["k_scale"]), _ptr(cache.get("k_zero")),
         _ptr(cache["v_codes"]), _ptr(cache["v_scale"]), _ptr(cache.get("v_zero")),
-        _ptr(cache.get("sink_k")), _ptr(cache.get("sink_v")), n_sink, _ptr(block_tables),
+        _ptr(cache.get("sink_k")), _ptr(cache.get("sink_v")), n_sink, _ptr(cache.get("win_k")),
+        _ptr(cache.get("win_v")), window, _ptr(block_tables),
         _ptr(context_lens), B, Hq, Hkv, D, NB, BS, block_tables.shape[1], group_size or D,
         float(scale), _ptr(out), _ptr(workspace), ws_bytes, partition_size, _qmode_code(qmode),
         _dtype_code(q), _stream(stream)), "pkv_paged_attention_decode_quant")

@@ -94,6 +94,8 @@ struct QuantArgs {
     __half* scale[2];
     __half* zero[2];
     void* sink[2];
+    void* win[2];        // 16-bit window rings [sink_rows, ring, Hkv, block_size, D] or null
+    int window, ring;    // window tokens (0: none) and ring blocks (window / block_size + 1)
     int* status;
 };
 
@@ -190,6 +192,27 @@ __global__ void kv_append_quant_kernel(QuantArgs a) {
         }
 
         const int pos = a.positions[t];
+        if (a.window > 0) {
+            // every token passes through the 16-bit window ring of its
+            // sequence; a token whose ring slot a later token of the same
+            // call takes again (the entry one ring span ahead: same sequence,
+            // position + span) is not written, so no two writes of one call
+            // race on a slot
+            const int sr = a.seq_idx[t];
+            const int64_t span = static_cast<int64_t>(a.ring) * a.block_size;
+            const bool superseded = t + span < a.T && a.seq_idx[t + span] == sr &&
+                                    a.positions[t + span] == pos + span;
+            if (pos < 0 || sr < 0 || sr >= a.sink_rows) {
+                if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_SINK);
+            } else if (!superseded) {
+                const int64_t rb = (pos / a.block_size) % a.ring;
+                T* dst = static_cast<T*>(a.win[which]) +
+                         (((static_cast<int64_t>(sr) * a.ring + rb) * a.hkv + h) * a.block_size +
+                          pos % a.block_size) * a.D +
+                         lane * EPL;
+                copy_row<T, EPL>(src, dst);
+            }
+        }
         if (pos < a.n_sink) {
             const int sr = a.seq_idx[t];
             if (pos < 0 || sr < 0 || sr >= a.sink_rows) {
@@ -271,14 +294,16 @@ extern "C" int pkv_kv_append_quant(const void* k, const void* v, const int64_t* 
                                    const int32_t* positions, const int32_t* seq_idx,
                                    int32_t num_tokens, void* k_codes, void* k_scale, void* k_zero,
                                    void* v_codes, void* v_scale, void* v_zero, void* sink_k,
-                                   void* sink_v, int32_t n_sink, int32_t sink_rows,
-                                   int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                                   void* sink_v, int32_t n_sink, int32_t sink_rows, void* win_k,
+                                   void* win_v, int32_t window, int32_t num_blocks,
+                                   int32_t num_kv_heads, int32_t head_dim,
                                    int32_t block_size, int32_t group_size, int qmode, int dtype,
                                    void* stream) {
     if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
-        n_sink < 0 || (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16))
+        n_sink < 0 || window < 0 || (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16))
         return PKV_ERR_INVALID_ARG;
     if (qmode != PKV_QMODE_INT4_ASYM && qmode != PKV_QMODE_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    if (window % block_size != 0) return PKV_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
     const int epl = head_dim / 32;
     if (qmode == PKV_QMODE_INT4_ASYM) {
@@ -295,6 +320,8 @@ extern "C" int pkv_kv_append_quant(const void* k, const void* v, const int64_t* 
         return PKV_ERR_INVALID_ARG;
     if (qmode == PKV_QMODE_INT4_ASYM && (!k_zero || !v_zero)) return PKV_ERR_INVALID_ARG;
     if (n_sink > 0 && (!sink_k || !sink_v || sink_rows <= 0)) return PKV_ERR_INVALID_ARG;
+    if (window > 0 && (!win_k || !win_v || sink_rows <= 0)) return PKV_ERR_INVALID_ARG;
+    if (window > 0 && (!pkv::aligned16(win_k) || !pkv::aligned16(win_v))) return PKV_ERR_MISALIGNED;
     if (!pkv::aligned16(k) || !pkv::aligned16(v) || !pkv::aligned16(k_codes) ||
         !pkv::aligned16(v_codes) || (n_sink > 0 && (!pkv::aligned16(sink_k) || !pkv::aligned16(sink_v))))
         return PKV_ERR_MISALIGNED;
@@ -322,6 +349,10 @@ extern "C" int pkv_kv_append_quant(const void* k, const void* v, const int64_t* 
     a.zero[1] = static_cast<__half*>(v_zero);
     a.sink[0] = sink_k;
     a.sink[1] = sink_v;
+    a.win[0] = win_k;
+    a.win[1] = win_v;
+    a.window = window;
+    a.ring = window / block_size + 1;
     a.status = st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (dtype == PKV_DTYPE_BF16) {

@@ -36,6 +36,8 @@
 // logits are recomputed in fp32 from the 16-bit sink keys, their PV weights
 // are zero in the MMA, and P * sink_v is added to the accumulator directly.
 
+#include <type_traits>
+
 #include "balanced.cuh"
 
 namespace pkv {
@@ -67,6 +69,9 @@ struct QDecodeArgs {
     const void* sink_k;
     const void* sink_v;
     int n_sink;
+    const void* win_k;   // 16-bit window rings [rows, ring, Hkv, 16, D] (window > 0)
+    const void* win_v;
+    int window, ring;
     const int32_t* tables;
     const int32_t* ctx_lens;
     int hq, hkv, G, num_blocks, max_blocks, part_blocks, max_parts;
@@ -125,9 +130,11 @@ struct QState {
     float m0, m1, l0, l1;
     float corr[NG][2];  // per column group, heads 2c / 2c + 1
     float o[MT][4];
+    bool true_units;    // o already in true units (a window block was attended)
     __device__ __forceinline__ void init() {
         m0 = m1 = neg_inf();
         l0 = l1 = 0.f;
+        true_units = false;
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) corr[gi][0] = corr[gi][1] = 0.f;
 #pragma unroll
@@ -154,7 +161,7 @@ __device__ __forceinline__ int pv_column(int e, int g) {
 // of sequence b, KV head kvh (context ctx): query fragments, then every block
 // loaded into registers and attended into st (reset first).  sq is the
 // lane's slot of the warp's shared query slice (row t at sq[t * 32]).
-template <typename T, int D, int QMODE, int NG>
+template <typename T, int D, int QMODE, int NG, bool WIN>
 __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh, int ctx, int lb_first,
                                            int lb_end, int stride, uint4* sq, QState<D / 16, NG>& st) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
@@ -554,6 +561,135 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         }
     };
 
+    // ---- 16-bit window blocks (the run's last blocks): read from the ring
+    // in the 16-bit decode layout, accumulated into o in true units (o is
+    // converted once, before the first of them; they come after every
+    // quantised block of the pass)
+    auto attend16 = [&](int lb) {
+        using H = Half16<T>;
+        constexpr int KC = D / 32;
+        constexpr int VC = D / 64;
+        if (!st.true_units) {
+            // the correction is a per-lane partial sum: total it over the 8
+            // token lanes first
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    corr[gi][0] += __shfl_xor_sync(0xffffffffu, corr[gi][0], off);
+                    corr[gi][1] += __shfl_xor_sync(0xffffffffu, corr[gi][1], off);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int el = INT4 ? pv_e<NG, MT>(mt, 0) : mt;
+                const int gi = INT4 ? (el >> 3) / VPG : 0;
+                const float u = INT4 ? ((el & 1) ? kTwo24 * 0.0625f : kTwo24) : 1.f;
+                o[mt][0] = o[mt][0] * u - corr[gi][0];
+                o[mt][1] = o[mt][1] * u - corr[gi][1];
+                o[mt][2] = o[mt][2] * u - corr[gi][0];
+                o[mt][3] = o[mt][3] * u - corr[gi][1];
+            }
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) corr[gi][0] = corr[gi][1] = 0.f;
+            st.true_units = true;
+        }
+        const int64_t rbase = ((static_cast<int64_t>(b) * a.ring + lb % a.ring) * a.hkv + kvh) * (BS * D);
+        const T* wk = static_cast<const T*>(a.win_k) + rbase;
+        const T* wv = static_cast<const T*>(a.win_v) + rbase;
+        // QK^T: K rows g, g+8 and query head g at [32i + 8c, +8)
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const T* qrow = static_cast<const T*>(a.q) +
+                            (static_cast<int64_t>(b) * a.hq + kvh * a.G + (g < a.G ? g : 0)) * D;
+            uint4 k0[KC], k1[KC], qv[KC];
+#pragma unroll
+            for (int i = 0; i < KC; ++i) {
+                k0[i] = ldg_stream(wk + g * D + 32 * i + 8 * c);
+                k1[i] = ldg_stream(wk + (g + 8) * D + 32 * i + 8 * c);
+                qv[i] = g < a.G ? *reinterpret_cast<const uint4*>(qrow + 32 * i + 8 * c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < KC; ++i) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    H::mma(s4, word(k0[i], 2 * e), word(k1[i], 2 * e), word(k0[i], 2 * e + 1),
+                           word(k1[i], 2 * e + 1), word(qv[i], 2 * e), word(qv[i], 2 * e + 1));
+                }
+            }
+        }
+        const int t0 = lb * BS;
+        const bool ok0 = t0 + g < ctx, ok1 = t0 + g + 8 < ctx;
+        const float x0 = ok0 ? s4[0] * a.scale_log2 : neg_inf();
+        const float x1 = ok0 ? s4[1] * a.scale_log2 : neg_inf();
+        const float x2 = ok1 ? s4[2] * a.scale_log2 : neg_inf();
+        const float x3 = ok1 ? s4[3] * a.scale_log2 : neg_inf();
+        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+        }
+        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+        if (mn0 != m0 || mn1 != m1) {
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            m0 = mn0;
+            m1 = mn1;
+        }
+        const float p0 = ex2(x0 - m0), p1 = ex2(x1 - m1);
+        const float p2 = ex2(x2 - m0), p3 = ex2(x3 - m1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        const uint32_t h01 = H::pack(p0, p1), h23 = H::pack(p2, p3);
+        const uint32_t pb0 = movmatrix_trans(h01), pb1 = movmatrix_trans(h23);
+        uint32_t pr0 = 0, pr1 = 0;
+        constexpr bool kSplit = sizeof(T) == 2 && !std::is_same<T, __half>::value;  // bf16 P: value + residual
+        if constexpr (kSplit) {
+            pr0 = movmatrix_trans(H::pack(p0 - __uint_as_float(h01 << 16), p1 - __uint_as_float(h01 & 0xffff0000u)));
+            pr1 = movmatrix_trans(H::pack(p2 - __uint_as_float(h23 << 16), p3 - __uint_as_float(h23 & 0xffff0000u)));
+        }
+        // PV: V rows 2c, 2c+1, 8+2c, 9+2c at the lane's columns (chunk j: the 8
+        // columns from pv_column(8 j, g)), rows past the context cleared
+        uint4 vv[4][VC];
+#pragma unroll
+        for (int j = 0; j < VC; ++j) {
+            const int col = pv_column<INT4 ? NG : 1, D>(8 * j, g);
+            vv[0][j] = ldg_stream(wv + (2 * c) * D + col);
+            vv[1][j] = ldg_stream(wv + (2 * c + 1) * D + col);
+            vv[2][j] = ldg_stream(wv + (8 + 2 * c) * D + col);
+            vv[3][j] = ldg_stream(wv + (9 + 2 * c) * D + col);
+            if (t0 + 2 * c >= ctx) vv[0][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 2 * c + 1 >= ctx) vv[1][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 8 + 2 * c >= ctx) vv[2][j] = make_uint4(0, 0, 0, 0);
+            if (t0 + 9 + 2 * c >= ctx) vv[3][j] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int el = INT4 ? pv_e<NG, MT>(mt, 0) : mt, eh = INT4 ? pv_e<NG, MT>(mt, 1) : mt + MT;
+            const int jl = el >> 3, wl = (el & 7) >> 1, jh = eh >> 3, wh = (eh & 7) >> 1;
+            const uint32_t sl = (el & 1) ? 0x7632u : 0x5410u, sh = (eh & 1) ? 0x7632u : 0x5410u;
+            const uint32_t a0 = __byte_perm(word(vv[0][jl], wl), word(vv[1][jl], wl), sl);
+            const uint32_t a1 = __byte_perm(word(vv[0][jh], wh), word(vv[1][jh], wh), sh);
+            const uint32_t a2 = __byte_perm(word(vv[2][jl], wl), word(vv[3][jl], wl), sl);
+            const uint32_t a3 = __byte_perm(word(vv[2][jh], wh), word(vv[3][jh], wh), sh);
+            H::mma(o[mt], a0, a1, a2, a3, pb0, pb1);
+            if constexpr (kSplit) H::mma(o[mt], a0, a1, a2, a3, pr0, pr1);
+        }
+    };
+
+    // blocks from win_lb0 on are read from the 16-bit window ring (WIN:
+    // kernels built for calls with a window; the others carry no such code)
+    const int win_lb0 = WIN ? max(ctx - a.window, 0) / BS : 0x7fffffff;
+
     // Lane j holds the physical id of the pass's j-th upcoming block (32 at
     // a time), so a block's loads never wait behind a table load.
     int tab = 0;
@@ -561,6 +697,12 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         if ((i & 31) == 0) {
             const int idx = lb + stride * lane;
             tab = idx < lb_end ? trow[idx] : -1;
+        }
+        if constexpr (WIN) {
+            if (lb >= win_lb0) {
+                attend16(lb);
+                continue;
+            }
         }
         const int phys = __shfl_sync(0xffffffffu, tab, i & 31);
         if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
@@ -589,6 +731,7 @@ __device__ __forceinline__ void quant_finish(QState<D / 16, NG>& st) {
             st.corr[gi][1] += __shfl_xor_sync(0xffffffffu, st.corr[gi][1], off);
         }
     }
+    if (st.true_units) return;  // converted before the first window block
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
         // INT4: back from the accumulator's units (both elements of an m-tile
@@ -616,7 +759,7 @@ __device__ __forceinline__ void out_columns(int mt, int g, int& dl, int& dh) {
 // Partition kernel: one CTA of NW warps per (partition, KV head, sequence);
 // the warps take the partition's blocks round-robin and merge through
 // shared memory.
-template <typename T, int D, int QMODE, int NG, bool SPLIT>
+template <typename T, int D, int QMODE, int NG, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_quant_kernel(QDecodeArgs a) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
@@ -639,7 +782,7 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_q
 
     __shared__ uint4 sq[NW][KSTEPS / 2][32];
     QState<MT, NG> st;
-    quant_pass<T, D, QMODE, NG>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
+    quant_pass<T, D, QMODE, NG, WIN>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
     quant_finish<D, QMODE, NG>(st);
     const float m0 = st.m0, m1 = st.m1, l0 = st.l0, l1 = st.l1;
     auto& o = st.o;
@@ -694,7 +837,7 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_q
 // Balanced split for the quantised cache (the split itself: balanced.cuh):
 // warp i walks its range run by run, one pass per run segment, and writes
 // the run's partial.  No barrier.
-template <typename T, int D, int QMODE, int NG>
+template <typename T, int D, int QMODE, int NG, bool WIN>
 __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     paged_decode_quant_balanced_kernel(QDecodeArgs a, int batch, int nwt_launch) {
     constexpr int KSTEPS = D / 16;
@@ -715,7 +858,7 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     if (!any) return;
     while (sp.next()) {
         QState<MT, NG> st;
-        quant_pass<T, D, QMODE, NG>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
+        quant_pass<T, D, QMODE, NG, WIN>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
         quant_finish<D, QMODE, NG>(st);
         // partial (m, l, o) of this run: o staged through shared memory so
         // the G x D rows go out in 16-byte stores
@@ -750,13 +893,16 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
 
 template <typename T, int D, int QMODE, int NG>
 void launch_balanced(const QDecodeArgs& a, int batch, int nwt, cudaStream_t st) {
-    paged_decode_quant_balanced_kernel<T, D, QMODE, NG><<<(nwt + NW - 1) / NW, NW * 32, 0, st>>>(a, batch, nwt);
+    const dim3 grid((nwt + NW - 1) / NW);
+    if (a.window > 0) paged_decode_quant_balanced_kernel<T, D, QMODE, NG, true><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
+    else paged_decode_quant_balanced_kernel<T, D, QMODE, NG, false><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
 }
 
 template <typename T, int D, int QMODE, int NG, bool SPLIT>
 void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
     dim3 grid(SPLIT ? parts : 1, hkv, batch);
-    paged_decode_quant_kernel<T, D, QMODE, NG, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+    if (a.window > 0) paged_decode_quant_kernel<T, D, QMODE, NG, true, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+    else paged_decode_quant_kernel<T, D, QMODE, NG, false, SPLIT><<<grid, NW * 32, 0, st>>>(a);
 }
 
 // The kernel for (dtype, head dim, mode, column groups); balanced or
@@ -793,12 +939,12 @@ int dispatch(const QDecodeArgs& a, int D, int qmode, int ng, int dtype, int part
 extern "C" int pkv_paged_attention_decode_quant(
     const void* q, const void* k_codes, const void* k_scale, const void* k_zero, const void* v_codes,
     const void* v_scale, const void* v_zero, const void* sink_k, const void* sink_v, int32_t n_sink,
-    const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+    const void* win_k, const void* win_v, int32_t window, const int32_t* block_tables, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
     int32_t max_blocks, int32_t group_size, float scale, void* out, void* workspace,
     size_t workspace_bytes, int32_t partition_size, int qmode, int dtype, void* stream) {
     if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
-        block_size <= 0 || max_blocks < 0 || partition_size < 0 || n_sink < 0)
+        block_size <= 0 || max_blocks < 0 || partition_size < 0 || n_sink < 0 || window < 0)
         return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_INVALID_ARG;
     if (qmode != PKV_QMODE_INT4_ASYM && qmode != PKV_QMODE_FP8_E4M3) return PKV_ERR_INVALID_ARG;
@@ -819,6 +965,9 @@ extern "C" int pkv_paged_attention_decode_quant(
         return PKV_ERR_INVALID_ARG;
     if (qmode == PKV_QMODE_INT4_ASYM && (!k_zero || !v_zero)) return PKV_ERR_INVALID_ARG;
     if (n_sink > 0 && (!sink_k || !sink_v)) return PKV_ERR_INVALID_ARG;
+    if (window % block_size != 0) return PKV_ERR_INVALID_ARG;
+    if (window > 0 && (!win_k || !win_v)) return PKV_ERR_INVALID_ARG;
+    if (window > 0 && (!pkv::aligned16(win_k) || !pkv::aligned16(win_v))) return PKV_ERR_MISALIGNED;
     if (!pkv::aligned16(q) || !pkv::aligned16(k_codes) || !pkv::aligned16(v_codes) ||
         !pkv::aligned16(out) || (reinterpret_cast<uintptr_t>(k_scale) & 1u) ||
         (reinterpret_cast<uintptr_t>(v_scale) & 1u))
@@ -836,6 +985,10 @@ extern "C" int pkv_paged_attention_decode_quant(
     a.sink_k = sink_k;
     a.sink_v = sink_v;
     a.n_sink = n_sink;
+    a.win_k = win_k;
+    a.win_v = win_v;
+    a.window = window;
+    a.ring = window / block_size + 1;
     a.tables = block_tables;
     a.ctx_lens = context_lens;
     a.hq = num_q_heads;

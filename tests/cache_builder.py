@@ -79,6 +79,11 @@ def build(pkv, w, device, quant=None, empty_fill=None, step_append=True):
         ns = max(n_sink, 1)
         c.cache["sink_k"] = torch.zeros((B, ns, Hkv, D), dtype=dt, device=device)
         c.cache["sink_v"] = torch.zeros((B, ns, Hkv, D), dtype=dt, device=device)
+        c.window = w.get("window", 0)
+        if c.window:
+            R = c.window // BS + 1
+            c.cache["win_k"] = torch.zeros((B, R, Hkv, BS, D), dtype=dt, device=device)
+            c.cache["win_v"] = torch.zeros((B, R, Hkv, BS, D), dtype=dt, device=device)
     row_of_handle = {h: i for i, h in enumerate(decoded)}
     rows = _rows_source(w)
     lens = {}
@@ -95,7 +100,8 @@ def build(pkv, w, device, quant=None, empty_fill=None, step_append=True):
         else:
             pos = torch.from_numpy(np.concatenate([p[3] for p in pending]).astype(np.int32)).to(device)
             sidx = torch.from_numpy(np.concatenate([p[4] for p in pending]).astype(np.int32)).to(device)
-            pkv.pkv_kv_append_quant(k, v, slots, pos, sidx, c.cache, n_sink, quant, c.group_size)
+            pkv.pkv_kv_append_quant(k, v, slots, pos, sidx, c.cache, n_sink, quant, c.group_size,
+                                    window=getattr(c, "window", 0))
         pending.clear()
 
     c.all_pairs = []
@@ -190,7 +196,8 @@ def expected(c, seq_ids=None):
             out.append(oatt.sequence_attention(q[i], k, v, c.w["scale"]))
         else:
             out.append(okv.sequence_attention_quant(q[i], k, v, c.w["scale"], c.n_sink, c.quant,
-                                                    getattr(c, "group_size", c.w["d"])))
+                                                    getattr(c, "group_size", c.w["d"]),
+                                                    window=getattr(c, "window", 0)))
     return np.stack(out)
 
 

@@ -156,7 +156,8 @@ def _decode_quant(pkv, c, lens=None):
     n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, 0)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device=c.q.device)
     pkv.pkv_paged_attention_decode_quant(c.q, c.cache, c.n_sink, c.tables, c.lens if lens is None else lens,
-                                         w["scale"], out, c.quant, c.group_size, ws, 0)
+                                         w["scale"], out, c.quant, c.group_size, ws, 0,
+                                         window=getattr(c, "window", 0))
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
@@ -204,3 +205,16 @@ def test_quant_int4_group64_many_short_sequences(pkv, cuda_dev):
     got = _decode_quant(pkv, c)
     assert pkv.pkv_device_status() == 0
     assert_close(got, expected(c), what="int4 g64, 640 short sequences")
+
+
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_quant_window_many_short_sequences(pkv, cuda_dev, qmode):
+    """640 sequences of 1..320 tokens with a 128-token 16-bit window: runs
+    start and end inside warp ranges, and the window blocks of a run may be
+    split between warps."""
+    w = _short_quant_workload(group_size=64 if qmode == "int4" else 128, n_sink=8, window=128)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    assert _is_balanced(c)
+    got = _decode_quant(pkv, c)
+    assert pkv.pkv_device_status() == 0
+    assert_close(got, expected(c), what="%s window, 640 short sequences" % qmode)

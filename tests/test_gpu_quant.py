@@ -84,7 +84,8 @@ def _decode_quant(pkv, c, partition_size=0):
     n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, partition_size)
     ws = torch.empty(max(n, 16), dtype=torch.uint8, device=c.q.device)
     pkv.pkv_paged_attention_decode_quant(c.q, c.cache, c.n_sink, c.tables, c.lens, w["scale"], out,
-                                         c.quant, c.group_size, ws, partition_size)
+                                         c.quant, c.group_size, ws, partition_size,
+                                         window=getattr(c, "window", 0))
     torch.cuda.synchronize()
     assert pkv.pkv_device_status() == 0
     return out.float().cpu().numpy()
@@ -186,3 +187,42 @@ def test_int4_group_size_checks(pkv, cuda_dev):
     c = build(pkv, w, cuda_dev, quant="int4")
     with pytest.raises(pkv.PkvError):
         _decode_quant(pkv, c, 0)
+
+
+# The pages' full layout: INT4 groups of 64, 8 sinks, and the last 128
+# tokens kept in 16-bit (a per-sequence window ring).
+
+@pytest.mark.parametrize("ctx", [1, 100, 128, 129, 143, 144, 145, 161, 500])
+@pytest.mark.parametrize("qmode", ["int4", "fp8"])
+def test_window_boundaries(pkv, cuda_dev, qmode, ctx):
+    w = syn.workload("quant", batch=3, ctx=ctx, num_blocks=256, group_size=64 if qmode == "int4" else 128,
+                     n_sink=8, window=128)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    want = expected(c)
+    for ps in (0, 16, 64):
+        assert_close(_decode_quant(pkv, c, ps), want, what="%s window ctx %d ps %d" % (qmode, ctx, ps))
+
+
+def test_window_ring_holds_the_last_tokens(pkv, cuda_dev):
+    """Every token of every sequence passed through its ring: the ring's
+    blocks from the window start on equal the 16-bit rows."""
+    w = syn.workload("quant", batch=2, ctx=300, num_blocks=128, group_size=64, n_sink=8, window=128)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    R = 128 // 16 + 1
+    for i in range(2):
+        k, v = logical_rows(c, i)
+        L = k.shape[0]
+        ws = max(L - 128, 0) // 16 * 16
+        wk = c.cache["win_k"][i].float().cpu().numpy()
+        for t in range(ws, L):
+            np.testing.assert_array_equal(wk[(t // 16) % R, :, t % 16], k[t])
+
+
+def test_pages_layout_full_size_sampled(pkv, cuda_dev):
+    """32 x 16,384 tokens in the pages' BIE layout (INT4 g = 64, 8 sinks,
+    128-token 16-bit window): sampled outputs within the bound."""
+    w = syn.workload("quant", group_size=64, n_sink=8, window=128)
+    c = build(pkv, w, cuda_dev, quant="int4")
+    got = _decode_quant(pkv, c, 0)
+    sample = [0, 9, 31]
+    assert_close(got[sample], expected(c, sample), what="BIE layout full size")
