@@ -56,9 +56,29 @@ TRAFFIC = {
                   [_CSRC + "decode_quant.cu", _CSRC + "common.cuh", _CSRC + "balanced.cuh"]),
 }
 
-# name -> (synthetic workload, overrides, cache mode)
+
+
+def _slab_overrides(syn):
+    """The 64-sequence layer as one contiguous slab per (sequence, KV head):
+    each of the 64 x 8 (sequence, KV head) pairs becomes a sequence with one
+    KV head and its GQA group of 4 query heads, whose blocks are allocated in
+    ascending order, so its K (and V) rows are one contiguous run -- the
+    layout of an unpaged [sequence, head, token, dim] cache, read by the same
+    kernel at the same bytes."""
+    base = syn.workload("llama3_8b_b64")
+    lens = syn.context_lengths(base)
+    return {"lens": [L for L in lens for _ in range(base["hkv"])], "hq": base["hq"] // base["hkv"],
+            "hkv": 1, "in_order": True, "num_blocks": base["num_blocks"] * base["hkv"]}
+
+
+# name -> (synthetic workload, overrides (or a function of the synthetic
+# module returning them), cache mode)
 WORKLOADS = {
     "llama3_8b_b64": ("llama3_8b_b64", {}, None),
+    "llama3_8b_b64_bs8": ("llama3_8b_b64", {"block_size": 8, "num_blocks": 80000}, None),
+    "llama3_8b_b64_bs32": ("llama3_8b_b64", {"block_size": 32, "num_blocks": 20000}, None),
+    "llama3_8b_b64_in_order": ("llama3_8b_b64", {"in_order": True}, None),
+    "llama3_8b_b64_slab": ("llama3_8b_b64", _slab_overrides, None),
     "long_splitk": ("long_splitk", {}, None),
     "quant_int4": ("quant", {}, "int4"),
     "quant_fp8": ("quant", {}, "fp8"),
@@ -69,6 +89,10 @@ WORKLOADS = {
     "prefill_chunk512": ("llama3_8b_b64", {"lens": [4096] * 8, "num_blocks": 4096}, None),
 }
 
+# decoded rows per model sequence (the slab layout decodes each KV head's
+# group as its own row)
+ROWS_PER_SEQ = {"llama3_8b_b64_slab": 8}
+
 # multi-query workloads: query tokens per sequence (the last ones of its context)
 MQ_LEN = {"verify_b64_g5": 6, "prefill_chunk512": 512}
 
@@ -76,6 +100,18 @@ DESCRIPTIONS = {
     "llama3_8b_b64": "one Llama-3-8B-shaped layer, 64 sequences, context uniform in [512, 4096] "
                      "(seeded), 32 q / 8 KV heads, head dim 128, bf16, 16-token blocks, "
                      "40,000-block pool in seeded random order",
+    "llama3_8b_b64_bs8": "the 64-sequence Llama-3-8B-shaped layer (contexts uniform in [512, 4096], "
+                         "32 q / 8 KV heads, head dim 128, bf16) in 8-token blocks: 80,000-block "
+                         "pool in seeded random order (same bytes as the 16-token pool)",
+    "llama3_8b_b64_bs32": "the 64-sequence Llama-3-8B-shaped layer in 32-token blocks: 20,000-block "
+                          "pool in seeded random order (same bytes as the 16-token pool)",
+    "llama3_8b_b64_in_order": "the 64-sequence Llama-3-8B-shaped layer in 16-token blocks allocated "
+                              "in ascending order: each sequence's prompt blocks are consecutive "
+                              "(paged layout, unscattered)",
+    "llama3_8b_b64_slab": "the 64-sequence Llama-3-8B-shaped layer as 512 contiguous (sequence, KV "
+                          "head) slabs: each pair is a 1-KV-head sequence with its 4 query heads "
+                          "and consecutive blocks, i.e. the unpaged [sequence, head, token, dim] "
+                          "layout, read by the same kernel at the same bytes",
     "long_splitk": "4 sequences of 65,536 / 32,768 / 32,768 / 32,768 tokens, blocks allocated "
                    "round-robin across the sequences from a shuffled 12,288-block pool, 32 q / 8 "
                    "KV heads, head dim 128, bf16",
@@ -246,7 +282,7 @@ class Cache:
     def __init__(self, pkv, torch, device, name, partition_size, headroom_tokens, pool_blocks=0):
         import synthetic as syn
         base, over, qmode = WORKLOADS[name]
-        over = dict(over)
+        over = dict(over(syn) if callable(over) else over)
         if pool_blocks:
             over["num_blocks"] = pool_blocks
         w = syn.workload(base, **over)
@@ -346,13 +382,13 @@ class Cache:
         # 0 = the library's automatic split: balanced over the GPU's warps for
         # the 16-bit cache, automatic partitions for the quantised one
         self.partition_size = partition_size
-        auto_ps = pkv.pkv_decode_auto_partition_size(B, Hq, self.max_blocks)
+        auto_ps = pkv.pkv_decode_auto_partition_size(B, Hq, self.max_blocks, BS)
         self.split = self.max_blocks * BS > (partition_size or auto_ps)
         if not self.split:
             self.split_desc = "single pass (one partition covers every context)"
         elif partition_size == 0 and qmode is None and B <= 1024:
             self.split_desc = ("balanced split-K: every warp of 4 resident 4-warp CTAs per SM "
-                               "streams an equal share of the (sequence, KV head, block) items")
+                               "streams an equal share of the (sequence, KV head, 16-token unit) items")
         else:
             self.split_desc = "%d-token split-K partitions" % (partition_size or auto_ps)
         ws = pkv.pkv_decode_workspace_bytes(B, Hq, D, self.max_blocks, BS, self.partition_size)
@@ -733,7 +769,7 @@ def oracle_sample(name, S):
     import synthetic as syn
     from oracle import allocator, attention, kvcache
     base, over, qmode = WORKLOADS[name]
-    w = syn.workload(base, **over)
+    w = syn.workload(base, **(over(syn) if callable(over) else over))
     S = min(S, len(syn.context_lengths(w)))
     q = syn.kv_rows_to_numpy(syn.query(w))[:S]
     ks, vs = [], []
@@ -741,8 +777,9 @@ def oracle_sample(name, S):
         k, v = syn.sequence_kv(w, i)
         ks.append(syn.kv_rows_to_numpy(k))
         vs.append(syn.kv_rows_to_numpy(v))
-    nb = sum(-(-k.shape[0] // 16) for k in ks)
-    m = allocator.KVCacheManager(nb, 16, syn.free_order(dict(w, num_blocks=nb)))
+    bs = w["block_size"] if qmode is None else 16
+    nb = sum(-(-k.shape[0] // bs) for k in ks)
+    m = allocator.KVCacheManager(nb, bs, syn.free_order(dict(w, num_blocks=nb)))
     Hkv, D = w["hkv"], w["d"]
     sids, all_slots = [], []
     for i in range(S):
@@ -752,13 +789,13 @@ def oracle_sample(name, S):
         all_slots.append(slots)
     tables, ctx = m.block_tables(sids, max(len(m.table(s)) for s in sids))
     if qmode is None:
-        kp = np.zeros((nb, Hkv, 16, D), np.float32)
+        kp = np.zeros((nb, Hkv, bs, D), np.float32)
         vp = np.zeros_like(kp)
         for i in range(S):
-            kvcache.kv_append(ks[i], vs[i], all_slots[i], kp, vp)
+            kvcache.kv_append(ks[i], vs[i], all_slots[i], kp, vp, block_size=bs)
 
         def decode():
-            attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"])
+            attention.paged_attention_decode(q, kp, vp, tables, ctx, w["scale"], block_size=bs)
         kvb = int(np.sum(ctx)) * 2 * Hkv * D * 2
     else:
         ns = w["n_sink"]
@@ -821,7 +858,8 @@ def cpu_worker(name, min_seconds, S):
                       "sample_seqs": S, "sample_tokens": toks}))
 
 
-CPU_SAMPLE_SEQS = {"llama3_8b_b64": 16, "long_splitk": 1, "quant_int4": 1, "quant_fp8": 1,
+CPU_SAMPLE_SEQS = {"llama3_8b_b64": 16, "llama3_8b_b64_bs8": 16, "llama3_8b_b64_bs32": 16,
+                   "llama3_8b_b64_in_order": 16, "llama3_8b_b64_slab": 128, "long_splitk": 1, "quant_int4": 1, "quant_fp8": 1,
                    "quant_int4_g64": 1, "quant_int4_bie": 1, "prefix_cow": 8}
 
 
@@ -838,7 +876,7 @@ def cpu_baseline(name, min_seconds):
         "cores": 1,
         "kind": "oracle",
         "sample": "float64 NumPy oracle paged decode of %d sequence(s) of the workload (%d tokens, "
-                  "all 32 query heads), repeated %d times in %.1f s, single thread"
+                  "all query heads), repeated %d times in %.1f s, single thread"
                   % (res["sample_seqs"], res["sample_tokens"], res["reps"], res["seconds"]),
         "seq_per_s": res["seqs"] / res["seconds"],
     }
@@ -912,7 +950,8 @@ def main():
         "data": "synthetic",
         "config": config_block(args.workload, res["B"], res["kv_bytes"], res["partition_size"],
                                res["split_desc"]),
-        "seq_per_s_per_layer": round(res["B"] * world / (res["ms_per_step"] * 1e-3), 1),
+        "seq_per_s_per_layer": round(res["B"] / ROWS_PER_SEQ.get(args.workload, 1) * world
+                                     / (res["ms_per_step"] * 1e-3), 1),
         "pct_of_8tbs_nominal": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100.0 * value / world / peak, 2),
         "roofline": {
@@ -980,7 +1019,7 @@ def run_reference(args, world):
                                "the oracle has no split: plain softmax per (sequence, query head)"),
         "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
                          "sample": "float64 NumPy oracle paged decode of %d sequence(s) of the "
-                                   "workload (%d tokens, all 32 query heads) per step" % (S, toks)},
+                                   "workload (%d tokens, all query heads) per step" % (S, toks)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))

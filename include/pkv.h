@@ -212,19 +212,20 @@ int pkv_prefix_stats(const pkv_pool* pool, int64_t* entries, int64_t* lookups, i
 
 /* Bytes of the split-K workspace pkv_paged_attention_decode* needs for this
  * shape.  Zero when a single partition covers max_blocks * block_size
- * (single-pass decode).
- *   - partition_size > 0 (a positive multiple of block_size): fixed
- *     partitions, fp32 partial outputs [batch, num_q_heads, P, head_dim] and
- *     fp32 (max, sum) pairs [batch, num_q_heads, P, 2], P = ceil(max_blocks *
- *     block_size / partition_size).
+ * (single-pass decode).  U = ceil(max_blocks * block_size / 16), the
+ * tables' capacity in 16-token units (the kernels' token tile).
+ *   - partition_size > 0 (a positive multiple of 16 and of block_size):
+ *     fixed partitions, fp32 partial outputs [batch, num_q_heads, P,
+ *     head_dim] and fp32 (max, sum) pairs [batch, num_q_heads, P, 2],
+ *     P = ceil(max_blocks * block_size / partition_size).
  *   - partition_size 0 (automatic): the same for the automatic partition
  *     size (pkv_decode_auto_partition_size), or, when the automatic split
- *     may be balanced (batch <= 1024 and batch * num_q_heads * max_blocks >=
+ *     may be balanced (batch <= 1024 and batch * num_q_heads * U >=
  *     32 * 16 * SMs), the larger of that and the balanced split's need:
  *     (nwt * 8 + batch * num_q_heads) * (head_dim + 2) * 4 bytes,
- *     nwt = min(20 * SMs, batch * num_q_heads * max_blocks / 2), the most
- *     warps a balanced kernel launches (SMs of the current device, 152 if
- *     none). */
+ *     nwt = min(20 * SMs, batch * num_q_heads * U / 2), the most warps a
+ *     balanced kernel launches (SMs of the current device, 152 if none).
+ * max_blocks * block_size above 2^30 is UNSUPPORTED. */
 int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_dim,
                                int32_t max_blocks, int32_t block_size, int32_t partition_size,
                                size_t* out);
@@ -235,7 +236,7 @@ int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t head_
  * 256, 128, 64 tokens for which batch * num_q_heads * ceil(max_blocks *
  * block_size / size) >= 12 * (SM count of the current device, 152 if none),
  * else 64.  Small batches get finer splits so the GPU has enough partition
- * CTAs. */
+ * CTAs.  block_size 8, 16 or 32 (else UNSUPPORTED). */
 int pkv_decode_auto_partition_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                                    int32_t block_size, int32_t* out);
 
@@ -261,16 +262,21 @@ int pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int
  * launched behind the first with programmatic dependent launch, merges them
  * with a log-sum-exp rescale (flash-decoding split-K); otherwise one pass
  * writes out directly.
- *   - partition_size > 0: the context is cut into partitions of that many
+ *   - partition_size > 0 (a multiple of 16 and of block_size, else
+ *     INVALID_ARG): the context is cut into partitions of that many
  *     tokens, one CTA each.
  *   - partition_size 0 (automatic): if batch <= 1024 and batch *
- *     num_kv_heads * max_blocks is at least 32 items per launched warp
- *     (16 warps per SM) and below 2^30, a balanced split: the (sequence, KV
- *     head, block) items of the call, in that order, are cut into one
- *     contiguous, equal share per warp, whatever the mix of context
- *     lengths; else partitions of pkv_decode_auto_partition_size tokens.
+ *     num_kv_heads * U (U = ceil(max_blocks * block_size / 16)) is at least
+ *     32 items per launched warp (16 warps per SM) and below 2^30, a
+ *     balanced split: the (sequence, KV head, 16-token unit) items of the
+ *     call, in that order, are cut into one contiguous, equal share per
+ *     warp, whatever the mix of context lengths; else partitions of
+ *     pkv_decode_auto_partition_size tokens.
+ * The kernels' token tile is 16 tokens: one block at block_size 16, half a
+ * block at 32, two blocks at 8 (both table entries of a tile are checked;
+ * a bad one skips the whole 16-token tile and sets PKV_STATUS_BAD_BLOCK).
  * Calls that share a workspace must not overlap on the GPU.
- * Supported: block_size 16, head_dim 64 or 128, 1 <= num_q_heads /
+ * Supported: block_size 8, 16 or 32, head_dim 64 or 128, 1 <= num_q_heads /
  * num_kv_heads <= 8 (else UNSUPPORTED). */
 int pkv_paged_attention_decode(const void* q, const void* k_pool, const void* v_pool,
                                const int32_t* block_tables, const int32_t* context_lens,

@@ -2,12 +2,13 @@
 // the quantised decode kernels.
 //
 // The work of one decode call is the ordered list of (sequence, KV head,
-// logical block) items -- sequence-major, then KV head, then block --
-// W = Hkv * sum_b nblk_b items.  Warp i of nwt = min(launched warps,
-// W / min_items) takes the contiguous range [i W / nwt, (i + 1) W / nwt), so
-// every warp streams the same number of blocks whatever the mix of context
-// lengths: no wave quantisation, no short last partitions, one prologue per
-// warp.  A range falls into runs of one (sequence, KV head); a warp writes
+// 16-token unit) items -- sequence-major, then KV head, then unit --
+// W = Hkv * sum_b ceil(ctx_b / 16) items (a unit is one block at the
+// default block size of 16, half a 32-token block, or two 8-token blocks).
+// Warp i of nwt = min(launched warps, W / min_items) takes the contiguous
+// range [i W / nwt, (i + 1) W / nwt), so every warp streams the same number
+// of units whatever the mix of context lengths: no wave quantisation, no
+// short last partitions, one prologue per warp.  A range falls into runs of one (sequence, KV head); a warp writes
 // one fp32 partial (m, l, o) per run it touches, at slot i + b * Hkv + kvh
 // (rows slot * G + h of the partial arrays): the warps touching one run are
 // consecutive and every range is non-empty, so slots never collide, and
@@ -18,12 +19,12 @@
 
 namespace pkv {
 
-constexpr int kSplitBS = 16;  // tokens per block
+constexpr int kSplitBS = 16;  // tokens per item (the kernels' token tile)
 
 // Batches up to this size may use the balanced split (every warp scans the
 // context lengths once).
 constexpr int kBalancedMaxBatch = 1024;
-// Fewest (sequence, KV head, block) items a warp of the balanced split takes.
+// Fewest (sequence, KV head, unit) items a warp of the balanced split takes.
 constexpr int kBalancedMinItems = 2;
 // The automatic split is balanced when the tables could hold this many items
 // per launched warp: below it fixed partitions measured as fast or faster
@@ -40,13 +41,15 @@ int balanced_warps(int64_t max_items, int warps_per_sm);
 constexpr int kBalancedMaxWarpsPerSm = 20;
 // Whether an automatic split may be balanced for at most max_items items.
 bool balanced_candidate(int64_t batch, int64_t max_items);
-// Whether an automatic split over these tables is balanced.
-bool use_balanced(int64_t batch, int64_t hkv, int64_t max_blocks);
+// Whether an automatic split over tables of max_units 16-token units is
+// balanced.
+bool use_balanced(int64_t batch, int64_t hkv, int64_t max_units);
 // Workspace bytes of a balanced split: nwt * G + batch * hq partial rows.
 size_t balanced_bytes(int32_t batch, int32_t hq, int32_t G, int32_t D, int32_t nwt);
 // The merge of a balanced split (decode.cu), launched behind the split
-// kernel with programmatic dependent launch; out has the 16-bit dtype.
-int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int max_blocks,
+// kernel with programmatic dependent launch; out has the 16-bit dtype.  cap:
+// the tables' capacity in tokens (max_blocks * block_size).
+int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int cap,
                           int nwt, const float* ws_o, const float* ws_ml, void* out, int dtype,
                           cudaStream_t st);
 
@@ -62,23 +65,24 @@ __device__ __forceinline__ int64_t first_warp(int64_t x, int64_t W, int64_t nwt)
 }
 
 // One warp's range, walked run by run.  The host keeps
-// batch * Hkv * max_blocks below 2^30, so item indices fit in int.
+// batch * Hkv * (units per table) below 2^30, so item indices fit in int.
 struct WarpSplit {
     const int32_t* ctx_lens;
     int cap, hkv;
     int pos, E;    // remaining items [pos, E)
-    int b, nb, cs; // current sequence, its block count, its first item
-    // current run segment: sequence b, KV head kvh, blocks [lb0, lb1)
+    int b, nb, cs; // current sequence, its unit count, its first item
+    // current run segment: sequence b, KV head kvh, units [lb0, lb1)
     int ctx, kvh, lb0, lb1;
 
     // Sets up warp i's range; false when it has none.  Every lane of the warp
-    // calls it (warp-collective).  bad: some context length was outside
-    // [0, max_blocks * 16].
-    __device__ __forceinline__ bool begin(const int32_t* lens, int batch, int max_blocks, int hkv_,
+    // calls it (warp-collective).  cap_tokens: the tables' capacity
+    // (max_blocks * block_size); bad: some context length was outside
+    // [0, cap_tokens].
+    __device__ __forceinline__ bool begin(const int32_t* lens, int batch, int cap_tokens, int hkv_,
                                           int nwt_launch, int min_items, int i, bool& bad) {
         const int lane = threadIdx.x & 31;
         ctx_lens = lens;
-        cap = max_blocks * kSplitBS;
+        cap = cap_tokens;
         hkv = hkv_;
         int mine = 0;
         bad = false;

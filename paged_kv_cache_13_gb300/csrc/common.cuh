@@ -15,8 +15,9 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 // Device address of this device's status word (host side, status.cu).
 int* status_word();
 
-// Partition size chosen when a decode call passes partition_size 0 (decode.cu).
-int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks);
+// Partition size chosen when a decode call passes partition_size 0 (decode.cu);
+// tokens: the tables' capacity, max_blocks * block_size.
+int auto_partition_size(int32_t batch, int32_t hq, int64_t tokens);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

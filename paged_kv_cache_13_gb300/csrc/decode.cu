@@ -22,8 +22,11 @@
 // * Each warp loads the physical ids of all its blocks with one coalesced
 //   load (lane k holds the id of the warp's k-th block), so a block's K/V
 //   loads never wait behind a table load.
-// * A block of one KV head is 16 tokens x D contiguous 16-bit values (4 KiB
-//   for D = 128).  Each lane issues 16-byte loads straight from global memory
+// * The token tile is a 16-token unit.  At the default block size of 16 a
+//   unit is one block; at 32 it is half a block; at 8 it is two blocks, so
+//   its rows 0-7 and 8-15 come from two table entries.  Either way a unit's
+//   rows of one KV head are two runs of 8 x D contiguous 16-bit values (one
+//   16 x D run, 4 KiB for D = 128, at block sizes 16 and 32).  Each lane issues 16-byte loads straight from global memory
 //   into registers, shaped so that the registers ARE the tensor-core fragments
 //   (no shared-memory staging, no shuffles of K or V):
 //     QK^T : S^T[16 tok x 8 heads] = K[16 x D] . Q^T[D x 8]   (mma m16n8k16,
@@ -53,7 +56,7 @@
 namespace pkv {
 namespace {
 
-constexpr int BS = 16;  // tokens per block (the kernels are specialised to 16)
+constexpr int kUnit = 16;  // tokens per unit: the kernels' token tile (block sizes 8, 16, 32)
 constexpr int kNW = 4;  // warps per CTA (4 beat 8 in a sweep on the 64-sequence layer)
 constexpr float kLog2e = 1.4426950408889634f;
 // Headroom (log2 units) a logit may rise above the running reference max
@@ -74,6 +77,7 @@ struct DecodeArgs {
     const int32_t* tables;
     const int32_t* ctx_lens;
     int hq, hkv, G, num_blocks, max_blocks, part_blocks, max_parts;
+    int cap;  // table capacity in tokens: max_blocks * block_size
     float scale_log2;
     void* out;
     float* ws_o;   // [B, Hq, max_parts, D]
@@ -184,29 +188,72 @@ __device__ __forceinline__ uint32_t stage_query(const DecodeArgs& a, int b, int 
     return static_cast<uint32_t>(__cvta_generic_to_shared(slot));
 }
 
-// Attend one 16-token block (physical id `phys`, logical index lb) into the
-// warp state.  INJECT: row app_off of the block is the decode step's new row;
-// it is taken from the inputs (and stored to the pool) instead of the loads.
+// Table entries of 16-token unit u of a sequence at block size BS: entry u
+// (BS 16); entry u / 2, from its row 16 (u % 2) (BS 32); entries 2u and
+// 2u + 1 (BS 8), the second only while it holds context tokens (nent:
+// entries the context covers) -- past it the first stands in, its rows
+// being masked.
+template <int BS>
+struct UnitIds {
+    int e0, e1;
+    __device__ __forceinline__ void load(const int32_t* trow, int u, bool in, int nent) {
+        e0 = e1 = 0;
+        if (!in) return;
+        if constexpr (BS == 8) {
+            e0 = trow[2 * u];
+            e1 = 2 * u + 1 < nent ? trow[2 * u + 1] : e0;
+        } else {
+            e0 = trow[u * kUnit / BS];
+        }
+    }
+    // lane src's entries
+    __device__ __forceinline__ UnitIds shfl(int src) const {
+        UnitIds r;
+        r.e0 = __shfl_sync(0xffffffffu, e0, src);
+        r.e1 = BS == 8 ? __shfl_sync(0xffffffffu, e1, src) : 0;
+        return r;
+    }
+    __device__ __forceinline__ bool valid(int num_blocks) const {
+        return static_cast<unsigned>(e0) < static_cast<unsigned>(num_blocks) &&
+               (BS != 8 || static_cast<unsigned>(e1) < static_cast<unsigned>(num_blocks));
+    }
+    // Element offsets, within a pool, of the unit's rows 0-7 (lo) and 8-15
+    // (hi) of KV head kvh.
+    template <int D>
+    __device__ __forceinline__ void bases(int hkv, int kvh, int u, int64_t& lo, int64_t& hi) const {
+        lo = (static_cast<int64_t>(e0) * hkv + kvh) * (BS * D);
+        if constexpr (BS == 32) lo += (u & 1) * (kUnit * D);
+        if constexpr (BS == 8) {
+            hi = (static_cast<int64_t>(e1) * hkv + kvh) * (BS * D);
+        } else {
+            hi = lo + 8 * D;
+        }
+    }
+};
+
+// Attend one 16-token unit (logical index lb; rows 0-7 at pool offset lo,
+// rows 8-15 at hi) into the warp state.  INJECT: row app_off of the unit is
+// the decode step's new row; it is taken from the inputs (and stored to the
+// pool) instead of the loads.
 template <typename T, int D, bool INJECT, typename QS>
-__device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh, int lb, int phys,
-                                             int ctx, int app_off, const QS& qs,
+__device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh, int lb, int64_t lo,
+                                             int64_t hi, int ctx, int app_off, const QS& qs,
                                              WarpState<D / 16>& w, int g, int c) {
     using H = Half16<T>;
     constexpr int KC = D / 32;
     constexpr int VC = D / 64;
     constexpr int MT = D / 16;
     const int vrow0 = 2 * c, vrow1 = 2 * c + 1, vrow2 = 8 + 2 * c, vrow3 = 9 + 2 * c;
-    const int64_t base = (static_cast<int64_t>(phys) * a.hkv + kvh) * (BS * D);
-    const T* kb = static_cast<const T*>(a.k_pool) + base;
-    const T* vb = static_cast<const T*>(a.v_pool) + base;
+    const T* kp = static_cast<const T*>(a.k_pool);
+    const T* vpl = static_cast<const T*>(a.v_pool);
     // Row sources: the pool, except that with INJECT the lanes holding row
     // app_off read the decode step's new row from the inputs instead.
-    const T* kr0p = kb + g * D;
-    const T* kr1p = kb + (g + 8) * D;
-    const T* vp0 = vb + vrow0 * D;
-    const T* vp1 = vb + vrow1 * D;
-    const T* vp2 = vb + vrow2 * D;
-    const T* vp3 = vb + vrow3 * D;
+    const T* kr0p = kp + lo + g * D;
+    const T* kr1p = kp + hi + g * D;
+    const T* vp0 = vpl + lo + vrow0 * D;
+    const T* vp1 = vpl + lo + vrow1 * D;
+    const T* vp2 = vpl + hi + (vrow2 - 8) * D;
+    const T* vp3 = vpl + hi + (vrow3 - 8) * D;
     if constexpr (INJECT) {
         const int64_t nrow = (static_cast<int64_t>(b) * a.hkv + kvh) * D;
         const T* kn = static_cast<const T*>(a.k_new) + nrow;
@@ -236,8 +283,9 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
     if constexpr (INJECT) {
         // Store the new row to the pool from the lanes that hold its pieces
         // (each 16-byte piece exactly once).
-        T* kw = static_cast<T*>(a.k_pool_w) + base + app_off * D;
-        T* vw = static_cast<T*>(a.v_pool_w) + base + app_off * D;
+        const int64_t row = app_off < 8 ? lo + app_off * D : hi + (app_off - 8) * D;
+        T* kw = static_cast<T*>(a.k_pool_w) + row;
+        T* vw = static_cast<T*>(a.v_pool_w) + row;
 #pragma unroll
         for (int i = 0; i < KC; ++i) {
             if (g == app_off) *reinterpret_cast<uint4*>(kw + 32 * i + 8 * c) = kr0[i];
@@ -263,7 +311,7 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
                    word(kr1[i], 2 * e + 1), word(qf, 2 * e), word(qf, 2 * e + 1));
         }
     }
-    const int tok0 = lb * BS + g;
+    const int tok0 = lb * kUnit + g;
     const bool ok0 = tok0 < ctx, ok1 = tok0 + 8 < ctx;
     const float x0 = ok0 ? s[0] * a.scale_log2 : neg_inf();
     const float x1 = ok0 ? s[1] * a.scale_log2 : neg_inf();
@@ -314,8 +362,8 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
         pr1 = movmatrix_trans(H::pack(p2 - lo_float(h23), p3 - hi_float(h23)));
     }
 
-    if (lb * BS + BS > ctx) {  // last, partial block: zero masked V rows
-        const int t0 = lb * BS;
+    if (lb * kUnit + kUnit > ctx) {  // last, partial unit: zero masked V rows
+        const int t0 = lb * kUnit;
 #pragma unroll
         for (int j = 0; j < VC; ++j) {
             if (t0 + vrow0 >= ctx) vr[0][j] = make_uint4(0, 0, 0, 0);
@@ -341,6 +389,25 @@ __device__ __forceinline__ void attend_block(const DecodeArgs& a, int b, int kvh
         H::mma(w.o[mt], a0, a1, a2, a3, pb0, pb1);
         if constexpr (kSplitP<T>) H::mma(w.o[mt], a0, a1, a2, a3, pr0, pr1);
     }
+}
+
+// The fused append's unit: its table entry holding the new row was checked
+// against the slot, but at block size 8 the unit's other entry was not, so
+// the entries are checked again here (a bad one skips the unit, store
+// included, and flags the status).
+template <typename T, int D, int BS, typename QS>
+__device__ __forceinline__ void attend_appended(const DecodeArgs& a, int b, int kvh, int lb,
+                                                const int32_t* trow, int nent, int ctx, int app_off,
+                                                const QS& qs, WarpState<D / 16>& w, int g, int c) {
+    UnitIds<BS> e;
+    e.load(trow, lb, true, nent);
+    if (!e.valid(a.num_blocks)) {
+        if ((threadIdx.x & 31) == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+        return;
+    }
+    int64_t lo, hi;
+    e.template bases<D>(a.hkv, kvh, lb, lo, hi);
+    attend_block<T, D, true>(a, b, kvh, lb, lo, hi, ctx, app_off, qs, w, g, c);
 }
 
 // Merge the NW warps' online-softmax states of one CTA through shared memory
@@ -393,7 +460,7 @@ __device__ __forceinline__ void cta_merge(const WarpState<D / 16>& ws, int warp,
     __syncthreads();
 }
 
-template <typename T, int D, int NW, int MODE, bool APPEND>
+template <typename T, int D, int NW, int MODE, bool APPEND, int BS>
 __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeArgs a) {
     using H = Half16<T>;
     constexpr int KC = D / 32;  // 16-byte K pieces per lane per row
@@ -404,12 +471,13 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
     const int g = lane >> 2, c = lane & 3;
 
     int ctx = a.ctx_lens[b];
-    const int cap = a.max_blocks * BS;
+    const int cap = a.cap;
     if (ctx < 0 || ctx > cap) {
         if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
         ctx = ctx < 0 ? 0 : cap;
     }
-    const int nblk = (ctx + BS - 1) / BS;
+    const int nblk = (ctx + kUnit - 1) / kUnit;  // units
+    const int nent = (ctx + BS - 1) / BS;        // table entries
     const int nparts = MODE == kSingle ? 1 : max((nblk + a.part_blocks - 1) / a.part_blocks, 1);
     if constexpr (MODE == kPartials) {
         // let the merge grid (launched with programmatic serialization) be
@@ -426,13 +494,13 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
     if constexpr (APPEND) {
         const int64_t slot = ctx > 0 ? a.slots[b] : -1;
         if (slot >= 0) {
-            const int lb_last = (ctx - 1) / BS, off = (ctx - 1) % BS;
+            const int lb_last = (ctx - 1) / kUnit;
             if (lb_last >= blk_begin && lb_last < blk_end) {
-                const int phys = trow[lb_last];
+                const int phys = trow[(ctx - 1) / BS], off = (ctx - 1) % BS;
                 if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks) &&
                     slot == static_cast<int64_t>(phys) * BS + off) {
                     app_lb = lb_last;
-                    app_off = off;
+                    app_off = (ctx - 1) % kUnit;
                 } else if (threadIdx.x == 0) {
                     atomicOr(a.status, PKV_STATUS_BAD_SLOT);
                 }
@@ -450,26 +518,28 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) ws.o[mt][0] = ws.o[mt][1] = ws.o[mt][2] = ws.o[mt][3] = 0.f;
 
-    // The appended block, if any, is the last block of this partition and so
-    // the last one its warp visits: the loop stops there and the block is
+    // The appended unit, if any, is the last unit of this partition and so
+    // the last one its warp visits: the loop stops there and the unit is
     // attended after the loop with the injection.
-    int tab = 0, k = 0, lb = blk_begin + warp;
+    UnitIds<BS> tab;
+    tab.e0 = tab.e1 = 0;
+    int k = 0, lb = blk_begin + warp;
     for (; lb < blk_end && lb != app_lb; ++k, lb += NW) {
-        if ((k & 31) == 0) {  // physical ids of this warp's next 32 blocks
+        if ((k & 31) == 0) {  // table entries of this warp's next 32 units
             const int idx = lb + NW * lane;
-            tab = idx < blk_end ? trow[idx] : 0;
+            tab.load(trow, idx, idx < blk_end, nent);
         }
-        const int phys = __shfl_sync(0xffffffffu, tab, k & 31);
-        if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+        const UnitIds<BS> e = tab.shfl(k & 31);
+        if (!e.valid(a.num_blocks)) {
             if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
             continue;
         }
-        attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qs, ws, g, c);
+        int64_t lo, hi;
+        e.template bases<D>(a.hkv, kvh, lb, lo, hi);
+        attend_block<T, D, false>(a, b, kvh, lb, lo, hi, ctx, 0, qs, ws, g, c);
     }
     if constexpr (APPEND) {
-        if (lb == app_lb) {  // app_lb was validated above
-            attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qs, ws, g, c);
-        }
+        if (lb == app_lb) attend_appended<T, D, BS>(a, b, kvh, lb, trow, nent, ctx, app_off, qs, ws, g, c);
     }
     __shared__ float sm_ml[NW][8][2];
     __shared__ float sm_o[NW][8][D];
@@ -491,7 +561,7 @@ __global__ void __launch_bounds__(NW * 32, 16 / NW) paged_decode_kernel(DecodeAr
 // Balanced split-K kernel for the 16-bit cache (the split itself:
 // balanced.cuh).  Warp i walks its range run by run; within a run it
 // attends its blocks in order, then writes the run's partial.  No barrier.
-template <typename T, int D, bool APPEND>
+template <typename T, int D, bool APPEND, int BS>
 __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
     paged_decode_balanced_kernel(DecodeArgs a, int batch, int nwt_launch, int min_items) {
     constexpr int KC = D / 32;
@@ -506,25 +576,26 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
     const int i = blockIdx.x * kNW + warp;
     WarpSplit ws_;
     bool bad = false;
-    const bool any = ws_.begin(a.ctx_lens, batch, a.max_blocks, a.hkv, nwt_launch, min_items, i, bad);
+    const bool any = ws_.begin(a.ctx_lens, batch, a.cap, a.hkv, nwt_launch, min_items, i, bad);
     if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
     if (!any) return;
 
     while (ws_.next()) {
         const int b = ws_.b, nb = ws_.nb, ctx = ws_.ctx, kvh = ws_.kvh, lb0 = ws_.lb0, lb1 = ws_.lb1;
         const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+        const int nent = (ctx + BS - 1) / BS;  // table entries the context covers
 
-        // fused append: the new row is at ctx - 1, in the run's last block
+        // fused append: the new row is at ctx - 1, in the run's last unit
         int app_lb = -1, app_off = 0;
         if constexpr (APPEND) {
             if (lb1 == nb) {
                 const int64_t slot = a.slots[b];
                 if (slot >= 0) {
-                    const int phys = trow[nb - 1], off = (ctx - 1) % BS;
+                    const int phys = trow[nent - 1], off = (ctx - 1) % BS;
                     if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks) &&
                         slot == static_cast<int64_t>(phys) * BS + off) {
                         app_lb = nb - 1;
-                        app_off = off;
+                        app_off = (ctx - 1) % kUnit;
                     } else if (lane == 0) {
                         atomicOr(a.status, PKV_STATUS_BAD_SLOT);
                     }
@@ -540,22 +611,26 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) ws.o[mt][0] = ws.o[mt][1] = ws.o[mt][2] = ws.o[mt][3] = 0.f;
 
-        // the appended block is the run's last: attended after the loop
-        int tab = 0, k = 0, lb = lb0;
+        // the appended unit is the run's last: attended after the loop
+        UnitIds<BS> tab;
+        tab.e0 = tab.e1 = 0;
+        int k = 0, lb = lb0;
         for (; lb < lb1 && lb != app_lb; ++k, ++lb) {
-            if ((k & 31) == 0) {  // physical ids of the next 32 blocks of the run
+            if ((k & 31) == 0) {  // table entries of the next 32 units of the run
                 const int idx = lb + lane;
-                tab = idx < lb1 ? trow[idx] : 0;
+                tab.load(trow, idx, idx < lb1, nent);
             }
-            const int phys = __shfl_sync(0xffffffffu, tab, k & 31);
-            if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+            const UnitIds<BS> e = tab.shfl(k & 31);
+            if (!e.valid(a.num_blocks)) {
                 if (lane == 0) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
                 continue;
             }
-            attend_block<T, D, false>(a, b, kvh, lb, phys, ctx, 0, qs, ws, g, c);
+            int64_t lo, hi;
+            e.template bases<D>(a.hkv, kvh, lb, lo, hi);
+            attend_block<T, D, false>(a, b, kvh, lb, lo, hi, ctx, 0, qs, ws, g, c);
         }
         if constexpr (APPEND) {
-            if (lb == app_lb) attend_block<T, D, true>(a, b, kvh, lb, trow[lb], ctx, app_off, qs, ws, g, c);
+            if (lb == app_lb) attend_appended<T, D, BS>(a, b, kvh, lb, trow, nent, ctx, app_off, qs, ws, g, c);
         }
 
         float l0 = ws.l0, l1 = ws.l1;
@@ -600,7 +675,7 @@ __global__ void __launch_bounds__(kNW * 32, 16 / kNW)
 // dependent launch.
 template <typename T, int D, int PG>
 __global__ void __launch_bounds__(D * PG) merge_balanced_kernel(
-    const int32_t* __restrict__ ctx_lens, int batch, int hq, int hkv, int max_blocks,
+    const int32_t* __restrict__ ctx_lens, int batch, int hq, int hkv, int cap,
     int nwt_launch, int min_items, const float* __restrict__ ws_o,
     const float* __restrict__ ws_ml, T* __restrict__ out) {
     constexpr int NT = D * PG, NWARP = NT / 32;
@@ -608,7 +683,6 @@ __global__ void __launch_bounds__(D * PG) merge_balanced_kernel(
     const int d = threadIdx.x % D, pg = threadIdx.x / D;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = hq / hkv, kvh = h / G, hl = h - kvh * G;
-    const int cap = max_blocks * BS;
     // Where the run sits among the items follows from the context lengths
     // alone -- inputs of the call, not outputs of the decode grid -- so it is
     // worked out before the wait: the blocks of the sequences before b and
@@ -686,14 +760,13 @@ __global__ void __launch_bounds__(D * PG) merge_balanced_kernel(
 // launch_merge).
 template <typename T, int D, int PG>
 __global__ void __launch_bounds__(D * PG) merge_kernel(
-    const int32_t* __restrict__ ctx_lens, int hq, int max_blocks, int part_blocks, int max_parts,
+    const int32_t* __restrict__ ctx_lens, int hq, int cap, int part_blocks, int max_parts,
     const float* __restrict__ ws_o, const float* __restrict__ ws_ml, T* __restrict__ out) {
     const int h = blockIdx.x, b = blockIdx.y;
     const int d = threadIdx.x % D, pg = threadIdx.x / D;
     int ctx = ctx_lens[b];
-    const int cap = max_blocks * BS;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int nblk = (ctx + BS - 1) / BS;
+    const int nblk = (ctx + kUnit - 1) / kUnit;  // units
     const int np = (nblk + part_blocks - 1) / part_blocks;
     const int64_t row0 = (static_cast<int64_t>(b) * hq + h) * max_parts;
     // partials are produced by the preceding grid: wait for it (a no-op
@@ -727,9 +800,11 @@ __global__ void __launch_bounds__(D * PG) merge_kernel(
     }
 }
 
+// part_blocks: 16-token units per partition; units: units per table.
 struct Shape {
     int batch, hq, hkv, D, num_blocks, block_size, max_blocks, part_blocks, max_parts;
-    bool balanced;  // automatic split: balanced over warps instead of fixed partitions
+    int cap, units;  // table capacity in tokens and in 16-token units
+    bool balanced;   // automatic split: balanced over warps instead of fixed partitions
 };
 
 
@@ -753,9 +828,8 @@ int num_sms() {
 // still gives >= 12 x SMs (query head, partition) work items, i.e. ~3
 // partition CTAs per SM at a GQA group of 4; small batches get finer splits.
 // (Measured on the 8-sequence prefix workload: 256 beat both 128 and 512.)
-int auto_partition_size(int32_t batch, int32_t hq, int32_t max_blocks) {
+int auto_partition_size(int32_t batch, int32_t hq, int64_t tokens) {
     const int n = num_sms();
-    const int64_t tokens = static_cast<int64_t>(max_blocks) * BS;
     for (int ps = 512; ps > 64; ps /= 2) {
         const int64_t parts = (tokens + ps - 1) / ps;
         if (static_cast<int64_t>(batch) * hq * parts >= 12LL * n) return ps;
@@ -776,8 +850,8 @@ bool balanced_candidate(int64_t batch, int64_t max_items) {
            max_items >= static_cast<int64_t>(kBalancedItemsPerWarp) * num_sms() * 16;
 }
 
-bool use_balanced(int64_t batch, int64_t hkv, int64_t max_blocks) {
-    const int64_t items = batch * hkv * max_blocks;
+bool use_balanced(int64_t batch, int64_t hkv, int64_t max_units) {
+    const int64_t items = batch * hkv * max_units;
     return balanced_candidate(batch, items) && items < (1LL << 30);
 }
 
@@ -788,6 +862,26 @@ size_t balanced_bytes(int32_t batch, int32_t hq, int32_t G, int32_t D, int32_t n
 
 namespace {
 
+// Block sizes the 16-bit decode kernels are built for.
+bool block_size_supported(int32_t bs) { return bs == 8 || bs == 16 || bs == 32; }
+
+// Partition layout of a split-K call: units per table, 16-token units per
+// partition and partitions per table.  partition_size (0: automatic) must be
+// a positive multiple of both 16 and block_size.
+int partition_layout(int32_t batch, int32_t hq, int32_t max_blocks, int32_t block_size,
+                     int32_t partition_size, Shape* s) {
+    const int64_t cap = static_cast<int64_t>(max_blocks) * block_size;
+    if (cap > (1LL << 30)) return PKV_ERR_UNSUPPORTED;
+    if (partition_size == 0) partition_size = auto_partition_size(batch, hq, cap);
+    if (partition_size % block_size != 0 || partition_size % kUnit != 0) return PKV_ERR_INVALID_ARG;
+    s->cap = static_cast<int>(cap);
+    s->units = static_cast<int>((cap + kUnit - 1) / kUnit);
+    s->part_blocks = partition_size / kUnit;
+    s->max_parts = (s->units + s->part_blocks - 1) / s->part_blocks;
+    if (s->max_parts < 1) s->max_parts = 1;
+    return PKV_OK;
+}
+
 int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_blocks,
                 int32_t block_size, int32_t max_blocks, int32_t partition_size, int dtype,
                 Shape* s) {
@@ -796,11 +890,12 @@ int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_b
         return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_INVALID_ARG;
     if (hq % hkv != 0) return PKV_ERR_INVALID_ARG;
-    if (block_size != BS || (D != 64 && D != 128) || hq / hkv > 8) return PKV_ERR_UNSUPPORTED;
+    if (!block_size_supported(block_size) || (D != 64 && D != 128) || hq / hkv > 8)
+        return PKV_ERR_UNSUPPORTED;
     if (batch > 65535 || hkv > 65535) return PKV_ERR_UNSUPPORTED;
-    s->balanced = partition_size == 0 && use_balanced(batch, hkv, max_blocks);
-    if (partition_size == 0) partition_size = auto_partition_size(batch, hq, max_blocks);
-    if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
+    const int st = partition_layout(batch, hq, max_blocks, block_size, partition_size, s);
+    if (st != PKV_OK) return st;
+    s->balanced = partition_size == 0 && use_balanced(batch, hkv, s->units);
     s->batch = batch;
     s->hq = hq;
     s->hkv = hkv;
@@ -808,9 +903,6 @@ int check_shape(int32_t batch, int32_t hq, int32_t hkv, int32_t D, int32_t num_b
     s->num_blocks = num_blocks;
     s->block_size = block_size;
     s->max_blocks = max_blocks;
-    s->part_blocks = partition_size / block_size;
-    s->max_parts = (max_blocks + s->part_blocks - 1) / s->part_blocks;
-    if (s->max_parts < 1) s->max_parts = 1;
     return PKV_OK;
 }
 
@@ -818,32 +910,32 @@ size_t partial_bytes(const Shape& s) {
     return static_cast<size_t>(s.batch) * s.hq * s.max_parts * (s.D + 2) * sizeof(float);
 }
 
-template <typename T, int D, int MODE, bool APPEND>
+template <typename T, int D, int MODE, bool APPEND, int BS>
 int launch_kernel(const DecodeArgs& a, const Shape& s, cudaStream_t st) {
     dim3 grid(MODE == kSingle ? 1 : s.max_parts, s.hkv, s.batch);
-    paged_decode_kernel<T, D, kNW, MODE, APPEND><<<grid, kNW * 32, 0, st>>>(a);
+    paged_decode_kernel<T, D, kNW, MODE, APPEND, BS><<<grid, kNW * 32, 0, st>>>(a);
     return launch_status();
+}
+
+template <int MODE, bool APPEND, int BS>
+int dispatch_bs(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
+    if (dtype == PKV_DTYPE_BF16) {
+        if (s.D == 128) return launch_kernel<__nv_bfloat16, 128, MODE, APPEND, BS>(a, s, st);
+        return launch_kernel<__nv_bfloat16, 64, MODE, APPEND, BS>(a, s, st);
+    }
+    if (s.D == 128) return launch_kernel<__half, 128, MODE, APPEND, BS>(a, s, st);
+    return launch_kernel<__half, 64, MODE, APPEND, BS>(a, s, st);
 }
 
 template <int MODE, bool APPEND>
 int dispatch(const DecodeArgs& a, const Shape& s, int dtype, cudaStream_t st) {
-    if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128) return launch_kernel<__nv_bfloat16, 128, MODE, APPEND>(a, s, st);
-        return launch_kernel<__nv_bfloat16, 64, MODE, APPEND>(a, s, st);
-    }
-    if (s.D == 128) return launch_kernel<__half, 128, MODE, APPEND>(a, s, st);
-    return launch_kernel<__half, 64, MODE, APPEND>(a, s, st);
-}
-
-template <typename T, int D, bool APPEND>
-int launch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int min_items, cudaStream_t st) {
-    paged_decode_balanced_kernel<T, D, APPEND>
-        <<<(nwt + kNW - 1) / kNW, kNW * 32, 0, st>>>(a, s.batch, nwt, min_items);
-    return launch_status();
+    if (s.block_size == 8) return dispatch_bs<MODE, APPEND, 8>(a, s, dtype, st);
+    if (s.block_size == 32) return dispatch_bs<MODE, APPEND, 32>(a, s, dtype, st);
+    return dispatch_bs<MODE, APPEND, 16>(a, s, dtype, st);
 }
 
 template <typename T, int D, int PG>
-int launch_merge_balanced_t(const int32_t* ctx_lens, int batch, int hq, int hkv, int max_blocks, int nwt,
+int launch_merge_balanced_t(const int32_t* ctx_lens, int batch, int hq, int hkv, int cap, int nwt,
                             const float* ws_o, const float* ws_ml, void* out, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(hq, batch);
@@ -856,30 +948,37 @@ int launch_merge_balanced_t(const int32_t* ctx_lens, int batch, int hq, int hkv,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_balanced_kernel<T, D, PG>, ctx_lens, batch, hq, hkv,
-                                             max_blocks, nwt, kBalancedMinItems, ws_o, ws_ml,
+                                             cap, nwt, kBalancedMinItems, ws_o, ws_ml,
                                              static_cast<T*>(out));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // Balanced split: the warp-range kernel, then its merge.
-template <typename T, int D, bool APPEND>
+template <typename T, int D, bool APPEND, int BS>
 int run_balanced(const DecodeArgs& a, const Shape& s, int nwt, cudaStream_t st) {
-    paged_decode_balanced_kernel<T, D, APPEND>
+    paged_decode_balanced_kernel<T, D, APPEND, BS>
         <<<(nwt + kNW - 1) / kNW, kNW * 32, 0, st>>>(a, s.batch, nwt, kBalancedMinItems);
     const int r = launch_status();
     if (r != PKV_OK) return r;
-    return launch_balanced_merge(a.ctx_lens, s.batch, s.hq, s.hkv, D, s.max_blocks, nwt, a.ws_o, a.ws_ml,
-                                 a.out, std::is_same<T, __half>::value ? PKV_DTYPE_F16 : PKV_DTYPE_BF16, st);
+    return launch_balanced_merge(a.ctx_lens, s.batch, s.hq, s.hkv, D, s.cap, nwt, a.ws_o, a.ws_ml, a.out,
+                                 std::is_same<T, __half>::value ? PKV_DTYPE_F16 : PKV_DTYPE_BF16, st);
+}
+
+template <bool APPEND, int BS>
+int dispatch_balanced_bs(const DecodeArgs& a, const Shape& s, int nwt, int dtype, cudaStream_t st) {
+    if (dtype == PKV_DTYPE_BF16) {
+        if (s.D == 128) return run_balanced<__nv_bfloat16, 128, APPEND, BS>(a, s, nwt, st);
+        return run_balanced<__nv_bfloat16, 64, APPEND, BS>(a, s, nwt, st);
+    }
+    if (s.D == 128) return run_balanced<__half, 128, APPEND, BS>(a, s, nwt, st);
+    return run_balanced<__half, 64, APPEND, BS>(a, s, nwt, st);
 }
 
 template <bool APPEND>
 int dispatch_balanced(const DecodeArgs& a, const Shape& s, int nwt, int dtype, cudaStream_t st) {
-    if (dtype == PKV_DTYPE_BF16) {
-        if (s.D == 128) return run_balanced<__nv_bfloat16, 128, APPEND>(a, s, nwt, st);
-        return run_balanced<__nv_bfloat16, 64, APPEND>(a, s, nwt, st);
-    }
-    if (s.D == 128) return run_balanced<__half, 128, APPEND>(a, s, nwt, st);
-    return run_balanced<__half, 64, APPEND>(a, s, nwt, st);
+    if (s.block_size == 8) return dispatch_balanced_bs<APPEND, 8>(a, s, nwt, dtype, st);
+    if (s.block_size == 32) return dispatch_balanced_bs<APPEND, 32>(a, s, nwt, dtype, st);
+    return dispatch_balanced_bs<APPEND, 16>(a, s, nwt, dtype, st);
 }
 
 // The merge grid is launched with programmatic stream serialization: it may
@@ -900,7 +999,7 @@ int launch_merge(const int32_t* ctx_lens, const Shape& s, const float* ws_o, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D, PG>, ctx_lens, s.hq, s.max_blocks,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, merge_kernel<T, D, PG>, ctx_lens, s.hq, s.cap,
                                              s.part_blocks, s.max_parts, ws_o, ws_ml,
                                              static_cast<T*>(out));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
@@ -940,6 +1039,7 @@ int fill_args(DecodeArgs* a, const void* q, const void* k_pool, const void* v_po
     a->G = s.hq / s.hkv;
     a->num_blocks = s.num_blocks;
     a->max_blocks = s.max_blocks;
+    a->cap = s.cap;
     a->part_blocks = s.part_blocks;
     a->max_parts = s.max_parts;
     a->scale_log2 = scale * kLog2e;
@@ -964,12 +1064,12 @@ int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_
     DecodeArgs a = a0;
     a.out = out;
     if (s.max_parts <= 1) {
-        a.part_blocks = s.max_blocks > 0 ? s.max_blocks : 1;
+        a.part_blocks = s.units > 0 ? s.units : 1;
         return dispatch<kSingle, APPEND>(a, s, dtype, cs);
     }
     if (s.balanced) {
         // 4 CTAs of 4 warps per SM
-        const int nwt = balanced_warps(static_cast<int64_t>(s.batch) * s.hkv * s.max_blocks, 4 * kNW);
+        const int nwt = balanced_warps(static_cast<int64_t>(s.batch) * s.hkv * s.units, 4 * kNW);
         const int G = s.hq / s.hkv;
         if (!ws || ws_bytes < balanced_bytes(s.batch, s.hq, G, s.D, nwt)) return PKV_ERR_WORKSPACE;
         if (!aligned16(ws)) return PKV_ERR_MISALIGNED;
@@ -988,15 +1088,13 @@ int decode(const DecodeArgs& a0, const Shape& s, void* out, void* ws, size_t ws_
 
 // Runs of one (sequence, KV head) span about nwt / (batch * Hkv) warp ranges
 // at the longest; beyond 16 the merge folds with 4 partial groups per CTA.
-int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int max_blocks,
-                          int nwt, const float* ws_o, const float* ws_ml, void* out, int dtype,
-                          cudaStream_t st) {
+int launch_balanced_merge(const int32_t* ctx_lens, int batch, int hq, int hkv, int D, int cap, int nwt,
+                          const float* ws_o, const float* ws_ml, void* out, int dtype, cudaStream_t st) {
     const bool many = nwt > 16LL * batch * hkv;
-#define PKV_BMERGE(TT, DD)                                                                             \
-    return many ? launch_merge_balanced_t<TT, DD, 4>(ctx_lens, batch, hq, hkv, max_blocks, nwt, ws_o, \
-                                                     ws_ml, out, st)                                 \
-                : launch_merge_balanced_t<TT, DD, 1>(ctx_lens, batch, hq, hkv, max_blocks, nwt, ws_o, \
-                                                     ws_ml, out, st)
+#define PKV_BMERGE(TT, DD)                                                                                \
+    return many ? launch_merge_balanced_t<TT, DD, 4>(ctx_lens, batch, hq, hkv, cap, nwt, ws_o, ws_ml, out, \
+                                                     st)                                                  \
+                : launch_merge_balanced_t<TT, DD, 1>(ctx_lens, batch, hq, hkv, cap, nwt, ws_o, ws_ml, out, st)
     if (dtype == PKV_DTYPE_BF16) {
         if (D == 128) PKV_BMERGE(__nv_bfloat16, 128);
         PKV_BMERGE(__nv_bfloat16, 64);
@@ -1015,16 +1113,16 @@ extern "C" int pkv_decode_workspace_bytes(int32_t batch, int32_t num_q_heads, in
         block_size <= 0 || partition_size < 0)
         return PKV_ERR_INVALID_ARG;
     const bool automatic = partition_size == 0;
-    if (automatic) partition_size = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
-    if (partition_size % block_size != 0) return PKV_ERR_INVALID_ARG;
-    const int64_t part_blocks = partition_size / block_size;
-    const int64_t parts = (max_blocks + part_blocks - 1) / part_blocks;
+    pkv::Shape s;
+    const int st = pkv::partition_layout(batch, num_q_heads, max_blocks, block_size, partition_size, &s);
+    if (st != PKV_OK) return st;
+    const int64_t parts = s.max_parts;
     if (parts <= 1) {
         *out = 0;
         return PKV_OK;
     }
     const size_t fixed = static_cast<size_t>(batch) * num_q_heads * parts * (head_dim + 2) * sizeof(float);
-    const int64_t max_items = static_cast<int64_t>(batch) * num_q_heads * max_blocks;  // Hkv <= Hq
+    const int64_t max_items = static_cast<int64_t>(batch) * num_q_heads * s.units;  // Hkv <= Hq
     if (automatic && pkv::balanced_candidate(batch, max_items)) {
         // room for a balanced split (16-bit cache) with Hkv anywhere in
         // [1, Hq] and a GQA group up to 8; the quantised decode still splits
@@ -1066,13 +1164,12 @@ extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int
     if (batch < 0 || num_q_heads <= 0 || max_blocks < 0 || partition_size < 0 ||
         (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16))
         return PKV_ERR_INVALID_ARG;
-    if (block_size != pkv::BS || (head_dim != 64 && head_dim != 128) || batch > 65535 ||
+    if (!pkv::block_size_supported(block_size) || (head_dim != 64 && head_dim != 128) || batch > 65535 ||
         num_q_heads > 65535)
         return PKV_ERR_UNSUPPORTED;
-    const int32_t ps = partition_size == 0 ? pkv::auto_partition_size(batch, num_q_heads, max_blocks)
-                                           : partition_size;
-    if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
     pkv::Shape s;
+    const int st = pkv::partition_layout(batch, num_q_heads, max_blocks, block_size, partition_size, &s);
+    if (st != PKV_OK) return st;
     s.batch = batch;
     s.hq = num_q_heads;
     s.hkv = 1;
@@ -1080,9 +1177,7 @@ extern "C" int pkv_paged_attention_decode_merge(const int32_t* context_lens, int
     s.num_blocks = 1;
     s.block_size = block_size;
     s.max_blocks = max_blocks;
-    s.part_blocks = ps / block_size;
-    s.max_parts = (max_blocks + s.part_blocks - 1) / s.part_blocks;
-    if (s.max_parts < 1) s.max_parts = 1;
+    s.balanced = false;
     if (batch == 0) return PKV_OK;
     if (!context_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!pkv::aligned16(out)) return PKV_ERR_MISALIGNED;
@@ -1144,7 +1239,7 @@ extern "C" int pkv_paged_attention_decode_append(
 extern "C" int pkv_decode_auto_partition_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks,
                                               int32_t block_size, int32_t* out) {
     if (!out || batch < 0 || num_q_heads <= 0 || max_blocks < 0) return PKV_ERR_INVALID_ARG;
-    if (block_size != pkv::BS) return PKV_ERR_UNSUPPORTED;
-    *out = pkv::auto_partition_size(batch, num_q_heads, max_blocks);
+    if (!pkv::block_size_supported(block_size)) return PKV_ERR_UNSUPPORTED;
+    *out = pkv::auto_partition_size(batch, num_q_heads, static_cast<int64_t>(max_blocks) * block_size);
     return PKV_OK;
 }

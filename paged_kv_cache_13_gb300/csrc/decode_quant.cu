@@ -853,7 +853,8 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     const int i = blockIdx.x * NW + warp;
     WarpSplit sp;
     bool bad = false;
-    const bool any = sp.begin(a.ctx_lens, batch, a.max_blocks, a.hkv, nwt_launch, kBalancedMinItems, i, bad);
+    const bool any =
+        sp.begin(a.ctx_lens, batch, a.max_blocks * BS, a.hkv, nwt_launch, kBalancedMinItems, i, bad);
     if (i == 0 && bad && lane == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
     if (!any) return;
     while (sp.next()) {
@@ -957,8 +958,9 @@ extern "C" int pkv_paged_attention_decode_quant(
     if (qmode == PKV_QMODE_INT4_ASYM &&
         !(group_size == head_dim || (head_dim == 128 && group_size == 64)))
         return PKV_ERR_UNSUPPORTED;
-    const int32_t ps = partition_size == 0 ? pkv::auto_partition_size(batch, num_q_heads, max_blocks)
-                                           : partition_size;
+    const int32_t ps = partition_size == 0
+                           ? pkv::auto_partition_size(batch, num_q_heads, static_cast<int64_t>(max_blocks) * pkv::BS)
+                           : partition_size;
     if (ps % block_size != 0) return PKV_ERR_INVALID_ARG;
     if (batch == 0) return PKV_OK;
     if (!q || !k_codes || !k_scale || !v_codes || !v_scale || !block_tables || !context_lens || !out)
@@ -1019,8 +1021,8 @@ extern "C" int pkv_paged_attention_decode_quant(
         a.ws_ml = a.ws_o + rows * head_dim;
         int r = pkv::dispatch<true, true>(a, head_dim, qmode, ng, dtype, 0, num_kv_heads, batch, nwt, cs);
         if (r != PKV_OK) return r;
-        return pkv::launch_balanced_merge(context_lens, batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
-                                          nwt, a.ws_o, a.ws_ml, out, dtype, cs);
+        return pkv::launch_balanced_merge(context_lens, batch, num_q_heads, num_kv_heads, head_dim,
+                                          max_blocks * block_size, nwt, a.ws_o, a.ws_ml, out, dtype, cs);
     }
     if (a.max_parts <= 1) {
         a.part_blocks = max_blocks > 0 ? max_blocks : 1;

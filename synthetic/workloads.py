@@ -112,7 +112,11 @@ def context_lengths(w):
 
 
 def free_order(w):
-    """Seeded permutation of the pool's block ids: the allocation order."""
+    """The pool's allocation order: a seeded permutation of the block ids,
+    or, for a workload with ``in_order``, the ids in ascending order (each
+    sequence prefilled in one go then owns consecutive blocks)."""
+    if w.get("in_order"):
+        return np.arange(w["num_blocks"], dtype=np.int32)
     rng = _rng(w, _S_FREE)
     return rng.permutation(w["num_blocks"]).astype(np.int32)
 

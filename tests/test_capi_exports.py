@@ -51,13 +51,18 @@ def test_host_validation_rejects_before_launch(pkv):
     assert st == -1
     # unsupported head dim and block size
     assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 96, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -8
-    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 32, 4, 1.0, 16, None, 0, 0, 1, None) == -8
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 24, 4, 1.0, 16, None, 0, 0, 1, None) == -8
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 64, 4, 1.0, 16, None, 0, 0, 1, None) == -8
     # GQA group above 8
     assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 32, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -8
     # misaligned query pointer
     assert L.pkv_paged_attention_decode(18, 16, 16, 16, 16, 1, 8, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 0, 1, None) == -10
     # partition not a multiple of the block size
     assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 16, 4, 1.0, 16, None, 0, 100, 1, None) == -1
+    # 8-token blocks: the partition must also be a multiple of the 16-token tile
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 8, 4, 1.0, 16, None, 0, 24, 1, None) == -1
+    # 32-token blocks: a 16-token partition is not a multiple of the block
+    assert L.pkv_paged_attention_decode(16, 16, 16, 16, 16, 1, 8, 2, 128, 10, 32, 4, 1.0, 16, None, 0, 16, 1, None) == -1
     # bad dtype
     assert L.pkv_kv_append(16, 16, 16, 1, 16, 16, 4, 2, 128, 16, 7, None) == -1
     # empty work is a no-op even without a device
@@ -116,3 +121,22 @@ def test_auto_partition_size(pkv):
     assert pkv.pkv_decode_auto_partition_size(3, 8, 3) == 64
     # the workspace for partition 0 covers the automatic partitions
     assert pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 0) >= pkv.pkv_decode_workspace_bytes(8, 32, 128, 144, 16, 256)
+
+
+def test_block_sizes_8_and_32(pkv):
+    """Block sizes 8 and 32 keep the same split in tokens: the workspace
+    follows the tables' capacity in tokens (max_blocks x block_size), and
+    the automatic partition size depends on that capacity alone."""
+    for bs, mb in ((8, 512), (32, 128)):  # 4,096 tokens, as 256 blocks of 16
+        assert pkv.pkv_decode_workspace_bytes(64, 32, 128, mb, bs, 512) == \
+            pkv.pkv_decode_workspace_bytes(64, 32, 128, 256, 16, 512)
+        assert pkv.pkv_decode_workspace_bytes(4, 32, 128, mb * 16, bs, 0) == \
+            pkv.pkv_decode_workspace_bytes(4, 32, 128, 4096, 16, 0)
+        assert pkv.pkv_decode_auto_partition_size(8, 32, 144 * 16 // bs, bs) == 256
+    # an odd number of 8-token blocks: 3 blocks = 24 tokens = 2 tiles of 16
+    assert pkv.pkv_decode_workspace_bytes(1, 3, 64, 3, 8, 16) == 3 * 2 * 66 * 4
+    # 32-token blocks: 48-token partitions are not whole blocks
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_decode_workspace_bytes(1, 3, 64, 4, 32, 48)
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_decode_auto_partition_size(8, 32, 144, 24)
