@@ -342,15 +342,37 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
  *   over KV head h / (num_q_heads / num_kv_heads).  out: [T, num_q_heads,
  *   head_dim] (dtype).  L_b = 1 is pkv_paged_attention_decode.
  *   context_lens[b] < L_b sets PKV_STATUS_BAD_CONTEXT; rows at negative
- *   positions get zeros.  No workspace; one pass per (8 or 16 query rows,
- *   KV head, sequence).
+ *   positions get zeros.
+ * Two kernels:
+ *   - workspace (device, nullable) of at least
+ *     pkv_multi_query_workspace_bytes bytes, and that size is non-zero
+ *     (max_q_len * G <= 24, batch <= 1024, enough (sequence, KV head,
+ *     block) items to fill the GPU): a balanced split.  Every warp streams
+ *     an equal share of the call's (sequence, KV head, block) items, holding
+ *     all L_b * G rows of its runs, so each K/V byte is read once.  A merge
+ *     kernel follows behind it with programmatic dependent launch.  L_b >
+ *     max_q_len there sets PKV_STATUS_BAD_CONTEXT and only the first
+ *     max_q_len * G rows are computed.  A workspace that is too small
+ *     returns PKV_ERR_WORKSPACE.
+ *   - otherwise one pass per (8 or 16 query rows, KV head, sequence); the
+ *     workspace is not touched.
+ * Calls that share a workspace must not overlap on the GPU.
  * Supported: block_size 16, head_dim 64 or 128, 1 <= G <= 8. */
 int pkv_paged_attention_multi_query(const void* q, const int32_t* q_start, const void* k_pool,
                                     const void* v_pool, const int32_t* block_tables,
                                     const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                     int32_t block_size, int32_t max_blocks, int32_t max_q_len,
-                                    float scale, void* out, int dtype, void* stream);
+                                    float scale, void* out, void* workspace, size_t workspace_bytes,
+                                    int dtype, void* stream);
+
+/* Workspace bytes for pkv_paged_attention_multi_query's balanced split:
+ * (nwt + batch * num_kv_heads) * R * (head_dim + 2) * 4 with R =
+ * 8 * ceil(max_q_len * G / 8) partial rows per slot and nwt the warps it
+ * launches (at most 8 or 12 per SM).  0 when the split does not apply. */
+int pkv_multi_query_workspace_bytes(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t max_blocks, int32_t block_size,
+                                    int32_t max_q_len, size_t* out);
 
 /* Allocation-free decode.  The source pages have no counterpart for this
  * entry point: it exists for callers that cannot provide a device workspace

@@ -75,7 +75,9 @@ _SIGS = {
     "pkv_kv_append": ([_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _int, _vp], _int),
     "pkv_paged_attention_multi_query": (
         [_vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp,
-         _int, _vp], _int),
+         _vp, _sz, _int, _vp], _int),
+    "pkv_multi_query_workspace_bytes": ([_i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)],
+                                        _int),
     "pkv_paged_attention_decode": (
         [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _f32, _vp, _vp, _sz,
          _i32, _int, _vp], _int),
@@ -350,18 +352,30 @@ def pkv_paged_attention_decode(q, k_pool, v_pool, block_tables, context_lens, sc
         _dtype_code(q), _stream(stream)), "pkv_paged_attention_decode")
 
 
+def pkv_multi_query_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks, max_q_len,
+                                    block_size=16):
+    v = _sz()
+    _check(lib.pkv_multi_query_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim, max_blocks,
+                                               block_size, int(max_q_len), ctypes.byref(v)),
+           "pkv_multi_query_workspace_bytes")
+    return v.value
+
+
 def pkv_paged_attention_multi_query(q, q_start, k_pool, v_pool, block_tables, context_lens, scale,
-                                    out, max_q_len, stream=None):
+                                    out, max_q_len, workspace=None, stream=None):
     """q, out [T, Hq, D]; q_start int32 [B + 1] (sequence b's queries are rows
-    q_start[b] .. q_start[b+1]-1, the last of its context_lens[b] tokens)."""
+    q_start[b] .. q_start[b+1]-1, the last of its context_lens[b] tokens).
+    workspace: device bytes (pkv_multi_query_workspace_bytes) for the
+    balanced split, or None."""
     T, Hq, D = q.shape
     NB, Hkv, BS, _ = k_pool.shape
     B = q_start.shape[0] - 1
     mb = block_tables.shape[1]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.pkv_paged_attention_multi_query(
         _ptr(q), _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables), _ptr(context_lens),
-        B, Hq, Hkv, D, NB, BS, mb, int(max_q_len), float(scale), _ptr(out), _dtype_code(q),
-        _stream(stream)), "pkv_paged_attention_multi_query")
+        B, Hq, Hkv, D, NB, BS, mb, int(max_q_len), float(scale), _ptr(out), _ptr(workspace), ws_bytes,
+        _dtype_code(q), _stream(stream)), "pkv_paged_attention_multi_query")
 
 
 def pkv_paged_attention_decode_append(q, k_new, v_new, slot_mapping, k_pool, v_pool, block_tables,

@@ -89,47 +89,6 @@ struct DecodeArgs {
 // head-dim column 64 * (e / 8) + 8 * g + e % 8.
 __device__ __forceinline__ int pv_col(int e, int g) { return 64 * (e >> 3) + 8 * g + (e & 7); }
 
-// Log-sum-exp merge of the partition partials q = q0, q0 + step, ... < np of
-// one (sequence, query head, column): each partial holds (m_q, l_q, o_q[d])
-// with o_q unnormalised.  Loads of 8 partitions are issued together, then
-// folded into a running (M, L, acc) with one rescale per chunk.  Partials
-// are read from L2 (.cg): they were written by another grid.
-struct MergeAcc {
-    float M, L, acc;
-};
-
-__device__ __forceinline__ MergeAcc merge_range(const float* __restrict__ ml, int64_t stride_ml,
-                                                const float* __restrict__ ov, int64_t stride_o,
-                                                int q0, int np, int step) {
-    MergeAcc r{neg_inf(), 0.f, 0.f};
-    for (int qa = q0; qa < np; qa += 8 * step) {
-        float mq[8], lq[8], oq[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int q = qa + j * step;
-            const bool v = q < np;
-            mq[j] = v ? __ldcg(ml + q * stride_ml) : neg_inf();
-            lq[j] = v ? __ldcg(ml + q * stride_ml + 1) : 0.f;
-            oq[j] = v ? __ldcg(ov + q * stride_o) : 0.f;
-        }
-        float mx = r.M;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) mx = fmaxf(mx, mq[j]);
-        if (mx == neg_inf()) continue;  // every partition so far was empty
-        const float sc = ex2(r.M - mx);  // 0 while M is still -inf
-        r.acc *= sc;
-        r.L *= sc;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float w = ex2(mq[j] - mx);
-            r.acc += w * oq[j];
-            r.L += w * lq[j];
-        }
-        r.M = mx;
-    }
-    return r;
-}
-
 // Whether P enters the PV product as two 16-bit terms (value + residual).
 template <typename T>
 constexpr bool kSplitP = false;

@@ -140,3 +140,20 @@ def test_block_sizes_8_and_32(pkv):
         pkv.pkv_decode_workspace_bytes(1, 3, 64, 4, 32, 48)
     with pytest.raises(pkv.PkvError):
         pkv.pkv_decode_auto_partition_size(8, 32, 144, 24)
+
+
+def test_multi_query_workspace_bytes(pkv):
+    """The balanced multi-query split: (nwt + batch x Hkv) slots of R =
+    8 ceil(rows / 8) partial rows of (D + 2) fp32, nwt = min(SMs x warps per
+    SM, items / 2) with 8 warps per SM at 17..24 rows (12 at 1..8)."""
+    sms = _sms()
+    nwt = min(sms * 8, 64 * 8 * 256 // 2)
+    assert pkv.pkv_multi_query_workspace_bytes(64, 32, 8, 128, 256, 6) == (nwt + 64 * 8) * 24 * 130 * 4
+    nwt1 = min(sms * 12, 64 * 8 * 256 // 2)
+    assert pkv.pkv_multi_query_workspace_bytes(64, 32, 8, 128, 256, 2) == (nwt1 + 64 * 8) * 8 * 130 * 4
+    # more than 24 rows per KV head, too few items, too many sequences: none
+    assert pkv.pkv_multi_query_workspace_bytes(64, 32, 8, 128, 256, 7) == 0
+    assert pkv.pkv_multi_query_workspace_bytes(2, 32, 8, 128, 16, 6) == 0
+    assert pkv.pkv_multi_query_workspace_bytes(1025, 32, 8, 128, 256, 1) == 0
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_multi_query_workspace_bytes(64, 32, 8, 128, 256, 6, block_size=8)

@@ -127,3 +127,99 @@ def test_speculative_verify_full_layer_sampled(pkv, cuda_dev):
     q, q_start, got = _run(pkv, c, [6] * len(c.decoded), seed=5)
     assert pkv.pkv_device_status() == 0
     _check(c, q, q_start, got, seqs=[0, 17, 63], what="verify")
+
+
+# ---------------------------------------------------------------- balanced split
+def _run_balanced(pkv, c, qlens, seed=0, lens=None, max_q_len=None):
+    """The multi-query call with a workspace: the balanced split where it
+    applies (asserted)."""
+    w = c.w
+    B = len(qlens)
+    mq = max(max(qlens), 1) if max_q_len is None else max_q_len
+    n = pkv.pkv_multi_query_workspace_bytes(B, w["hq"], w["hkv"], w["d"], c.max_blocks, mq)
+    assert n > 0, "the balanced split should apply"
+    ws = torch.empty(n, dtype=torch.uint8, device=c.q.device)
+    q, q_start = _queries(w, qlens, seed)
+    dev = c.q.device
+    out = torch.full(q.shape, 7.0, dtype=q.dtype, device=dev)
+    pkv.pkv_paged_attention_multi_query(q.to(dev), torch.from_numpy(q_start).to(dev), c.k_pool, c.v_pool,
+                                        c.tables, c.lens if lens is None else lens, w["scale"], out, mq,
+                                        workspace=ws)
+    torch.cuda.synchronize()
+    return q, q_start, out.float().cpu().numpy()
+
+
+def test_balanced_verify_full_layer(pkv, cuda_dev):
+    """gamma + 1 = 6 queries on the 64-sequence layer (24 rows per KV head):
+    every sequence against the oracle, and against the one-pass kernel."""
+    w = syn.workload("llama3_8b_b64")
+    c = build(pkv, w, cuda_dev)
+    q, q_start, got = _run_balanced(pkv, c, [6] * len(c.decoded), seed=5)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="balanced verify")
+    _, _, tile = _run(pkv, c, [6] * len(c.decoded), seed=5)
+    assert_close(got, tile.astype(np.float64), what="balanced vs one-pass")
+
+
+def _short(n=640, hi=320, **over):
+    rng = np.random.default_rng(21)
+    lens = [int(x) for x in rng.integers(1, hi + 1, size=n)]
+    base = dict(lens=lens, num_blocks=sum(-(-L // 16) for L in lens) + n + 64)
+    base.update(over)
+    return syn.workload("llama3_8b_b64", **base)
+
+
+@pytest.mark.parametrize("hq,hkv,d,dtype,maxL", [(32, 8, 128, "bf16", 6), (64, 8, 64, "fp16", 3),
+                                                 (8, 8, 128, "bf16", 17), (16, 8, 64, "bf16", 8),
+                                                 (32, 8, 128, "fp16", 2)])
+def test_balanced_many_short_sequences(pkv, cuda_dev, hq, hkv, d, dtype, maxL):
+    """640 sequences of 1..320 tokens with ragged query counts 0..maxL (never
+    more than the context): runs start and end inside warp ranges, and some
+    sequences have no queries at all."""
+    w = _short(hq=hq, hkv=hkv, d=d, dtype=dtype)
+    c = build(pkv, w, cuda_dev)
+    rng = np.random.default_rng(hq + d)
+    ctx = syn.context_lengths(w)
+    qlens = [int(min(x, L)) for x, L in zip(rng.integers(0, maxL + 1, size=len(ctx)), ctx)]
+    q, q_start, got = _run_balanced(pkv, c, qlens, seed=7, max_q_len=maxL)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="balanced short G %d D %d" % (hq // hkv, d))
+
+
+def test_balanced_bad_table_entry_and_excess_queries(pkv, cuda_dev):
+    w = _short()
+    c = build(pkv, w, cuda_dev)
+    ctx = syn.context_lengths(w)
+    qlens = [min(4, L) for L in ctx]
+    victim = int(np.argmax(ctx))
+    tables = c.tables.clone()
+    tables[victim, 1] = 1 << 24
+    c.tables = tables
+    pkv.pkv_device_status()
+    q, q_start, got = _run_balanced(pkv, c, qlens, seed=9)
+    assert pkv.pkv_device_status() & pkv.PKV_STATUS_BAD_BLOCK
+    keep = [b for b in range(len(ctx)) if b != victim]
+    _check(c, q, q_start, got, seqs=keep, what="other sequences")
+    # a sequence with more queries than max_q_len: status, first rows computed
+    qlens2 = list(qlens)
+    j = next(b for b in range(len(ctx)) if ctx[b] >= 8 and b != victim)
+    qlens2[j] = 5
+    pkv.pkv_device_status()
+    q2, q_start2, got2 = _run_balanced(pkv, c, qlens2, seed=10, max_q_len=4)
+    assert pkv.pkv_device_status() & pkv.PKV_STATUS_BAD_CONTEXT
+    _check(c, q2, q_start2, got2, seqs=[b for b in keep if b != j], what="others, excess queries")
+    assert pkv.pkv_device_status() == 0
+
+
+def test_balanced_workspace_too_small(pkv, cuda_dev):
+    w = _short()
+    c = build(pkv, w, cuda_dev)
+    B = len(c.decoded)
+    n = pkv.pkv_multi_query_workspace_bytes(B, w["hq"], w["hkv"], w["d"], c.max_blocks, 4)
+    ws = torch.empty(n - 16, dtype=torch.uint8, device=cuda_dev)
+    q = torch.zeros((B * 4, w["hq"], w["d"]), dtype=w["torch_dtype"], device=cuda_dev)
+    q_start = torch.arange(0, B * 4 + 1, 4, dtype=torch.int32, device=cuda_dev)
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.pkv_paged_attention_multi_query(q, q_start, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"],
+                                            torch.empty_like(q), 4, workspace=ws)
+    assert e.value.name == "PKV_ERR_WORKSPACE"
