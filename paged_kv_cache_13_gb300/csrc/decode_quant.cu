@@ -57,6 +57,9 @@ constexpr int kCtasPerSm = QMODE == PKV_QMODE_INT4_ASYM && NG == 1 ? 5 : 4;
 template <int QMODE>
 constexpr bool kQueryInShared = QMODE == PKV_QMODE_INT4_ASYM;
 constexpr float kLog2e = 1.4426950408889634f;
+// Headroom (log2 units) a logit may rise above the running reference max
+// before the online softmax rescales: weights stay <= 2^8 (fp16-safe).
+constexpr float kSlack = 8.f;
 
 struct QDecodeArgs {
     const void* q;
@@ -439,15 +442,19 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         if (!ok0) x0 = x1 = neg_inf();
         if (!ok1) x2 = x3 = neg_inf();
 
-        // ---- online softmax (base 2)
-        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+        // ---- online softmax (base 2).  The reference max m is raised only
+        // when a logit of the block exceeds it by more than kSlack; otherwise
+        // the weights 2^(x - m) <= 2^kSlack are taken against the old m, with
+        // no warp-wide max and no rescale (m cancels in o / l and the merges).
+        const float bx0 = fmaxf(x0, x2), bx1 = fmaxf(x1, x3);
+        if (__any_sync(0xffffffffu, bx0 > m0 + kSlack || bx1 > m1 + kSlack)) {
+            float bm0 = bx0, bm1 = bx1;
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-            bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-        }
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        if (mn0 != m0 || mn1 != m1) {  // warp-uniform: the max is warp-wide
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
             const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
             l0 *= al0;
             l1 *= al1;
@@ -763,7 +770,6 @@ template <typename T, int D, int QMODE, int NG, bool WIN, bool SPLIT>
 __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_quant_kernel(QDecodeArgs a) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
-    constexpr int DS = D / 8;
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
@@ -842,7 +848,6 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     paged_decode_quant_balanced_kernel(QDecodeArgs a, int batch, int nwt_launch) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
-    constexpr int DS = D / 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
     // the merge grid may be scheduled now; it waits for this grid to finish
