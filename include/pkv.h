@@ -90,7 +90,10 @@ enum {
     PKV_STATUS_BAD_SLOT = 2,    /* slot outside [0, num_blocks * block_size)     */
     PKV_STATUS_BAD_CONTEXT = 4, /* context_len < 0 or > max_blocks * block_size  */
     PKV_STATUS_BAD_PAIR = 8,    /* copy pair outside [0, num_blocks)             */
-    PKV_STATUS_BAD_SINK = 16    /* sink row / position outside its buffer        */
+    PKV_STATUS_BAD_SINK = 16,   /* sink row / position outside its buffer        */
+    PKV_STATUS_COPY_TIMEOUT = 32 /* a bounded wait for an asynchronous copy or a
+                                  * tensor-core operation ran out; that call's
+                                  * outputs are undefined                      */
 };
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -354,8 +357,14 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
  *     max_q_len there sets PKV_STATUS_BAD_CONTEXT and only the first
  *     max_q_len * G rows are computed.  A workspace that is too small
  *     returns PKV_ERR_WORKSPACE.
- *   - otherwise one pass per (8 or 16 query rows, KV head, sequence); the
- *     workspace is not touched.
+ *   - otherwise, with head_dim 128, G in {1, 2, 4, 8} and max_q_len * G >
+ *     64 (chunked-prefill slices): the 5th-generation tensor cores, one CTA
+ *     per 128 (query token, query head) rows, tcgen05.mma with the
+ *     accumulators in tensor memory and K/V tiles of 128 keys gathered from
+ *     the blocks by TMA; a wait on those copies or MMAs that runs out sets
+ *     PKV_STATUS_COPY_TIMEOUT.
+ *   - otherwise one pass per (8 or 16 query rows, KV head, sequence).
+ *   Only the balanced split touches the workspace.
  * Calls that share a workspace must not overlap on the GPU.
  * Supported: block_size 16, head_dim 64 or 128, 1 <= G <= 8. */
 int pkv_paged_attention_multi_query(const void* q, const int32_t* q_start, const void* k_pool,

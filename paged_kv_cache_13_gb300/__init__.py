@@ -37,7 +37,7 @@ STATUS_NAMES = {
     -10: "PKV_ERR_MISALIGNED",
 }
 PKV_STATUS_BAD_BLOCK, PKV_STATUS_BAD_SLOT, PKV_STATUS_BAD_CONTEXT = 1, 2, 4
-PKV_STATUS_BAD_PAIR, PKV_STATUS_BAD_SINK = 8, 16
+PKV_STATUS_BAD_PAIR, PKV_STATUS_BAD_SINK, PKV_STATUS_COPY_TIMEOUT = 8, 16, 32
 
 _i32, _i64, _f32, _int = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_int
 _vp, _sz = ctypes.c_void_p, ctypes.c_size_t

@@ -24,6 +24,7 @@
 // per element; blocks past the tile's last position are not read.
 
 #include "balanced.cuh"
+#include "prefill_tc.cuh"
 
 namespace pkv {
 namespace {
@@ -844,6 +845,11 @@ extern "C" int pkv_paged_attention_multi_query(
         return head_dim == 128 ? pkv::dispatch_mq_balanced<__half, 128>(a, batch, nt, nwt, ws_o, ws_ml, cs)
                                : pkv::dispatch_mq_balanced<__half, 64>(a, batch, nt, nwt, ws_o, ws_ml, cs);
     }
+    // long query spans (chunked-prefill slices): the tensor-core kernel
+    if (pkv::prefill_tc_applies(head_dim, num_q_heads / num_kv_heads, rows))
+        return pkv::launch_prefill_tc(q, q_start, k_pool, v_pool, block_tables, context_lens, batch, num_q_heads,
+                                      num_kv_heads, num_blocks, max_blocks, max_q_len, scale, out, st,
+                                      dtype == PKV_DTYPE_BF16, cs);
     if (dtype == PKV_DTYPE_BF16) {
         if (head_dim == 128) pkv::launch_nt<__nv_bfloat16, 128>(a, r, batch, cs);
         else pkv::launch_nt<__nv_bfloat16, 64>(a, r, batch, cs);

@@ -1,0 +1,584 @@
+// Multi-query paged attention over long query spans (chunked-prefill slices)
+// on the 5th-generation tensor cores: tcgen05.mma with the accumulators in
+// tensor memory (TMEM), K/V tiles gathered from the paged pool by TMA.
+//
+// What it computes: exactly pkv_paged_attention_multi_query (multi_query.cu):
+// query token i of sequence b sits at position p = ctx_b - L_b + i and
+//   out[q_start[b] + i, h] = sum_{t <= p} softmax_t(scale <q, K_t>) V_t
+// over KV head h / G ("The 8GB VRAM Breakthrough", §5 "Chunked Prefill": a
+// 512-token slice of a prompt attends to the cache before it and causally
+// to itself).
+//
+// Design (one CTA of 4 warps per 128 query rows of one (sequence, KV head);
+// a row is a (query token, query head) pair, 128 / G tokens per tile):
+// * Q tile [128 rows x 128 dims] bf16/fp16 in shared memory; K and V tiles
+//   of 128 keys (8 pool blocks) in a 2-stage ring, each block's 16 rows
+//   fetched by TMA straight from its physical block (the table is read on
+//   the device; unused or bad blocks are fetched from out of range, which
+//   TMA fills with zeros).
+// * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into TMEM columns
+//   [0, 128); thread r (= TMEM lane r) loads its row of S, applies the
+//   causal mask, runs the online softmax (base 2, the reference max raised
+//   only by more than 8) and writes P to shared memory (bf16: P and its
+//   rounding residual, two operands, so the products see ~16 bits of P).
+// * O += P V (M 128, N 128, K 128 keys) into TMEM columns [128, 256); a
+//   rescale of O (when a row's reference max moves) is a TMEM load / store
+//   of that row.  O / l goes out at the end.
+// * Every operand tile is a grid of 8-row x 128-byte swizzle atoms (128-byte
+//   swizzle), atom (g, h) -- rows 8g .. 8g+7, columns 64h .. 64h+63 -- at
+//   byte h * 16 KiB + g * 1 KiB of its tile.  K-major operands (Q, K, P)
+//   step 32 bytes per K-16 slice inside an atom row (and 16 KiB to the
+//   second column half); V is the MN-major B operand of O += P V (its 8-key
+//   atom groups 1 KiB apart, its two 64-dim halves 16 KiB apart).
+// * One thread issues the TMA loads and the MMAs; completion is tracked by
+//   mbarriers (tcgen05.commit arrives on them).  Every wait is bounded: one
+//   that runs out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together
+//   (the flag is read after a barrier), still freeing its TMEM.
+
+#include <cuda.h>
+
+#include <mutex>
+#include <type_traits>
+
+#include "balanced.cuh"
+#include "prefill_tc.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kRows = 128;   // query rows per CTA (MMA M)
+constexpr int kKeys = 128;   // keys per tile (MMA N of S, K of O)
+constexpr int kDim = 128;    // head dim
+constexpr int kBS = 16;      // tokens per pool block
+constexpr int kTile = kRows * kDim * 2;  // bytes of one 128 x 128 16-bit tile
+constexpr int kThreads = 128;
+constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.f;
+// polls of an mbarrier before a wait gives up: non-blocking tests 32-64 ns
+// apart, so a wait that will never complete ends within ~0.3 s
+constexpr int kSpin = 1 << 22;
+
+// shared-memory map (bytes from the 1 KiB-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;      // 2 stages
+constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
+constexpr int kOffP = kOffV + 2 * kTile;  // P, then its residual (bf16)
+constexpr int kOffBar = kOffP + 2 * kTile;
+constexpr int kSmemBytes = kOffBar + 128 + 1024;  // barriers, then alignment slack
+
+struct TcArgs {
+    const void* q;
+    const int32_t* q_start;
+    const int32_t* tables;
+    const int32_t* ctx_lens;
+    int hq, hkv, G, num_blocks, max_blocks, total_rows;
+    float scale_log2;
+    void* out;
+    int* status;
+};
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ uint32_t sh_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// one arrival that also expects `bytes` of copies to complete on the barrier
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Waits for the barrier's phase of the given parity; false if it has not
+// completed after kSpin polls.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
+    for (int it = 0; it < kSpin; ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (it >= 64) __nanosleep(32);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// UMMA shared-memory descriptor: start, leading and stride byte offsets (16-
+// byte units), version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t start, uint32_t lbo, uint32_t sbo) {
+    return static_cast<uint64_t>((start >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B of the
+// 16-bit type (bf16 or fp16), K-major A, B K-major or MN-major, M 128, N 128.
+template <typename T>
+__device__ __forceinline__ uint32_t instr_desc(bool b_mn_major) {
+    constexpr uint32_t fmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(b_mn_major) << 16) |
+           (static_cast<uint32_t>(kKeys >> 3) << 17) | (static_cast<uint32_t>(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane (warp w: lanes 32w ..)
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Byte offset of element (row r, column col) in a swizzled 128 x 128 tile.
+__device__ __forceinline__ uint32_t tile_off(int r, int col) {
+    return (col >> 6) * 16384 + (r >> 3) * 1024 + (r & 7) * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4) +
+           (col & 7) * 2;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return Half16<T>::pack(lo, hi);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, TcArgs a) {
+    constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = sh_addr(sm);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+    // bars: 0-1 K full, 2-3 V full, 4 S ready, 5 O ready
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
+    int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 68);
+    const uint32_t bar0 = sh_addr(bars);
+    auto bar = [&](int i) { return bar0 + 8 * i; };
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int q0 = a.q_start[b], L = a.q_start[b + 1] - q0;
+    const int tpt = kRows / a.G;  // query tokens per tile
+    const int tok0 = tile * tpt;
+    if (L <= 0 || tok0 >= L) return;
+    int ctx = a.ctx_lens[b];
+    const int cap = a.max_blocks * kBS;
+    if (ctx < L || ctx > cap) {
+        if (tid == 0 && tile == 0 && kvh == 0) atomicOr(a.status, PKV_STATUS_BAD_CONTEXT);
+        ctx = ctx > cap ? cap : ctx;
+    }
+    const int first_pos = ctx - L;
+    const int last_tok = min(tok0 + tpt, L) - 1;
+    const int last_pos = first_pos + last_tok;  // the tile's last query position
+    const int ntiles = last_pos >= 0 ? last_pos / kKeys + 1 : 0;
+    const int nblk = (ctx + kBS - 1) / kBS;  // blocks holding context tokens
+
+    if (tid == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncwarp();
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(sh_addr(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+
+    // ---- Q tile: thread r writes row r (token tok0 + r / G, head r % G)
+    {
+        const int r = tid;
+        const int tok = tok0 + r / a.G, h = r - (r / a.G) * a.G;
+        const bool valid = tok < L;
+        const uint4* src = valid ? reinterpret_cast<const uint4*>(
+                                       static_cast<const T*>(a.q) +
+                                       ((static_cast<int64_t>(q0) + tok) * a.hq + kvh * a.G + h) * kDim)
+                                 : nullptr;
+#pragma unroll
+        for (int ch = 0; ch < kDim / 8; ++ch) {
+            const uint4 v = valid ? src[ch] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sm + kOffQ + tile_off(r, ch * 8)) = v;
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the MMA
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + kKeys;
+
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    // TMA of key tile j into stage j % 2 (thread 0): 8 blocks x 2 column halves
+    // of 16 rows, K and V; blocks past the context or with a bad id read rows
+    // past the map's end (zeros)
+    int issued = 0, s_commits = 0, o_commits = 0;  // thread 0's async work, for the drain
+    auto issue_tile = [&](int j) {
+        ++issued;
+        const int s = j & 1;
+        mbar_arrive_expect_tx(bar(s), kTile);
+        mbar_arrive_expect_tx(bar(2 + s), kTile);
+        for (int jj = 0; jj < kKeys / kBS; ++jj) {
+            const int lb = j * (kKeys / kBS) + jj;
+            int y = a.total_rows;
+            if (lb < nblk) {
+                const int phys = trow[lb];
+                if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks))
+                    y = (phys * a.hkv + kvh) * kBS;
+                else
+                    atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t off = h * 16384 + jj * 2048;
+                tma_load_2d(sbase + kOffK + s * kTile + off, &kmap, h * 64, y, bar(s));
+                tma_load_2d(sbase + kOffV + s * kTile + off, &vmap, h * 64, y, bar(2 + s));
+            }
+        }
+    };
+
+    const uint32_t idesc_s = instr_desc<T>(false), idesc_o = instr_desc<T>(true);
+    const int r = tid;  // this thread's row and TMEM lane
+    const int my_tok = tok0 + r / a.G;
+    const int my_pos = my_tok < L ? first_pos + my_tok : -1;  // -1: padding row, all masked
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m = neg_inf(), l = 0.f;
+    bool aborted = false;
+    if (tid == 0 && ntiles > 0) issue_tile(0);
+
+    for (int j = 0; j < ntiles; ++j) {
+        const int s = j & 1;
+        // ---- S = Q K^T (thread 0 issues)
+        if (tid == 0) {
+            if (!wait_bar(bar(s), (j >> 1) & 1)) {
+                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+                *abort_flag = 1;
+            } else {
+                fence_after_sync();
+                const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kDim / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_f16(tS, smem_desc(qa + off, 16384, 1024), smem_desc(kb + off, 16384, 1024), idesc_s,
+                            kk > 0);
+                }
+                mma_commit(bar(4));
+                ++s_commits;
+            }
+        }
+        __syncwarp();
+        // ---- softmax of this thread's row
+        if (!wait_bar(bar(4), j & 1)) {
+            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+            *abort_flag = 1;
+        }
+        fence_after_sync();
+        float x[kKeys];
+#pragma unroll
+        for (int cc = 0; cc < kKeys / 32; ++cc) {
+            float v[32];
+            tmem_ld32(tS + lane_base + cc * 32, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
+        }
+        tmem_wait_ld();
+        const int key0 = j * kKeys;
+        float mx = neg_inf();
+#pragma unroll
+        for (int i = 0; i < kKeys; ++i) {
+            x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
+            mx = fmaxf(mx, x[i]);
+        }
+        const bool raise = mx > m + kSlack;
+        float alpha = 1.f;
+        if (raise) {
+            alpha = m == neg_inf() ? 0.f : ex2(m - mx);
+            m = mx;
+            l *= alpha;
+        }
+        // the previous tile's O += P V must be done before P and O are touched
+        if (j > 0 && !wait_bar(bar(5), (j - 1) & 1)) {
+            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+            *abort_flag = 1;
+        }
+        fence_after_sync();
+        if (tid == 0 && j + 1 < ntiles) issue_tile(j + 1);  // stage (j + 1) % 2 is free now
+        __syncwarp();
+        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+            for (int cc = 0; cc < kDim / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tO + lane_base + cc * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                tmem_st32(tO + lane_base + cc * 32, v);
+            }
+            tmem_wait_st();
+        }
+        const float mref = m == neg_inf() ? 0.f : m;
+        float sum = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kKeys / 8; ++ch) {
+            float p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                p[i] = ex2(x[ch * 8 + i] - mref);
+                sum += p[i];
+            }
+            uint4 hi, lo;
+            hi.x = pack2<T>(p[0], p[1]);
+            hi.y = pack2<T>(p[2], p[3]);
+            hi.z = pack2<T>(p[4], p[5]);
+            hi.w = pack2<T>(p[6], p[7]);
+            *reinterpret_cast<uint4*>(sm + kOffP + tile_off(r, ch * 8)) = hi;
+            if constexpr (kSplit) {
+                auto res = [](uint32_t w, float a0, float a1) {
+                    return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
+                };
+                lo.x = res(hi.x, p[0], p[1]);
+                lo.y = res(hi.y, p[2], p[3]);
+                lo.z = res(hi.z, p[4], p[5]);
+                lo.w = res(hi.w, p[6], p[7]);
+                *reinterpret_cast<uint4*>(sm + kOffP + kTile + tile_off(r, ch * 8)) = lo;
+            }
+        }
+        l += sum;
+        // keys past the context in this tile: their V rows may hold any bits
+        // (0 x NaN would poison O); zero them once the tile has landed
+        if (key0 + kKeys > ctx) {
+            if (!wait_bar(bar(2 + s), (j >> 1) & 1)) {
+                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+                *abort_flag = 1;
+            } else if (key0 + r >= ctx) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + h * 16384 + (r >> 3) * 1024 +
+                                                          (r & 7) * 128);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
+        fence_before_sync();
+        __syncthreads();
+        if (*abort_flag) {
+            aborted = true;
+            break;
+        }
+        // ---- O += P V (thread 0 issues)
+        if (tid == 0) {
+            fence_after_sync();
+            if (!wait_bar(bar(2 + s), (j >> 1) & 1)) {
+                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+                *abort_flag = 1;
+            } else {
+                const uint32_t pa = sbase + kOffP, vb = sbase + kOffV + s * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    const uint64_t bd = smem_desc(vb + kk * 2048, 16384, 1024);
+                    mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc_o, j > 0 || kk > 0);
+                    if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc_o, true);
+                }
+                mma_commit(bar(5));
+                ++o_commits;
+            }
+        }
+        __syncwarp();
+    }
+    if (aborted && tid == 0) {
+        // let the copies and MMAs still in flight finish (bounded) before the
+        // shared memory and TMEM are given up
+        for (int t = issued - 1; t >= 0 && t >= issued - 2; --t) {
+            wait_bar(bar(t & 1), (t >> 1) & 1);
+            wait_bar(bar(2 + (t & 1)), (t >> 1) & 1);
+        }
+        if (s_commits > 0) wait_bar(bar(4), (s_commits - 1) & 1);
+        if (o_commits > 0) wait_bar(bar(5), (o_commits - 1) & 1);
+    }
+    __syncwarp();
+
+    // ---- epilogue: O / l of this thread's row
+    bool ok = !aborted && ntiles > 0;
+    if (ok && !wait_bar(bar(5), (ntiles - 1) & 1)) {
+        atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+        ok = false;
+    }
+    fence_after_sync();
+    if (__any_sync(0xffffffffu, ok)) {  // warp-collective TMEM loads
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        T* orow = my_pos >= 0 || my_tok < L
+                      ? static_cast<T*>(a.out) + ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G +
+                                                  (r - (r / a.G) * a.G)) * kDim
+                      : nullptr;
+#pragma unroll
+        for (int cc = 0; cc < kDim / 32; ++cc) {
+            float v[32];
+            tmem_ld32(tO + lane_base + cc * 32, v);
+            tmem_wait_ld();
+            if (ok && my_tok < L) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 w;
+                    w.x = pack2<T>(v[8 * q] * inv, v[8 * q + 1] * inv);
+                    w.y = pack2<T>(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+                    w.z = pack2<T>(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+                    w.w = pack2<T>(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+                    dst[q] = w;
+                }
+            }
+        }
+    } else if (ntiles == 0 && my_tok < L) {  // every position negative: zeros
+        T* orow = static_cast<T*>(a.out) +
+                  ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + (r - (r / a.G) * a.G)) * kDim;
+        for (int d = 0; d < kDim; ++d) orow[d] = Half16<T>::from_float(0.f);
+    }
+    fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        fence_after_sync();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+    static std::once_flag once;
+    static EncodeTiled fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// The pool [num_blocks * Hkv * 16 rows, 128 dims] as a 2-D tensor; boxes of
+// 16 rows x 64 dims (128 bytes: one swizzle span), 128-byte swizzle.
+bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, bool bf16) {
+    EncodeTiled enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBS)};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+               const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+int launch_t(const CUtensorMap& km, const CUtensorMap& vm, const TcArgs& a, int tiles, int batch, cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(prefill_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr != cudaSuccess) return PKV_ERR_CUDA;
+    prefill_tc_kernel<T><<<dim3(tiles, a.hkv, batch), kThreads, kSmemBytes, st>>>(km, vm, a);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace
+
+bool prefill_tc_applies(int head_dim, int G, int64_t rows) {
+    return head_dim == kDim && (G == 1 || G == 2 || G == 4 || G == 8) && rows > kPrefillTcMinRows;
+}
+
+int launch_prefill_tc(const void* q, const int32_t* q_start, const void* k_pool, const void* v_pool,
+                      const int32_t* tables, const int32_t* ctx_lens, int batch, int hq, int hkv, int num_blocks,
+                      int max_blocks, int max_q_len, float scale, void* out, int* status, bool bf16,
+                      cudaStream_t st) {
+    const int64_t rows = static_cast<int64_t>(num_blocks) * hkv * kBS;
+    if (rows >= (1LL << 31)) return PKV_ERR_UNSUPPORTED;
+    CUtensorMap km, vm;
+    if (!pool_map(&km, k_pool, rows, bf16) || !pool_map(&vm, v_pool, rows, bf16)) return PKV_ERR_CUDA;
+    TcArgs a;
+    a.q = q;
+    a.q_start = q_start;
+    a.tables = tables;
+    a.ctx_lens = ctx_lens;
+    a.hq = hq;
+    a.hkv = hkv;
+    a.G = hq / hkv;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks;
+    a.total_rows = static_cast<int>(rows);
+    a.scale_log2 = scale * kLog2e;
+    a.out = out;
+    a.status = status;
+    const int tpt = kRows / a.G;
+    const int tiles = (max_q_len + tpt - 1) / tpt;
+    return bf16 ? launch_t<__nv_bfloat16>(km, vm, a, tiles, batch, st) : launch_t<__half>(km, vm, a, tiles, batch, st);
+}
+
+}  // namespace pkv

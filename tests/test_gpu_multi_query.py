@@ -223,3 +223,51 @@ def test_balanced_workspace_too_small(pkv, cuda_dev):
         pkv.pkv_paged_attention_multi_query(q, q_start, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"],
                                             torch.empty_like(q), 4, workspace=ws)
     assert e.value.name == "PKV_ERR_WORKSPACE"
+
+
+# ------------------------------------------------------- tensor-core prefill
+# Long query spans (max_q_len x G > 64 at head dim 128) run on the tcgen05
+# kernel: 128 (token, head) rows per CTA, K/V tiles of 128 keys by TMA.
+@pytest.mark.parametrize("hq,hkv,dtype,qlens", [
+    (32, 8, "bf16", [130, 77, 200, 33]),
+    (32, 8, "fp16", [130, 77, 200, 33]),
+    (8, 8, "bf16", [65, 300, 1, 129]),     # G = 1: 128 tokens per tile
+    (16, 8, "fp16", [40, 129, 64, 7]),     # G = 2
+    (64, 8, "bf16", [16, 17, 9, 250]),     # G = 8: 16 tokens per tile
+])
+def test_prefill_tc_groups_dtypes_nan_slots(pkv, cuda_dev, hq, hkv, dtype, qlens):
+    """Contexts 300..900 (several 128-key tiles, the last one partial), slots
+    past each context filled with NaN: those V rows must not reach O."""
+    w = syn.workload("llama3_8b_b64", lens=[900, 511, 640, 301], num_blocks=512, hq=hq, hkv=hkv, d=128,
+                     dtype=dtype)
+    c = build(pkv, w, cuda_dev, empty_fill=float("nan"))
+    q, q_start, got = _run(pkv, c, qlens, seed=hq + len(dtype))
+    assert pkv.pkv_device_status() == 0
+    assert not np.isnan(got).any()
+    _check(c, q, q_start, got, what="tc G %d %s" % (hq // hkv, dtype))
+
+
+def test_prefill_tc_chunk_of_long_prompts(pkv, cuda_dev):
+    """512-token chunked-prefill slices at the end of 4,096-token contexts
+    (the benchmark's shape), two sequences sampled in full."""
+    w = syn.workload("llama3_8b_b64", lens=[4096, 3000, 4096], num_blocks=1024)
+    c = build(pkv, w, cuda_dev)
+    q, q_start, got = _run(pkv, c, [512, 512, 300], seed=31)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, seqs=[0, 2], what="512-token slice")
+
+
+def test_prefill_tc_bad_block_and_short_context(pkv, cuda_dev):
+    w = syn.workload("llama3_8b_b64", lens=[700, 40, 500], num_blocks=256)
+    c = build(pkv, w, cuda_dev)
+    tables = c.tables.clone()
+    tables[2, 3] = 1 << 24
+    c.tables = tables
+    pkv.pkv_device_status()
+    # sequence 1 has 40 tokens but 60 queries: queries 0..19 sit at negative positions
+    q, q_start, got = _run(pkv, c, [100, 60, 80], seed=32)
+    st = pkv.pkv_device_status()
+    assert st & pkv.PKV_STATUS_BAD_BLOCK and st & pkv.PKV_STATUS_BAD_CONTEXT
+    assert not (st & pkv.PKV_STATUS_COPY_TIMEOUT)
+    assert (got[100:120] == 0).all()
+    _check(c, q, q_start, got, seqs=[0], what="intact sequence")
