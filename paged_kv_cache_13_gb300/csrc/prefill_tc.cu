@@ -9,21 +9,26 @@
 // 512-token slice of a prompt attends to the cache before it and causally
 // to itself).
 //
-// Design (one CTA of 4 warps per 128 query rows of one (sequence, KV head);
+// Design (one CTA of 8 warps per 128 query rows of one (sequence, KV head);
 // a row is a (query token, query head) pair, 128 / G tokens per tile):
 // * Q tile [128 rows x 128 dims] bf16/fp16 in shared memory; K and V tiles
 //   of 128 keys (8 pool blocks) in a 2-stage ring, each block's 16 rows
-//   fetched by TMA straight from its physical block (the table is read on
-//   the device; unused or bad blocks are fetched from out of range, which
-//   TMA fills with zeros).
-// * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into TMEM columns
-//   [0, 128); thread r (= TMEM lane r) loads its row of S, applies the
-//   causal mask, runs the online softmax (base 2, the reference max raised
-//   only by more than 8) and writes P to shared memory (bf16: P and its
-//   rounding residual, two operands, so the products see ~16 bits of P).
+//   fetched by TMA straight from its physical block.  The table entries of
+//   a tile are read into shared memory three tiles ahead (unused or bad
+//   blocks become rows past the map's end, which TMA fills with zeros), so
+//   the issuing thread never waits on a table load.
+// * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into one of two
+//   TMEM S buffers (columns [0, 128) and [256, 384)): the next tile's S is
+//   computed while this tile's softmax runs.  Warps w and w + 4 share the
+//   TMEM lanes (rows) 32 (w % 4) .. +31, each taking 64 of the 128 columns:
+//   the thread of row r loads its half row of S, applies the causal mask,
+//   and the two halves exchange their maxima through shared memory for the
+//   online softmax (base 2, the reference max raised only by more than 8).
+//   P goes to shared memory (bf16: P and its rounding residual, two
+//   operands, so the products see ~16 bits of P).
 // * O += P V (M 128, N 128, K 128 keys) into TMEM columns [128, 256); a
 //   rescale of O (when a row's reference max moves) is a TMEM load / store
-//   of that row.  O / l goes out at the end.
+//   of that half row.  O / l goes out at the end.
 // * Every operand tile is a grid of 8-row x 128-byte swizzle atoms (128-byte
 //   swizzle), atom (g, h) -- rows 8g .. 8g+7, columns 64h .. 64h+63 -- at
 //   byte h * 16 KiB + g * 1 KiB of its tile.  K-major operands (Q, K, P)
@@ -51,7 +56,7 @@ constexpr int kKeys = 128;   // keys per tile (MMA N of S, K of O)
 constexpr int kDim = 128;    // head dim
 constexpr int kBS = 16;      // tokens per pool block
 constexpr int kTile = kRows * kDim * 2;  // bytes of one 128 x 128 16-bit tile
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // 8 warps: two per 32-row TMEM lane quarter
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;
@@ -65,7 +70,9 @@ constexpr int kOffK = kOffQ + kTile;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
 constexpr int kOffP = kOffV + 2 * kTile;  // P, then its residual (bf16)
 constexpr int kOffBar = kOffP + 2 * kTile;
-constexpr int kSmemBytes = kOffBar + 128 + 1024;  // barriers, then alignment slack
+constexpr int kOffTab = kOffBar + 128;                // [4][8] TMA rows of the next tiles' blocks
+constexpr int kOffXch = kOffBar + 256;                // [2][128] floats: row values of the two halves
+constexpr int kSmemBytes = kOffXch + 2 * 128 * 4 + 1024;  // then alignment slack
 
 struct TcArgs {
     const void* q;
@@ -202,17 +209,24 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, TcArgs a) {
     constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int kHalf = kKeys / 2;  // columns of S (and O) per thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = sh_addr(sm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-    // bars: 0-1 K full, 2-3 V full, 4 S ready, 5 O ready
+    // bars: 0-1 K full, 2-3 V full, 4-5 S ready (per S buffer), 6 O ready
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
     int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 68);
+    float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2][128]: per-half row values
+    // tab[t % 4][jj]: TMA row of block jj of key tile t (past the map's end:
+    // zeros), read from the table two tiles ahead of its copies
+    int* tab = reinterpret_cast<int*>(sm + kOffTab);
     const uint32_t bar0 = sh_addr(bars);
     auto bar = [&](int i) { return bar0 + 8 * i; };
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    // warp w: TMEM lanes (rows) 32 (w % 4) .. +31, columns 64 (w / 4) .. +63
+    const int r = 32 * (warp & 3) + (tid & 31), hc = warp >> 2;
     const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int q0 = a.q_start[b], L = a.q_start[b + 1] - q0;
     const int tpt = kRows / a.G;  // query tokens per tile
@@ -231,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nblk = (ctx + kBS - 1) / kBS;  // blocks holding context tokens
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -243,109 +257,131 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    // ---- Q tile: thread r writes row r (token tok0 + r / G, head r % G)
+    // ---- Q tile: thread (r, hc) writes columns 64 hc .. +63 of row r
+    const int my_tok = tok0 + r / a.G, my_h = r - (r / a.G) * a.G;
     {
-        const int r = tid;
-        const int tok = tok0 + r / a.G, h = r - (r / a.G) * a.G;
-        const bool valid = tok < L;
+        const bool valid = my_tok < L;
         const uint4* src = valid ? reinterpret_cast<const uint4*>(
                                        static_cast<const T*>(a.q) +
-                                       ((static_cast<int64_t>(q0) + tok) * a.hq + kvh * a.G + h) * kDim)
+                                       ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + my_h) * kDim) +
+                                       hc * 8
                                  : nullptr;
 #pragma unroll
-        for (int ch = 0; ch < kDim / 8; ++ch) {
+        for (int ch = 0; ch < 8; ++ch) {
             const uint4 v = valid ? src[ch] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + kOffQ + tile_off(r, ch * 8)) = v;
+            *reinterpret_cast<uint4*>(sm + kOffQ + tile_off(r, hc * 64 + ch * 8)) = v;
         }
     }
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    // TMA row of logical block lb (a global load of the table)
+    auto block_row = [&](int lb) {
+        int y = a.total_rows;
+        if (lb < nblk) {
+            const int phys = trow[lb];
+            if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks))
+                y = (phys * a.hkv + kvh) * kBS;
+            else
+                atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+        }
+        return y;
+    };
+    if (tid < 24) tab[tid] = block_row(tid);  // tiles 0, 1, 2
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the MMA
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + kKeys;
+    const uint32_t tO = tmem + kKeys;  // S buffers at columns 0 and 256, O at 128
+    auto tS = [&](int s) { return tmem + (s ? 2 * kKeys : 0); };
 
-    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
-    // TMA of key tile j into stage j % 2 (thread 0): 8 blocks x 2 column halves
-    // of 16 rows, K and V; blocks past the context or with a bad id read rows
-    // past the map's end (zeros)
-    int issued = 0, s_commits = 0, o_commits = 0;  // thread 0's async work, for the drain
-    auto issue_tile = [&](int j) {
-        ++issued;
+    // TMA of key tile j's K (or V) into stage j % 2 (thread 0): 8 blocks x 2
+    // column halves of 16 rows; blocks past the context or with a bad id read
+    // rows past the map's end (zeros)
+    int issued_k = 0, issued_v = 0, s_commits[2] = {0, 0}, o_commits = 0;  // thread 0, for the drain
+    auto issue = [&](int j, bool is_v) {
         const int s = j & 1;
-        mbar_arrive_expect_tx(bar(s), kTile);
-        mbar_arrive_expect_tx(bar(2 + s), kTile);
-        for (int jj = 0; jj < kKeys / kBS; ++jj) {
-            const int lb = j * (kKeys / kBS) + jj;
-            int y = a.total_rows;
-            if (lb < nblk) {
-                const int phys = trow[lb];
-                if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks))
-                    y = (phys * a.hkv + kvh) * kBS;
-                else
-                    atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
-            }
+        const uint32_t fb = bar((is_v ? 2 : 0) + s);
+        mbar_arrive_expect_tx(fb, kTile);
+        const uint32_t dst0 = sbase + (is_v ? kOffV : kOffK) + s * kTile;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t off = h * 16384 + jj * 2048;
-                tma_load_2d(sbase + kOffK + s * kTile + off, &kmap, h * 64, y, bar(s));
-                tma_load_2d(sbase + kOffV + s * kTile + off, &vmap, h * 64, y, bar(2 + s));
-            }
+        for (int jj = 0; jj < kKeys / kBS; ++jj) {
+            const int y = tab[(j & 3) * 8 + jj];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                tma_load_2d(dst0 + h * 16384 + jj * 2048, is_v ? &vmap : &kmap, h * 64, y, fb);
         }
+        if (is_v) ++issued_v;
+        else ++issued_k;
+    };
+    const uint32_t idesc_s = instr_desc<T>(false), idesc_o = instr_desc<T>(true);
+    // S(j) = Q K(j)^T into S buffer j % 2 (thread 0)
+    auto mma_s = [&](int j) {
+        const int s = j & 1;
+        if (!wait_bar(bar(s), (j >> 1) & 1)) {
+            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+            *abort_flag = 1;
+            return;
+        }
+        fence_after_sync();
+        const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
+#pragma unroll
+        for (int kk = 0; kk < kDim / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_f16(tS(s), smem_desc(qa + off, 16384, 1024), smem_desc(kb + off, 16384, 1024), idesc_s, kk > 0);
+        }
+        mma_commit(bar(4 + s));
+        ++s_commits[s];
     };
 
-    const uint32_t idesc_s = instr_desc<T>(false), idesc_o = instr_desc<T>(true);
-    const int r = tid;  // this thread's row and TMEM lane
-    const int my_tok = tok0 + r / a.G;
-    const int my_pos = my_tok < L ? first_pos + my_tok : -1;  // -1: padding row, all masked
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    float m = neg_inf(), l = 0.f;
+    const int my_pos = my_tok < L ? first_pos + my_tok : -1;  // padding rows: all masked
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    float m = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
     bool aborted = false;
-    if (tid == 0 && ntiles > 0) issue_tile(0);
+    if (tid == 0 && ntiles > 0) {
+        issue(0, false);
+        issue(0, true);
+        if (ntiles > 1) issue(1, false);
+        mma_s(0);
+    }
+    __syncwarp();
 
     for (int j = 0; j < ntiles; ++j) {
         const int s = j & 1;
-        // ---- S = Q K^T (thread 0 issues)
-        if (tid == 0) {
-            if (!wait_bar(bar(s), (j >> 1) & 1)) {
-                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-                *abort_flag = 1;
-            } else {
-                fence_after_sync();
-                const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
-#pragma unroll
-                for (int kk = 0; kk < kDim / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_f16(tS, smem_desc(qa + off, 16384, 1024), smem_desc(kb + off, 16384, 1024), idesc_s,
-                            kk > 0);
-                }
-                mma_commit(bar(4));
-                ++s_commits;
-            }
-        }
+        // ---- the next tile's S = Q K^T, overlapping this tile's softmax; its
+        // S buffer was last read by the softmax of tile j - 1
+        if (tid == 0 && j + 1 < ntiles) mma_s(j + 1);
         __syncwarp();
-        // ---- softmax of this thread's row
-        if (!wait_bar(bar(4), j & 1)) {
+        // the table entries of tile j + 3 (stored before the barrier below;
+        // tile j - 1's slot was last read two iterations ago)
+        int ahead = 0;
+        if (warp == 1 && (tid & 31) < 8) ahead = block_row((j + 3) * 8 + (tid & 31));
+        // ---- this thread's half row of S(j), masked and scaled (base 2)
+        if (!wait_bar(bar(4 + s), (j >> 1) & 1)) {
             atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
             *abort_flag = 1;
         }
         fence_after_sync();
-        float x[kKeys];
+        float x[kHalf];
 #pragma unroll
-        for (int cc = 0; cc < kKeys / 32; ++cc) {
+        for (int cc = 0; cc < kHalf / 32; ++cc) {
             float v[32];
-            tmem_ld32(tS + lane_base + cc * 32, v);
+            tmem_ld32(tS(s) + lane_base + hc * kHalf + cc * 32, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
         }
         tmem_wait_ld();
-        const int key0 = j * kKeys;
+        const int key0 = j * kKeys + hc * kHalf;
         float mx = neg_inf();
 #pragma unroll
-        for (int i = 0; i < kKeys; ++i) {
+        for (int i = 0; i < kHalf; ++i) {
             x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
             mx = fmaxf(mx, x[i]);
         }
+        // the row max over both halves
+        xch[hc * kRows + r] = mx;
+        if (warp == 1 && (tid & 31) < 8) tab[((j + 3) & 3) * 8 + (tid & 31)] = ahead;
+        __syncthreads();
+        mx = fmaxf(mx, xch[(1 - hc) * kRows + r]);
         const bool raise = mx > m + kSlack;
         float alpha = 1.f;
         if (raise) {
@@ -354,67 +390,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
         }
         // the previous tile's O += P V must be done before P and O are touched
-        if (j > 0 && !wait_bar(bar(5), (j - 1) & 1)) {
+        if (j > 0 && !wait_bar(bar(6), (j - 1) & 1)) {
             atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
             *abort_flag = 1;
         }
         fence_after_sync();
-        if (tid == 0 && j + 1 < ntiles) issue_tile(j + 1);  // stage (j + 1) % 2 is free now
+        if (tid == 0) {
+            // stages freed: V of tile j - 1 (its O += P V is done), K of tile
+            // j (its S was read above)
+            if (j + 1 < ntiles) issue(j + 1, true);
+            if (j + 2 < ntiles) issue(j + 2, false);
+        }
         __syncwarp();
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
-            for (int cc = 0; cc < kDim / 32; ++cc) {
+            for (int cc = 0; cc < kHalf / 32; ++cc) {
                 float v[32];
-                tmem_ld32(tO + lane_base + cc * 32, v);
+                tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tmem_st32(tO + lane_base + cc * 32, v);
+                tmem_st32(tO + lane_base + hc * kHalf + cc * 32, v);
             }
             tmem_wait_st();
         }
         const float mref = m == neg_inf() ? 0.f : m;
         float sum = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < kKeys / 8; ++ch) {
+        for (int ch = 0; ch < kHalf / 8; ++ch) {
             float p[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 p[i] = ex2(x[ch * 8 + i] - mref);
                 sum += p[i];
             }
-            uint4 hi, lo;
+            uint4 hi;
             hi.x = pack2<T>(p[0], p[1]);
             hi.y = pack2<T>(p[2], p[3]);
             hi.z = pack2<T>(p[4], p[5]);
             hi.w = pack2<T>(p[6], p[7]);
-            *reinterpret_cast<uint4*>(sm + kOffP + tile_off(r, ch * 8)) = hi;
+            const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
+            *reinterpret_cast<uint4*>(sm + kOffP + off) = hi;
             if constexpr (kSplit) {
                 auto res = [](uint32_t w, float a0, float a1) {
                     return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
                 };
+                uint4 lo;
                 lo.x = res(hi.x, p[0], p[1]);
                 lo.y = res(hi.y, p[2], p[3]);
                 lo.z = res(hi.z, p[4], p[5]);
                 lo.w = res(hi.w, p[6], p[7]);
-                *reinterpret_cast<uint4*>(sm + kOffP + kTile + tile_off(r, ch * 8)) = lo;
+                *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = lo;
             }
         }
         l += sum;
         // keys past the context in this tile: their V rows may hold any bits
         // (0 x NaN would poison O); zero them once the tile has landed
-        if (key0 + kKeys > ctx) {
+        if (j * kKeys + kKeys > ctx) {
             if (!wait_bar(bar(2 + s), (j >> 1) & 1)) {
                 atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
                 *abort_flag = 1;
-            } else if (key0 + r >= ctx) {
+            } else if (j * kKeys + r >= ctx) {
+                uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + hc * 16384 + (r >> 3) * 1024 +
+                                                      (r & 7) * 128);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + h * 16384 + (r >> 3) * 1024 +
-                                                          (r & 7) * 128);
-#pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
-                }
+                for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
@@ -439,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc_o, j > 0 || kk > 0);
                     if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc_o, true);
                 }
-                mma_commit(bar(5));
+                mma_commit(bar(6));
                 ++o_commits;
             }
         }
@@ -448,35 +488,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (aborted && tid == 0) {
         // let the copies and MMAs still in flight finish (bounded) before the
         // shared memory and TMEM are given up
-        for (int t = issued - 1; t >= 0 && t >= issued - 2; --t) {
-            wait_bar(bar(t & 1), (t >> 1) & 1);
-            wait_bar(bar(2 + (t & 1)), (t >> 1) & 1);
-        }
-        if (s_commits > 0) wait_bar(bar(4), (s_commits - 1) & 1);
-        if (o_commits > 0) wait_bar(bar(5), (o_commits - 1) & 1);
+        for (int t = issued_k - 1; t >= 0 && t >= issued_k - 2; --t) wait_bar(bar(t & 1), (t >> 1) & 1);
+        for (int t = issued_v - 1; t >= 0 && t >= issued_v - 2; --t) wait_bar(bar(2 + (t & 1)), (t >> 1) & 1);
+        for (int s = 0; s < 2; ++s)
+            if (s_commits[s] > 0) wait_bar(bar(4 + s), (s_commits[s] - 1) & 1);
+        if (o_commits > 0) wait_bar(bar(6), (o_commits - 1) & 1);
     }
     __syncwarp();
 
-    // ---- epilogue: O / l of this thread's row
+    // ---- epilogue: O / l for this thread's half row (l summed over halves)
+    xch[hc * kRows + r] = l;
+    __syncthreads();
+    l += xch[(1 - hc) * kRows + r];
     bool ok = !aborted && ntiles > 0;
-    if (ok && !wait_bar(bar(5), (ntiles - 1) & 1)) {
+    if (ok && !wait_bar(bar(6), (ntiles - 1) & 1)) {
         atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
         ok = false;
     }
     fence_after_sync();
+    T* orow = static_cast<T*>(a.out) + ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + my_h) * kDim;
     if (__any_sync(0xffffffffu, ok)) {  // warp-collective TMEM loads
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        T* orow = my_pos >= 0 || my_tok < L
-                      ? static_cast<T*>(a.out) + ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G +
-                                                  (r - (r / a.G) * a.G)) * kDim
-                      : nullptr;
 #pragma unroll
-        for (int cc = 0; cc < kDim / 32; ++cc) {
+        for (int cc = 0; cc < kHalf / 32; ++cc) {
             float v[32];
-            tmem_ld32(tO + lane_base + cc * 32, v);
+            tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
             tmem_wait_ld();
             if (ok && my_tok < L) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                uint4* dst = reinterpret_cast<uint4*>(orow + hc * kHalf + cc * 32);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint4 w;
@@ -489,9 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (ntiles == 0 && my_tok < L) {  // every position negative: zeros
-        T* orow = static_cast<T*>(a.out) +
-                  ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + (r - (r / a.G) * a.G)) * kDim;
-        for (int d = 0; d < kDim; ++d) orow[d] = Half16<T>::from_float(0.f);
+        for (int d = hc * kHalf; d < hc * kHalf + kHalf; ++d) orow[d] = Half16<T>::from_float(0.f);
     }
     fence_before_sync();
     __syncthreads();
