@@ -649,22 +649,24 @@ __global__ void __launch_bounds__(kMQWarps * 32, kMQCtas<NT>)
     }
 }
 
-// Merge of a balanced multi-query split: one CTA of D threads per (sequence,
-// KV head, row); the partials of the consecutive warps whose ranges met the
-// (sequence, KV head) run, folded with a log-sum-exp rescale.  Where the run
-// sits among the items follows from the context lengths alone (inputs of the
-// call), so it is worked out before the wait on the split grid.
+// Merge of a balanced multi-query split: one CTA of kMergeThreads threads
+// per (sequence, KV head) folds the partials of all its rows: for each (row,
+// column), the partials of the consecutive warps whose ranges met the run,
+// with a log-sum-exp rescale.  Where the run sits among the items follows
+// from the context lengths alone (inputs of the call), so it is worked out
+// before the wait on the split grid.
+constexpr int kMergeThreads = 256;
+
 template <typename T, int D, int NT>
-__global__ void __launch_bounds__(D) multi_query_merge_kernel(
+__global__ void __launch_bounds__(kMergeThreads) multi_query_merge_kernel(
     const int32_t* __restrict__ q_start, const int32_t* __restrict__ ctx_lens, int batch, int hq, int hkv,
     int cap, int nwt_launch, const float* __restrict__ ws_o, const float* __restrict__ ws_ml, T* __restrict__ out) {
-    constexpr int R = 8 * NT, NWARP = D / 32;
-    const int x = blockIdx.x, b = blockIdx.y;
-    const int kvh = x / R, r = x - kvh * R;
-    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    constexpr int R = 8 * NT, NWARP = kMergeThreads / 32;
+    const int kvh = blockIdx.x, b = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = hq / hkv;
     int before = 0, total = 0;
-    for (int j = d; j < batch; j += D) {
+    for (int j = tid; j < batch; j += kMergeThreads) {
         const int nbj = blocks_of(ctx_lens[j], cap);
         total += nbj;
         before += j < b ? nbj : 0;
@@ -688,24 +690,31 @@ __global__ void __launch_bounds__(D) multi_query_merge_kernel(
     }
     const int q0 = q_start[b], L = q_start[b + 1] - q0;
     const int rows = L > 0 ? (L * G < R ? L * G : R) : 0;
-    if (r >= rows) return;
+    if (rows == 0) return;
     const int nb = blocks_of(ctx_lens[b], cap);
-    const int tok = r / G, h = r - tok * G;
-    T* o = out + ((static_cast<int64_t>(q0) + tok) * hq + kvh * G + h) * D + d;
-    // partials are produced by the preceding grid: wait for it
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (nb == 0) {
-        *o = Half16<T>::from_float(0.f);
-        return;
-    }
     const int W = total * hkv;
     const int nwt = max(min(W / kBalancedMinItems, nwt_launch), 1);
     const int S = before * hkv + kvh * nb;
-    const int64_t i0 = first_warp(S, W, nwt), i1 = first_warp(S + nb - 1, W, nwt);
-    const int64_t slot0 = i0 + static_cast<int64_t>(b) * hkv + kvh;
-    const MergeAcc m = merge_range(ws_ml + (slot0 * R + r) * 2, 2 * R, ws_o + (slot0 * R + r) * D + d,
-                                   static_cast<int64_t>(R) * D, 0, static_cast<int>(i1 - i0 + 1), 1);
-    *o = Half16<T>::from_float(m.L > 0.f ? m.acc / m.L : 0.f);
+    int64_t slot0 = 0;
+    int np = 0;
+    if (nb > 0) {
+        const int64_t i0 = first_warp(S, W, nwt), i1 = first_warp(S + nb - 1, W, nwt);
+        slot0 = i0 + static_cast<int64_t>(b) * hkv + kvh;
+        np = static_cast<int>(i1 - i0 + 1);
+    }
+    // partials are produced by the preceding grid: wait for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int x = tid; x < rows * D; x += kMergeThreads) {
+        const int r = x / D, d = x - r * D;
+        const int tok = r / G, h = r - tok * G;
+        float v = 0.f;
+        if (np > 0) {
+            const MergeAcc m = merge_range(ws_ml + (slot0 * R + r) * 2, 2 * R, ws_o + (slot0 * R + r) * D + d,
+                                           static_cast<int64_t>(R) * D, 0, np, 1);
+            v = m.L > 0.f ? m.acc / m.L : 0.f;
+        }
+        out[((static_cast<int64_t>(q0) + tok) * hq + kvh * G + h) * D + d] = Half16<T>::from_float(v);
+    }
 }
 
 // Warps the balanced multi-query split launches for NT n-tiles.
@@ -736,8 +745,8 @@ int run_mq_balanced(const MQArgs& a, int batch, int nwt, float* ws_o, float* ws_
         <<<(nwt + kMQWarps - 1) / kMQWarps, kMQWarps * 32, 0, st>>>(a, batch, nwt, ws_o, ws_ml);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.hkv * 8 * NT, batch);
-    cfg.blockDim = dim3(D);
+    cfg.gridDim = dim3(a.hkv, batch);
+    cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
