@@ -60,6 +60,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Headroom (log2 units) a logit may rise above the running reference max
 // before the online softmax rescales: weights stay <= 2^8 (fp16-safe).
 constexpr float kSlack = 8.f;
+// Largest V scale for which a weight of 2^kSlack keeps W = P s well inside
+// fp16 (65,504): blocks with a larger one take the exact max.
+constexpr float kLazyMaxScale = 128.f;
 
 struct QDecodeArgs {
     const void* q;
@@ -446,8 +449,14 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
         // when a logit of the block exceeds it by more than kSlack; otherwise
         // the weights 2^(x - m) <= 2^kSlack are taken against the old m, with
         // no warp-wide max and no rescale (m cancels in o / l and the merges).
+        // A block whose V scales could carry W = P s past the fp16 range at
+        // P = 2^kSlack takes the exact max (then P <= 1, W <= s).
         const float bx0 = fmaxf(x0, x2), bx1 = fmaxf(x1, x3);
-        if (__any_sync(0xffffffffu, bx0 > m0 + kSlack || bx1 > m1 + kSlack)) {
+        float vsmax = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            vsmax = fmaxf(vsmax, fmaxf(__low2float(B.vs[gi]), __high2float(B.vs[gi])));
+        if (__any_sync(0xffffffffu, bx0 > m0 + kSlack || bx1 > m1 + kSlack || vsmax > kLazyMaxScale)) {
             float bm0 = bx0, bm1 = bx1;
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {

@@ -226,3 +226,16 @@ def test_pages_layout_full_size_sampled(pkv, cuda_dev):
     got = _decode_quant(pkv, c, 0)
     sample = [0, 9, 31]
     assert_close(got[sample], expected(c, sample), what="BIE layout full size")
+
+
+@pytest.mark.parametrize("qmode,mag", [("int4", 4000.0), ("fp8", 60000.0)])
+def test_large_value_scales_take_the_exact_max(pkv, cuda_dev, qmode, mag):
+    """Outliers large enough that a token's V scale exceeds 128 (INT4: a
+    range of +-4,000; FP8: an amax of 60,000): the blocks holding them take
+    the exact softmax max (weights <= 1), so W = P s stays inside fp16."""
+    w = syn.workload("quant", batch=4, ctx=700, num_blocks=256, outlier_frac=0.02, outlier_mag=mag)
+    c = build(pkv, w, cuda_dev, quant=qmode)
+    want = expected(c)
+    got = _decode_quant(pkv, c)
+    assert np.isfinite(got).all()
+    assert_close(got, want, what="%s outliers +-%g" % (qmode, mag))
