@@ -504,12 +504,54 @@ def run_device(args, rank, world, dist):
     # ---------- end to end through the public API, host buffers
     e2e = run_e2e(pkv, torch, cache, e2e_steps, dist, device)
     prefix = prefix_cache_timing(pkv, cache) if "prompt" in cache.w else None
+    append = append_timing(pkv, torch, cache)
 
     return dict(ms_per_step=ms_per_step, call_ms=call_ms, kv_bytes=kv_bytes, clocks=clk, e2e=e2e,
-                prefix=prefix,
+                prefix=prefix, append=append,
                 B=cache.B, launches=cache.launches_per_step() * args.steps,
                 unique_blocks=cache.unique_blocks, partition_size=cache.partition_size,
                 split_desc=cache.split_desc)
+
+
+def append_timing(pkv, torch, cache, iters=200):
+    """The decode step's KV-append alone (the step itself fuses it into the
+    decode for the 16-bit cache): the step's B new K/V rows written to their
+    slots.  The calls are tiny, so back-to-back launches from Python would
+    time the host; `iters` calls are captured in one CUDA graph and its
+    replay is timed with CUDA events (after a warm-up replay)."""
+    def one():
+        if cache.qmode is None:
+            pkv.pkv_kv_append(cache.new_k, cache.new_v, cache.slots, cache.k_pool, cache.v_pool)
+        else:
+            pkv.pkv_kv_append_quant(cache.new_k, cache.new_v, cache.slots, cache.positions, cache.seq_idx,
+                                    cache.cache, cache.n_sink, cache.qmode, cache.group_size,
+                                    window=cache.window)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            one()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(iters):
+            one()
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / iters
+    row_bytes = cache.w["hkv"] * cache.w["d"] * 2 * 2  # K and V rows in, 16-bit
+    return {"kernel": "kv_append_kernel" if cache.qmode is None else "kv_append_quant_kernel",
+            "rows": cache.B, "us_per_call": round(us, 2), "input_bytes": cache.B * row_bytes,
+            "timing": "%d calls in one CUDA graph replay, CUDA events" % iters,
+            "note": "timed alone; the 16-bit step fuses it into the decode kernel"
+            if cache.qmode is None else "timed alone; part of each quantised step"}
 
 
 def run_mq(args, rank, world, dist):
@@ -990,6 +1032,8 @@ def main():
         line["unique_kv_bytes_per_step"] = res["unique_blocks"] * 16 * KV_BYTES_PER_TOKEN
     if res.get("prefix"):
         line["prefix_cache"] = res["prefix"]
+    if res.get("append"):
+        line["append"] = res["append"]
     print(json.dumps(line))
 
 
