@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA of key tile j's K (or V) into stage j % 2 (thread 0): 8 blocks x 2
     // column halves of 16 rows; blocks past the context or with a bad id read
     // rows past the map's end (zeros)
-    int issued_k = 0, issued_v = 0, s_commits[2] = {0, 0}, o_commits = 0;  // thread 0, for the drain
+    int issued_k = 0, issued_v = 0, s_commits[2] = {0, 0}, o_commits = 0;  // for the drain (thread 0)
     auto issue = [&](int j, bool is_v) {
         const int s = j & 1;
         const uint32_t fb = bar((is_v ? 2 : 0) + s);
@@ -370,13 +370,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
         }
         tmem_wait_ld();
+        // A tile wholly at or below the CTA's first query position needs no
+        // causal mask (padding rows there see zero queries: finite scores,
+        // outputs never written).  With a positive scale the max is taken
+        // over raw scores and the scale enters the exponent's FMA (mul);
+        // otherwise the scores are scaled first.
         const int key0 = j * kKeys + hc * kHalf;
+        const bool interior = j * kKeys + kKeys - 1 <= first_pos + tok0;
+        const float mul = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
+        if (a.scale_log2 > 0.f) {
+            if (!interior) {
+#pragma unroll
+                for (int i = 0; i < kHalf; ++i)
+                    if (key0 + i > my_pos) x[i] = neg_inf();
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kHalf; ++i) x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
+        }
         float mx = neg_inf();
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) {
-            x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
-            mx = fmaxf(mx, x[i]);
-        }
+        for (int i = 0; i < kHalf; ++i) mx = fmaxf(mx, x[i]);
+        mx *= mul;
         // the row max over both halves
         xch[hc * kRows + r] = mx;
         if (warp == 1 && (tid & 31) < 8) tab[((j + 3) & 3) * 8 + (tid & 31)] = ahead;
@@ -395,13 +410,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
         }
         fence_after_sync();
-        if (tid == 0) {
+        if (warp == 1) {
             // stages freed: V of tile j - 1 (its O += P V is done), K of tile
-            // j (its S was read above)
-            if (j + 1 < ntiles) issue(j + 1, true);
-            if (j + 2 < ntiles) issue(j + 2, false);
+            // j (its S was read above).  One copy per lane: lanes 0-15 the 16
+            // of K tile j + 2, lanes 16-31 the 16 of V tile j + 1
+            const int ln = tid & 31;
+            const bool is_v = ln >= 16;
+            const int jt = is_v ? j + 1 : j + 2;
+            if (jt < ntiles) {
+                const int st = jt & 1;
+                const uint32_t fb = bar((is_v ? 2 : 0) + st);
+                if ((ln & 15) == 0) mbar_arrive_expect_tx(fb, kTile);
+                const int jj = (ln & 15) >> 1, h = ln & 1;
+                tma_load_2d(sbase + (is_v ? kOffV : kOffK) + st * kTile + h * 16384 + jj * 2048, is_v ? &vmap : &kmap,
+                            h * 64, tab[(jt & 3) * 8 + jj], fb);
+            }
         }
-        __syncwarp();
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
             for (int cc = 0; cc < kHalf / 32; ++cc) {
@@ -421,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float p[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                p[i] = ex2(x[ch * 8 + i] - mref);
+                p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
                 sum += p[i];
             }
             uint4 hi;
@@ -462,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         if (*abort_flag) {
             aborted = true;
+            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1
+            issued_k = min(ntiles, j + 3);
+            issued_v = min(ntiles, j + 2);
             break;
         }
         // ---- O += P V (thread 0 issues)
