@@ -35,8 +35,9 @@
 //   step 32 bytes per K-16 slice inside an atom row (and 16 KiB to the
 //   second column half); V is the MN-major B operand of O += P V (its 8-key
 //   atom groups 1 KiB apart, its two 64-dim halves 16 KiB apart).
-// * One thread issues the TMA loads and the MMAs; completion is tracked by
-//   mbarriers (tcgen05.commit arrives on them).  Every wait is bounded: one
+// * One thread of warp 4 issues the S MMAs, thread 0 the O MMAs, the lanes
+//   of warp 1 the TMA copies of a tile (one copy each); completion is
+//   tracked by mbarriers (tcgen05.commit arrives on them).  Every wait is bounded: one
 //   that runs out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together
 //   (the flag is read after a barrier), still freeing its TMEM.
 
@@ -57,6 +58,7 @@ constexpr int kDim = 128;    // head dim
 constexpr int kBS = 16;      // tokens per pool block
 constexpr int kTile = kRows * kDim * 2;  // bytes of one 128 x 128 16-bit tile
 constexpr int kThreads = 256;  // 8 warps: two per 32-row TMEM lane quarter
+constexpr int kSIssuer = 128;  // thread issuing S = Q K^T (warp 4); thread 0 issues O += P V
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;
@@ -341,15 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue(0, false);
         issue(0, true);
         if (ntiles > 1) issue(1, false);
-        mma_s(0);
     }
+    if (tid == kSIssuer && ntiles > 0) mma_s(0);
     __syncwarp();
 
     for (int j = 0; j < ntiles; ++j) {
         const int s = j & 1;
         // ---- the next tile's S = Q K^T, overlapping this tile's softmax; its
         // S buffer was last read by the softmax of tile j - 1
-        if (tid == 0 && j + 1 < ntiles) mma_s(j + 1);
+        if (tid == kSIssuer && j + 1 < ntiles) mma_s(j + 1);
         __syncwarp();
         // the table entries of tile j + 3 (stored before the barrier below;
         // tile j - 1's slot was last read two iterations ago)
@@ -517,9 +519,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // shared memory and TMEM are given up
         for (int t = issued_k - 1; t >= 0 && t >= issued_k - 2; --t) wait_bar(bar(t & 1), (t >> 1) & 1);
         for (int t = issued_v - 1; t >= 0 && t >= issued_v - 2; --t) wait_bar(bar(2 + (t & 1)), (t >> 1) & 1);
+        if (o_commits > 0) wait_bar(bar(6), (o_commits - 1) & 1);
+    }
+    if (aborted && tid == kSIssuer) {
         for (int s = 0; s < 2; ++s)
             if (s_commits[s] > 0) wait_bar(bar(4 + s), (s_commits[s] - 1) & 1);
-        if (o_commits > 0) wait_bar(bar(6), (o_commits - 1) & 1);
     }
     __syncwarp();
 
