@@ -21,9 +21,11 @@
 //   TMEM S buffers (columns [0, 128) and [256, 384)): the next tile's S is
 //   computed while this tile's softmax runs.  Warps w and w + 4 share the
 //   TMEM lanes (rows) 32 (w % 4) .. +31, each taking 64 of the 128 columns:
-//   the thread of row r loads its half row of S, applies the causal mask,
-//   and the two halves exchange their maxima through shared memory for the
-//   online softmax (base 2, the reference max raised only by more than 8).
+//   the thread of row r loads its half row of S, applies the causal mask
+//   (only on tiles that reach past the CTA's first query position), and the
+//   two halves exchange their maxima through shared memory under a barrier
+//   of just those two warps, for the online softmax (base 2, the reference
+//   max raised only by more than 8).
 //   P goes to shared memory (bf16: P and its rounding residual, two
 //   operands, so the products see ~16 bits of P).
 // * O += P V (M 128, N 128, K 128 keys) into TMEM columns [128, 256); a
@@ -191,6 +193,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// max of three floats (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// named barrier of the 64 threads of warps w and w + 4 (id 1 .. 4)
+__device__ __forceinline__ void pair_sync(int id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -390,14 +404,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < kHalf; ++i) x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
         }
-        float mx = neg_inf();
+        // the half row's max: three-input max, four independent chains
+        float mq[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) mx = fmaxf(mx, x[i]);
-        mx *= mul;
+        for (int i = 4; i < kHalf; i += 8) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) mq[u] = max3f(mq[u], x[i + u], x[i + 4 + u < kHalf ? i + 4 + u : i + u]);
+        }
+        float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * mul;
         // the row max over both halves
         xch[hc * kRows + r] = mx;
         if (warp == 1 && (tid & 31) < 8) tab[((j + 3) & 3) * 8 + (tid & 31)] = ahead;
-        __syncthreads();
+        // only warps w and w + 4 (the two halves of the same rows) meet here
+        pair_sync(1 + (warp & 3));
         mx = fmaxf(mx, xch[(1 - hc) * kRows + r]);
         const bool raise = mx > m + kSlack;
         float alpha = 1.f;
