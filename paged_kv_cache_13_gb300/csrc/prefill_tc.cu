@@ -504,8 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
         fence_before_sync();
-        __syncthreads();
-        if (*abort_flag) {
+        // the stop decision is the barrier's own OR of every thread's view of
+        // the flag, so that all threads take it alike even when thread 0 sets
+        // the flag just after the barrier
+        if (__syncthreads_or(*reinterpret_cast<volatile int*>(abort_flag))) {
             aborted = true;
             // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1
             issued_k = min(ntiles, j + 3);
