@@ -64,9 +64,9 @@ constexpr int kSIssuer = 128;  // thread issuing S = Q K^T (warp 4); thread 0 is
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;
-// polls of an mbarrier before a wait gives up: non-blocking tests 32-64 ns
-// apart, so a wait that will never complete ends within ~0.3 s
-constexpr int kSpin = 1 << 22;
+// time after which an mbarrier wait gives up (ns): a wait that will never
+// complete ends within ~0.3 s
+constexpr uint64_t kWaitNs = 300000000ull;
 
 // shared-memory map (bytes from the 1 KiB-aligned base)
 constexpr int kOffQ = 0;
@@ -103,22 +103,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Waits for the barrier's phase of the given parity; false if it has not
-// completed after kSpin polls.
+// completed within kWaitNs.  try_wait suspends the thread in hardware until
+// the phase completes or a short system time limit passes, so a waiting
+// warp takes no issue slots from the warps still working.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
-    for (int it = 0; it < kSpin; ++it) {
+    uint64_t t0 = 0;
+    for (int it = 0;; ++it) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
-        if (it >= 64) __nanosleep(32);
+        if (it == 0) t0 = global_ns();
+        else if (global_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
