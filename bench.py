@@ -592,8 +592,15 @@ def run_mq(args, rank, world, dist):
     # the balanced split where it applies (a workspace of the size it asks for)
     ws_n = pkv.pkv_multi_query_workspace_bytes(B, Hq, Hkv, D, cache.max_blocks, L)
     mq_ws = torch.empty(ws_n, dtype=torch.uint8, device=device) if ws_n else None
-    mq_kernels = ("multi_query_balanced_kernel<bf16, 128, %d> + multi_query_merge_kernel" % (-(-L * Hq // Hkv // 8))
-                  if ws_n else "multi_query_kernel<bf16, 128, %d> (mma.sync)" % (1 if L * Hq // Hkv <= 8 else 2))
+    # the kernel the library picks: the balanced split (workspace), else the
+    # tcgen05 kernel for long spans at head dim 128, else the one-pass tiles
+    G = Hq // Hkv
+    if ws_n:
+        mq_kernels = "multi_query_balanced_kernel<bf16, 128, %d> + multi_query_merge_kernel" % (-(-L * G // 8))
+    elif D == 128 and G in (1, 2, 4, 8) and L * G > 64:
+        mq_kernels = "prefill_tc_kernel<bf16> (tcgen05 + TMA)"
+    else:
+        mq_kernels = "multi_query_kernel<bf16, %d, %d> (mma.sync)" % (D, 1 if L * G <= 8 else 2)
 
     def step(qq=q, oo=out):
         pkv.pkv_kv_append(mq_k, mq_v, mq_slots, cache.k_pool, cache.v_pool)
