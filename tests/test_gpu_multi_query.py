@@ -271,3 +271,17 @@ def test_prefill_tc_bad_block_and_short_context(pkv, cuda_dev):
     assert not (st & pkv.PKV_STATUS_COPY_TIMEOUT)
     assert (got[100:120] == 0).all()
     _check(c, q, q_start, got, seqs=[0], what="intact sequence")
+
+
+@pytest.mark.parametrize("scale", [-0.0884, 0.0])
+def test_prefill_tc_non_positive_scale(pkv, cuda_dev, scale):
+    """A scale <= 0 takes the kernel's path that scales the scores before the
+    max (with a positive scale the max is taken over raw scores): softmax of
+    -|s| q.k, and at 0 the plain mean of V up to each query's position."""
+    w = syn.workload("llama3_8b_b64", lens=[900, 640], num_blocks=256, hq=32, hkv=8, d=128, dtype="bf16",
+                     scale=scale)
+    c = build(pkv, w, cuda_dev, empty_fill=float("nan"))
+    q, q_start, got = _run(pkv, c, [130, 200], seed=41)
+    assert pkv.pkv_device_status() == 0
+    assert not np.isnan(got).any()
+    _check(c, q, q_start, got, what="tc scale %g" % scale)
