@@ -16,7 +16,7 @@
 //   fetched by TMA straight from its physical block.  The table entries of
 //   a tile are read into shared memory three tiles ahead (unused or bad
 //   blocks become rows past the map's end, which TMA fills with zeros), so
-//   the issuing thread never waits on a table load.
+//   the issuing lanes never wait on a table load.
 // * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into one of two
 //   TMEM S buffers (columns [0, 128) and [256, 384)): the next tile's S is
 //   computed while this tile's softmax runs.  Warps w and w + 4 share the
@@ -39,9 +39,10 @@
 //   atom groups 1 KiB apart, its two 64-dim halves 16 KiB apart).
 // * One thread of warp 4 issues the S MMAs, thread 0 the O MMAs, the lanes
 //   of warp 1 the TMA copies of a tile (one copy each); completion is
-//   tracked by mbarriers (tcgen05.commit arrives on them).  Every wait is bounded: one
-//   that runs out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together
-//   (the flag is read after a barrier), still freeing its TMEM.
+//   tracked by mbarriers (tcgen05.commit arrives on them).  Every wait
+//   suspends in hardware (try_wait) and is bounded in time: one that runs
+//   out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together (the
+//   decision is the OR the CTA barrier returns), still freeing its TMEM.
 
 #include <cuda.h>
 
