@@ -554,6 +554,18 @@ def append_timing(pkv, torch, cache, iters=200):
             if cache.qmode is None else "timed alone; part of each quantised step"}
 
 
+def mq_kernel_name(balanced, D, G, L):
+    """The kernel(s) pkv_paged_attention_multi_query runs for L queries per
+    sequence: the balanced split (when a workspace is given and it applies),
+    else the tcgen05 kernel for long spans at head dim 128 (more than 64
+    (token, head) rows per (sequence, KV head)), else the one-pass tiles."""
+    if balanced:
+        return "multi_query_balanced_kernel<bf16, %d, %d> + multi_query_merge_kernel" % (D, -(-L * G // 8))
+    if D == 128 and G in (1, 2, 4, 8) and L * G > 64:
+        return "prefill_tc_kernel<bf16> (tcgen05 + TMA)"
+    return "multi_query_kernel<bf16, %d, %d> (mma.sync)" % (D, 1 if L * G <= 8 else 2)
+
+
 def run_mq(args, rank, world, dist):
     """Multi-query workloads: every step rewrites the L new tokens' K/V rows
     of every sequence (pkv_kv_append) and runs pkv_paged_attention_multi_query
@@ -592,15 +604,7 @@ def run_mq(args, rank, world, dist):
     # the balanced split where it applies (a workspace of the size it asks for)
     ws_n = pkv.pkv_multi_query_workspace_bytes(B, Hq, Hkv, D, cache.max_blocks, L)
     mq_ws = torch.empty(ws_n, dtype=torch.uint8, device=device) if ws_n else None
-    # the kernel the library picks: the balanced split (workspace), else the
-    # tcgen05 kernel for long spans at head dim 128, else the one-pass tiles
-    G = Hq // Hkv
-    if ws_n:
-        mq_kernels = "multi_query_balanced_kernel<bf16, 128, %d> + multi_query_merge_kernel" % (-(-L * G // 8))
-    elif D == 128 and G in (1, 2, 4, 8) and L * G > 64:
-        mq_kernels = "prefill_tc_kernel<bf16> (tcgen05 + TMA)"
-    else:
-        mq_kernels = "multi_query_kernel<bf16, %d, %d> (mma.sync)" % (D, 1 if L * G <= 8 else 2)
+    mq_kernels = mq_kernel_name(bool(ws_n), D, Hq // Hkv, L)
 
     def step(qq=q, oo=out):
         pkv.pkv_kv_append(mq_k, mq_v, mq_slots, cache.k_pool, cache.v_pool)

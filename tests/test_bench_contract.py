@@ -42,3 +42,17 @@ def test_reference_arm_other_ranks_exit_without_output():
     r = _run(RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_multi_query_kernel_names_follow_the_dispatch():
+    sys.path.insert(0, ROOT)
+    import bench
+    # verify (6 queries x G 4 = 24 rows): the balanced split with 3 row tiles
+    assert bench.mq_kernel_name(True, 128, 4, 6).startswith("multi_query_balanced_kernel<bf16, 128, 3>")
+    # a 512-token slice at head dim 128: the tcgen05 kernel
+    assert bench.mq_kernel_name(False, 128, 4, 512).startswith("prefill_tc_kernel")
+    # 64 rows or fewer, head dim 64 or G outside {1, 2, 4, 8}: the one-pass tiles
+    assert bench.mq_kernel_name(False, 128, 4, 16) == "multi_query_kernel<bf16, 128, 2> (mma.sync)"
+    assert bench.mq_kernel_name(False, 64, 4, 512) == "multi_query_kernel<bf16, 64, 2> (mma.sync)"
+    assert bench.mq_kernel_name(False, 128, 2, 4) == "multi_query_kernel<bf16, 128, 1> (mma.sync)"
+    assert bench.mq_kernel_name(False, 128, 3, 512).startswith("multi_query_kernel")
