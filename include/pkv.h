@@ -345,8 +345,9 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
  *   over KV head h / (num_q_heads / num_kv_heads).  out: [T, num_q_heads,
  *   head_dim] (dtype).  L_b = 1 is pkv_paged_attention_decode.
  *   context_lens[b] < L_b sets PKV_STATUS_BAD_CONTEXT; rows at negative
- *   positions get zeros.
- * Two kernels:
+ *   positions get zeros.  scale may have any sign (zero gives the mean of V
+ *   up to each position).
+ * Three kernels:
  *   - workspace (device, nullable) of at least
  *     pkv_multi_query_workspace_bytes bytes, and that size is non-zero
  *     (max_q_len * G <= 24, batch <= 1024, enough (sequence, KV head,
