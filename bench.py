@@ -21,9 +21,10 @@ Other workloads (``--workload``, one JSON line each):
 Prints ONE JSON line.  Usage:
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference]
                     [--workload NAME]
-N > 1 runs under torch.distributed.run, one rank per GPU; every rank decodes
-its own batch (weak scaling, no collective on the data path; the barrier and
-the max-over-ranks of the elapsed time are the only cross-rank calls).
+N > 1 runs under torch.distributed.run, one rank per GPU; every rank builds
+and decodes its own replica of the whole workload (replicas only: weak
+scaling, no collective on the data path; the barrier and the max-over-ranks
+of the elapsed time are the only cross-rank calls).
 """
 
 import argparse
@@ -43,6 +44,10 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; sequences/s per layer"
 KV_BYTES_PER_TOKEN = 2 * 8 * 128 * 2  # K and V, 8 KV heads, head dim 128, bf16
 NOMINAL_HBM_GBS = 8000.0
+# the end-to-end leg runs at least this many pipelined steps, whatever --steps
+# is, so that filling and draining the copy/compute pipeline does not dominate
+E2E_MIN_STEPS = 1000
+E2E_RING = 64  # pinned host input buffers the end-to-end leg cycles through
 _CSRC = "paged_kv_cache_13_gb300/csrc/"
 # workload -> (committed ncu traffic summary of its decode kernel, the sources
 # that kernel is built from); the traffic is reported only while they hash
@@ -157,13 +162,6 @@ def parse_args():
 
 
 # ----------------------------------------------------------------- helpers
-def shard(n, world, rank):
-    """Contiguous share [lo, hi) of n independent units for one rank."""
-    base, extra = divmod(n, world)
-    lo = rank * base + min(rank, extra)
-    return lo, lo + base + (1 if rank < extra else 0)
-
-
 def max_over_ranks(x, dist, device):
     """The largest of every rank's x (the job ends with its slowest rank)."""
     if dist is None:
@@ -222,56 +220,103 @@ def recorded_traffic(workload, kv_bytes_per_launch):
 
 
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    """SM clock, power and clock-event reasons, read in-process from NVML
+    (read-only queries) by a background thread every ``period_s`` seconds.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    The sampler runs across the warm-up and the timed loop; ``mark_start`` /
+    ``mark_end`` bracket the timed region, and the summary is taken over the
+    samples inside it (a 20-step region lasts about 2 ms, so the period is a
+    fraction of a millisecond).  NVML is reached through ctypes on the
+    driver's ``libnvidia-ml.so.1``; when it cannot be loaded the summary says
+    so and holds no samples."""
 
-    def __init__(self, device_index):
-        self.proc = None
-        self.dev = device_index
-        self.path = os.path.join("/tmp", "pkv_clocks_%d_%d.csv" % (os.getpid(), device_index))
+    # clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+    def __init__(self, device_index, period_s=0.0002):
+        import ctypes
+        import threading
+        self.ct, self.period, self.samples = ctypes, period_s, []
+        self.lib, self.handle, self.error = None, None, None
+        self.t_start = self.t_end = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            handle = ctypes.c_void_p()
+            uuid = self._uuid(device_index)
+            ok = uuid is not None and lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) == 0
+            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index),
+                                                            ctypes.byref(handle)) != 0:
+                raise RuntimeError("no NVML handle for device %d" % device_index)
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+            self.sm_max = float(mx.value) or None
+            self.lib, self.handle = lib, handle
+        except Exception as e:  # no NVML: the summary records why
+            self.error = str(e)
+
+    @staticmethod
+    def _uuid(device_index):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def _read(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0
+        lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        self.reasons_fn(h, ct.byref(rs))
+        if ok:
+            self.samples.append((time.perf_counter(), float(mhz.value), mw.value / 1000.0, rs.value))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._read()
+            time.sleep(self.period)
 
     def start(self):
-        try:
-            self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh,
-                stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        if self.lib is None:
+            return
+        import threading
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+
+    def mark_start(self):
+        self.t_start = time.perf_counter()
+
+    def mark_end(self):
+        self.t_end = time.perf_counter()
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 8:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    mx.append(float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[4:8]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if self.lib is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "NVML unavailable: %s" % self.error}
+        self._stop.set()
+        self._thread.join(timeout=5)
+        self._read()
+        lo = self.t_start if self.t_start is not None else -1e30
+        hi = self.t_end if self.t_end is not None else 1e30
+        inside = [x for x in self.samples if lo <= x[0] <= hi]
+        reasons = sorted({n for x in inside for bit, n in self.REASONS if x[3] & bit})
+        out = {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
+               "sm_max_mhz": self.sm_max, "reasons": reasons, "samples": len(inside),
+               "power_w_max": max((x[2] for x in inside), default=None),
+               "samples_whole_run": len(self.samples),
+               "sm_mhz_median_whole_run": statistics.median([x[1] for x in self.samples])
+               if self.samples else None,
+               "source": "in-process NVML reads every %.1f ms across warm-up and timed loop; "
+                         "summary over the timed region" % (self.period * 1e3)}
+        return out
 
 
 # ----------------------------------------------------------- device setup
@@ -467,24 +512,25 @@ def run_device(args, rank, world, dist):
     dev_index = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev_index)
     device = torch.device("cuda", dev_index)
-    e2e_steps = max(1, min(args.steps, 200))
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     cache = Cache(pkv, torch, device, args.workload, args.partition_size,
                   headroom_tokens=e2e_steps + 8, pool_blocks=args.pool_blocks)
     stream = torch.cuda.current_stream()
     kv_bytes = cache.kv_bytes()
 
     # ---------- device-resident timed region
+    clocks = ClockSampler(dev_index)
+    clocks.start()
     for _ in range(args.warmup):
         cache.step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev_index)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark_start()
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -492,6 +538,7 @@ def run_device(args, rank, world, dist):
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     clk = clocks.stop()
     if dist is not None:
         dist.barrier()
@@ -611,16 +658,17 @@ def run_mq(args, rank, world, dist):
         pkv.pkv_paged_attention_multi_query(qq, q_start, cache.k_pool, cache.v_pool, cache.tables,
                                             cache.lens, w["scale"], oo, L, workspace=mq_ws)
 
+    clocks = ClockSampler(dev_index)
+    clocks.start()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(dev_index)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks.start()
+    clocks.mark_start()
     t0.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -628,6 +676,7 @@ def run_mq(args, rank, world, dist):
         ev[i][1].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     clk = clocks.stop()
     assert pkv.pkv_device_status() == 0
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dist, device)
@@ -635,7 +684,7 @@ def run_mq(args, rank, world, dist):
     call_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
 
     # end to end: q from pinned host memory, out back to pinned host memory
-    e2e_steps = max(1, min(args.steps, 200))
+    e2e_steps = max(E2E_MIN_STEPS, args.steps)
     hq_ = q.cpu().pin_memory()
     ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     dq = torch.empty_like(q)
@@ -753,10 +802,12 @@ def run_e2e(pkv, torch, cache, steps, dist, device):
                 "tab": v("tab", torch.int32, (B, mb)), "lens": v("lens", torch.int32, (B,)),
                 "pos": v("pos", torch.int32, (B,))}
 
-    # each step's q and new K/V rows arrive in pinned host memory (staged
-    # before the timed region, as an upstream producer would hand them over);
-    # the timed loop adds the block manager's slots, pairs and tables
-    h_in = [torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(steps)]
+    # each step's q and new K/V rows arrive in pinned host memory, a ring of
+    # R buffers an upstream producer fills ahead (staged before the timed
+    # region); the timed loop adds the block manager's slots, pairs and
+    # tables to buffer s % R once that buffer's previous copy has finished
+    R = min(steps, E2E_RING)
+    h_in = [torch.empty(in_bytes, dtype=torch.uint8, pin_memory=True) for _ in range(R)]
     d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
     h_out = [torch.empty((B, Hq, D), dtype=dt, pin_memory=True) for _ in range(2)]
     d_out = [torch.empty((B, Hq, D), dtype=dt, device=device) for _ in range(2)]
@@ -765,7 +816,7 @@ def run_e2e(pkv, torch, cache, steps, dist, device):
     ws = torch.empty(max(16, pkv.pkv_decode_workspace_bytes(B, Hq, D, mb, 16, cache.partition_size)),
                      dtype=torch.uint8, device=device)
     q16 = syn.query(w)
-    for s in range(steps):
+    for s in range(R):
         k, v = syn.new_token_kv(w, s)
         hv[s]["q"].copy_(q16)
         hv[s]["k"].copy_(k)
@@ -785,7 +836,9 @@ def run_e2e(pkv, torch, cache, steps, dist, device):
     t_start = time.perf_counter()
     for s in range(steps):
         j = s % 2
-        h = hv[s]
+        h = hv[s % R]
+        if s >= R:
+            e_h2d[s - R].synchronize()  # the ring buffer's previous copy is done
         _, pairs = pkv.pkv_seq_append_batch(cache.pool, cache.seqs, 1, h["slots"].numpy(),
                                             h["pairs"].view(-1).numpy())
         pkv.pkv_build_block_tables(cache.pool, cache.seqs, mb, h["tab"].numpy(), h["lens"].numpy())
@@ -796,7 +849,7 @@ def run_e2e(pkv, torch, cache, steps, dist, device):
         with torch.cuda.stream(copy):
             if s >= 2:
                 copy.wait_event(e_dec[s - 2])  # decode s-2 no longer reads this device slot
-            d_in[j].copy_(h_in[s], non_blocking=True)
+            d_in[j].copy_(h_in[s % R], non_blocking=True)
             e_h2d[s] = ev()
             e_h2d[s].record(copy)
         compute.wait_event(e_h2d[s])

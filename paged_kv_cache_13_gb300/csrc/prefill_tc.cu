@@ -243,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bars: 0-1 K full, 2-3 V full, 4-5 S ready (per S buffer), 6 O ready
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
     int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 68);
+    // set by warp 1 when it skipped its copies of an iteration (its wait for
+    // the previous O += P V ran out): the drain then expects one copy fewer
+    int* copies_skipped = reinterpret_cast<int*>(sm + kOffBar + 72);
     float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2][128]: per-half row values
     // tab[t % 4][jj]: TMA row of block jj of key tile t (past the map's end:
     // zeros), read from the table two tiles ahead of its copies
@@ -273,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
+        *copies_skipped = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
@@ -436,19 +440,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             l *= alpha;
         }
         // the previous tile's O += P V must be done before P and O are touched
+        bool o_done = true;
         if (j > 0 && !wait_bar(bar(6), (j - 1) & 1)) {
             atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
             *abort_flag = 1;
+            o_done = false;
         }
         fence_after_sync();
         if (warp == 1) {
             // stages freed: V of tile j - 1 (its O += P V is done), K of tile
             // j (its S was read above).  One copy per lane: lanes 0-15 the 16
-            // of K tile j + 2, lanes 16-31 the 16 of V tile j + 1
+            // of K tile j + 2, lanes 16-31 the 16 of V tile j + 1.  If any
+            // lane's wait ran out, the V stage may still be read by that MMA:
+            // the warp issues nothing this iteration (the CTA stops below).
             const int ln = tid & 31;
             const bool is_v = ln >= 16;
             const int jt = is_v ? j + 1 : j + 2;
-            if (jt < ntiles) {
+            const bool all_done = __all_sync(0xffffffffu, o_done);
+            if (!all_done && ln == 0) *copies_skipped = 1;
+            if (all_done && jt < ntiles) {
                 const int st = jt & 1;
                 const uint32_t fb = bar((is_v ? 2 : 0) + st);
                 if ((ln & 15) == 0) mbar_arrive_expect_tx(fb, kTile);
@@ -519,9 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the flag just after the barrier
         if (__syncthreads_or(*reinterpret_cast<volatile int*>(abort_flag))) {
             aborted = true;
-            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1
-            issued_k = min(ntiles, j + 3);
-            issued_v = min(ntiles, j + 2);
+            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1,
+            // or one fewer of each when warp 1 skipped this iteration's
+            const int skipped = *reinterpret_cast<volatile int*>(copies_skipped);
+            issued_k = min(ntiles, j + (skipped ? 2 : 3));
+            issued_v = min(ntiles, j + (skipped ? 1 : 2));
             break;
         }
         // ---- O += P V (thread 0 issues)

@@ -201,6 +201,36 @@ def expected(c, seq_ids=None):
     return np.stack(out)
 
 
+def _expected_one(args):
+    """Oracle output of one sequence, regenerated from the seeded workload
+    (runs in a worker process)."""
+    w, idx, q_row, quant, n_sink, group_size, window = args
+    k, v = syn.sequence_kv(w, idx)
+    k, v = syn.kv_rows_to_numpy(k), syn.kv_rows_to_numpy(v)
+    if quant is None:
+        return oatt.sequence_attention(q_row, k, v, w["scale"])
+    return okv.sequence_attention_quant(q_row, k, v, w["scale"], n_sink, quant, group_size,
+                                        window=window)
+
+
+def expected_parallel(c, seq_ids=None, workers=None):
+    """``expected`` computed in worker processes, one sequence each.
+
+    The pool is started with ``spawn``: the calling process already holds a
+    CUDA context, and a forked child of it would hang."""
+    import multiprocessing
+    import os
+    from concurrent.futures import ProcessPoolExecutor
+    q = syn.kv_rows_to_numpy(syn.query(c.w))
+    ids = list(range(len(c.decoded)) if seq_ids is None else seq_ids)
+    prefix = "prompt" in c.w
+    jobs = [(c.w, (c.decoded[i] - 1) if prefix else c.decoded[i], q[i], c.quant, c.n_sink,
+             getattr(c, "group_size", c.w["d"]), getattr(c, "window", 0)) for i in ids]
+    n = workers or max(1, min(len(jobs), (os.cpu_count() or 1), 16))
+    with ProcessPoolExecutor(max_workers=n, mp_context=multiprocessing.get_context("spawn")) as ex:
+        return np.stack(list(ex.map(_expected_one, jobs)))
+
+
 def assert_close(got, want, atol=2e-3, rtol=1e-2, what=""):
     """|got - want| <= atol + rtol * |want| element-wise (the acceptance bound)."""
     got = np.asarray(got, dtype=np.float64)

@@ -36,6 +36,16 @@ def test_every_declared_symbol_has_a_binding(pkv):
         assert hasattr(pkv, n) or n == "pkv_status_string" or n in ("pkv_pool_block_size",), n
 
 
+def test_static_workspace_size_agrees_with_the_header(pkv):
+    """The binding's PKV_STATIC_WORKSPACE_BYTES (used to size-check calls of
+    the allocation-free decode) is the header's #define, not a separate copy
+    that could drift."""
+    text = open(HEADER).read()
+    m = re.search(r"#define\s+PKV_STATIC_WORKSPACE_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "PKV_STATIC_WORKSPACE_BYTES not found in the header"
+    assert pkv.PKV_STATIC_WORKSPACE_BYTES == int(m.group(1)) << int(m.group(2))
+
+
 def test_status_strings(pkv):
     for code in range(-10, 1):
         s = pkv.lib.pkv_status_string(code)

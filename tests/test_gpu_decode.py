@@ -107,13 +107,18 @@ def test_zero_context_gives_zeros(pkv, cuda_dev):
     q = torch.randn((3, G * Hkv, D), dtype=torch.bfloat16, device=cuda_dev)
     tables = torch.tensor([[0, 1], [2, -1], [-1, -1]], dtype=torch.int32, device=cuda_dev)
     lens = torch.tensor([20, 3, 0], dtype=torch.int32, device=cuda_dev)
+    want = oatt.paged_attention_decode(q.float().cpu().numpy(), kp.float().cpu().numpy(),
+                                       kp.float().cpu().numpy(), tables.cpu().numpy(),
+                                       lens.cpu().numpy(), 0.1)
+    assert not want[2].any()
     for ps in (0, 16):
         out = torch.full((3, G * Hkv, D), 7.0, dtype=torch.bfloat16, device=cuda_dev)
         ws = torch.empty(1 << 20, dtype=torch.uint8, device=cuda_dev)
         pkv.pkv_paged_attention_decode(q, kp, kp, tables, lens, 0.1, out, ws, ps)
         torch.cuda.synchronize()
         assert (out[2] == 0).all()
-        assert (out[1] != 7.0).all()
+        assert_close(out.float().cpu().numpy(), want, what="zero context beside 20 and 3, ps %d" % ps)
+    assert pkv.pkv_device_status() == 0
 
 
 def test_bit_identical_across_block_permutations(pkv, cuda_dev):

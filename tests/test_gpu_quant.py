@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import synthetic as syn
-from cache_builder import assert_close, build, expected, logical_rows
+from cache_builder import assert_close, build, expected, expected_parallel, logical_rows
 from oracle import kvcache as okv
 
 pytestmark = pytest.mark.gpu
@@ -120,27 +120,33 @@ def test_quant_decode_fp16_head64(pkv, cuda_dev, qmode):
     assert_close(_decode_quant(pkv, c, 64), expected(c), what=qmode)
 
 
+def _codes_match(c, i, qmode):
+    """Every token's codes, scales (and zeros) of sequence i, K and V, equal
+    the oracle quantiser's, read through the sequence's table."""
+    k, v = logical_rows(c, i)
+    table = c.tables_host[i]
+    t = np.arange(k.shape[0])
+    blk, off = table[t // 16], t % 16
+    for name, x in (("k", k), ("v", v)):
+        _, codes, s, z = okv.quantize_sequence(x, qmode, c.group_size)
+        np.testing.assert_array_equal(c.cache[name + "_codes"].cpu().numpy()[blk, :, off], codes)
+        assert c.cache[name + "_scale"].cpu().numpy()[blk, :, off].tobytes() == s.tobytes()
+        if qmode == "int4":
+            assert c.cache[name + "_zero"].cpu().numpy()[blk, :, off].tobytes() == z.tobytes()
+
+
 @pytest.mark.parametrize("qmode", ["int4", "fp8"])
-def test_quant_workload_full_size_sampled(pkv, cuda_dev, qmode):
-    """32 sequences x 16,384 tokens, 4 sinks, 1% outliers at +-8: codes of
-    sampled sequences bit-exact, their outputs within the bound."""
+def test_quant_workload_full_size(pkv, cuda_dev, qmode):
+    """32 sequences x 16,384 tokens, 4 sinks, 1% outliers at +-8: every
+    sequence's output within the bound (balanced split), and every code,
+    scale and zero of three sequences bit-exact."""
     w = syn.workload("quant")
     c = build(pkv, w, cuda_dev, quant=qmode)
     got = _decode_quant(pkv, c, 0)
-    sample = [0, 13, 31]
-    want = expected(c, sample)
-    assert_close(got[sample], want, what="quant %s" % qmode)
-    # codes of a sampled sequence at its slots
-    k, v = logical_rows(c, 13)
-    table = c.tables_host[13]
-    _, kc, ks, kz = okv.quantize_sequence(k, qmode, c.group_size)
-    gk = c.cache["k_codes"].cpu().numpy()
-    gs = c.cache["k_scale"].cpu().numpy()
-    for t in range(0, k.shape[0], 997):
-        blk, off = table[t // 16], t % 16
-        assert np.array_equal(gk[blk, :, off], kc[t])
-        assert gs[blk, :, off].tobytes() == ks[t].tobytes()
     assert np.isfinite(got).all()
+    assert_close(got, expected_parallel(c), what="quant %s" % qmode)
+    for i in (0, 13, 31):
+        _codes_match(c, i, qmode)
 
 
 def test_quant_prefix_cow_int4(pkv, cuda_dev):
@@ -171,14 +177,15 @@ def test_int4_group64_short_contexts_and_8_sinks(pkv, cuda_dev, ctx):
         assert_close(_decode_quant(pkv, c, ps), want, what="g64 ctx %d" % ctx)
 
 
-def test_int4_group64_full_size_sampled(pkv, cuda_dev):
+def test_int4_group64_full_size(pkv, cuda_dev):
     """32 sequences x 16,384 tokens in the pages' layout (g = 64, 8 sinks):
-    sampled outputs within the bound (balanced split)."""
+    every output within the bound (balanced split), every code of one
+    sequence bit-exact."""
     w = syn.workload("quant", group_size=64, n_sink=8)
     c = build(pkv, w, cuda_dev, quant="int4")
     got = _decode_quant(pkv, c, 0)
-    sample = [0, 21, 31]
-    assert_close(got[sample], expected(c, sample), what="g64 full size")
+    assert_close(got, expected_parallel(c), what="g64 full size")
+    _codes_match(c, 21, "int4")
 
 
 def test_int4_group_size_checks(pkv, cuda_dev):
@@ -218,14 +225,13 @@ def test_window_ring_holds_the_last_tokens(pkv, cuda_dev):
             np.testing.assert_array_equal(wk[(t // 16) % R, :, t % 16], k[t])
 
 
-def test_pages_layout_full_size_sampled(pkv, cuda_dev):
+def test_pages_layout_full_size(pkv, cuda_dev):
     """32 x 16,384 tokens in the pages' BIE layout (INT4 g = 64, 8 sinks,
-    128-token 16-bit window): sampled outputs within the bound."""
+    128-token 16-bit window): every output within the bound."""
     w = syn.workload("quant", group_size=64, n_sink=8, window=128)
     c = build(pkv, w, cuda_dev, quant="int4")
     got = _decode_quant(pkv, c, 0)
-    sample = [0, 9, 31]
-    assert_close(got[sample], expected(c, sample), what="BIE layout full size")
+    assert_close(got, expected_parallel(c), what="BIE layout full size")
 
 
 @pytest.mark.parametrize("qmode,mag", [("int4", 4000.0), ("fp8", 60000.0)])

@@ -1,8 +1,10 @@
-"""The N > 1 host logic of bench.py with 2 gloo ranks on CPU: sharding of
-independent sequences, the max-over-ranks of the elapsed time and the
-whole-job rate.  Each rank also builds its own share of a workload's block
-tables with the C++ block manager (no GPU, no collective on the data path)."""
+"""The N > 1 host logic of bench.py with 2 gloo ranks on CPU: every rank
+builds its own replica of the workload's block tables with the C++ block
+manager (replicas only: no GPU, no collective on the data path), the
+max-over-ranks of the elapsed time, and the whole-job rate over all
+replicas."""
 
+import hashlib
 import os
 import socket
 
@@ -20,6 +22,11 @@ def _free_port():
     return p
 
 
+def tables_digest(pkv, pool, seqs):
+    tables, ctx = pkv.pkv_build_block_tables(pool, seqs, 256)
+    return hashlib.sha256(tables.tobytes() + ctx.tobytes()).hexdigest()
+
+
 def _worker(rank, world, port, q):
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
@@ -30,10 +37,9 @@ def _worker(rank, world, port, q):
         import synthetic as syn
         w = syn.workload("llama3_8b_b64")
         lens = syn.context_lengths(w)
-        lo, hi = bench.shard(len(lens), world, rank)
         pool = pkv.pkv_pool_create(w["num_blocks"], 16, syn.free_order(w))
         seqs = []
-        for L in lens[lo:hi]:
+        for L in lens:
             s = pkv.pkv_seq_create(pool)
             pkv.pkv_seq_append(pool, s, L)
             seqs.append(s)
@@ -43,7 +49,7 @@ def _worker(rank, world, port, q):
         slowest = bench.max_over_ranks(fake_seconds, dist, torch.device("cpu"))
         t = torch.tensor([my_bytes], dtype=torch.float64)
         dist.all_reduce(t)
-        q.put((rank, lo, hi, my_bytes, slowest, float(t.item())))
+        q.put((rank, tables_digest(pkv, pool, seqs), my_bytes, slowest, float(t.item())))
         pkv.pkv_pool_destroy(pool)
     finally:
         dist.destroy_process_group()
@@ -64,22 +70,13 @@ def test_two_gloo_ranks():
     import bench
     import synthetic as syn
     lens = syn.context_lengths(syn.workload("llama3_8b_b64"))
-    # shards are disjoint and cover the batch
-    assert res[0][1] == 0 and res[0][2] == res[1][1] and res[1][2] == len(lens)
-    total = sum(r[3] for r in res)
-    assert total == sum(lens) * bench.KV_BYTES_PER_TOKEN
-    assert all(r[4] == 2.0 for r in res)  # the slowest rank's time on every rank
-    assert all(r[5] == total for r in res)
+    # every rank holds the same replica: identical tables, the whole batch
+    assert res[0][1] == res[1][1]
+    replica = sum(lens) * bench.KV_BYTES_PER_TOKEN
+    assert all(r[2] == replica for r in res)
+    total = sum(r[2] for r in res)
+    assert total == world * replica
+    assert all(r[3] == 2.0 for r in res)  # the slowest rank's time on every rank
+    assert all(r[4] == total for r in res)
     # weak-scaling rate: units of all ranks over the slowest time
-    assert bench.whole_job_rate(100.0, 2, 2.0) == 100.0
-
-
-def test_shard_covers_any_size():
-    import bench
-    for n in (0, 1, 7, 64, 65):
-        for world in (1, 2, 3, 8):
-            parts = [bench.shard(n, world, r) for r in range(world)]
-            assert parts[0][0] == 0 and parts[-1][1] == n
-            assert all(parts[i][1] == parts[i + 1][0] for i in range(world - 1))
-            sizes = [b - a for a, b in parts]
-            assert max(sizes) - min(sizes) <= 1
+    assert bench.whole_job_rate(replica, world, 2.0) == total / 2.0

@@ -1,16 +1,17 @@
 """The allocation-free decode entry point, for callers that cannot allocate a
 device workspace (graph capture, host runtimes that own all device memory,
 fixed-budget serving loops).  Called through the C ABI, its output must
-match the regular entry point's (which gets a torch-allocated workspace),
-on two calls in a row -- the second call reuses the library's array with the
-first call's partials still in it."""
+match the regular entry point's (which gets a torch-allocated workspace) and
+the oracle's, on two calls in a row that follow a call with a different
+query -- so every call reuses the library's array with another call's
+partials still in it."""
 
 import numpy as np
 import pytest
 import torch
 
 import synthetic as syn
-from cache_builder import assert_close, build
+from cache_builder import assert_close, build, expected
 
 pytestmark = pytest.mark.gpu
 
@@ -26,7 +27,21 @@ def _regular(pkv, c, ps):
     return out
 
 
-@pytest.mark.parametrize("name,ps", [("llama3_8b_b64", 512), ("long_splitk", 512), ("tiny", 0)])
+def _static(pkv, c, q, ps):
+    w = c.w
+    B = len(c.decoded)
+    out = torch.full((B, w["hq"], w["d"]), float("nan"), dtype=w["torch_dtype"], device=q.device)
+    pkv.pkv_paged_attention_decode_static_ws(q, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"],
+                                             out, ps)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy()
+
+
+# partition 0 is the automatic choice: the balanced split and its merge on
+# the two large workloads (partials for every warp's runs in the array), a
+# single pass on the tiny one
+@pytest.mark.parametrize("name,ps", [("llama3_8b_b64", 0), ("long_splitk", 0),
+                                     ("llama3_8b_b64", 512), ("long_splitk", 512), ("tiny", 0)])
 def test_static_workspace_matches_regular_twice(pkv, cuda_dev, name, ps):
     w = syn.workload(name)
     c = build(pkv, w, cuda_dev)
@@ -34,14 +49,18 @@ def test_static_workspace_matches_regular_twice(pkv, cuda_dev, name, ps):
     need = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, ps)
     assert need <= pkv.PKV_STATIC_WORKSPACE_BYTES
     want = _regular(pkv, c, ps).float().cpu().numpy()
+    oracle = expected(c)
+    assert_close(want, oracle, what="%s regular entry point" % name)
+    # leave other partials in the shared array first: the same cache with a
+    # different query, so a missed write or a stale slot read shows
+    other = _static(pkv, c, (c.q.float() * -1.75).to(c.q.dtype), ps)
+    assert np.isfinite(other).all()
+    assert not np.allclose(other, want)
     for call in range(2):
-        out = torch.full((B, w["hq"], w["d"]), float("nan"), dtype=w["torch_dtype"], device=cuda_dev)
-        pkv.pkv_paged_attention_decode_static_ws(c.q, c.k_pool, c.v_pool, c.tables, c.lens,
-                                                 w["scale"], out, ps)
-        torch.cuda.synchronize()
-        got = out.float().cpu().numpy()
+        got = _static(pkv, c, c.q, ps)
         assert np.isfinite(got).all()
-        assert_close(got, want, what="%s call %d" % (name, call))
+        assert_close(got, want, what="%s call %d vs regular" % (name, call))
+        assert_close(got, oracle, what="%s call %d vs oracle" % (name, call))
     assert pkv.pkv_device_status() == 0
 
 
