@@ -46,7 +46,7 @@ KV_BYTES_PER_TOKEN = 2 * 8 * 128 * 2  # K and V, 8 KV heads, head dim 128, bf16
 NOMINAL_HBM_GBS = 8000.0
 # the end-to-end leg runs at least this many pipelined steps, whatever --steps
 # is, so that filling and draining the copy/compute pipeline does not dominate
-E2E_MIN_STEPS = 1000
+E2E_MIN_STEPS = 4000
 E2E_RING = 64  # pinned host input buffers the end-to-end leg cycles through
 _CSRC = "paged_kv_cache_13_gb300/csrc/"
 # workload -> (committed ncu traffic summary of its decode kernel, the sources
@@ -288,6 +288,10 @@ class ClockSampler:
         if self.lib is None:
             return
         import threading
+        # the launch loop holds the GIL between its calls: a short switch
+        # interval lets the sampling thread in every fraction of a millisecond
+        self._switch = sys.getswitchinterval()
+        sys.setswitchinterval(self.period / 2)
         self._thread = threading.Thread(target=self._loop, daemon=True)
         self._thread.start()
 
@@ -303,6 +307,7 @@ class ClockSampler:
                     "source": "NVML unavailable: %s" % self.error}
         self._stop.set()
         self._thread.join(timeout=5)
+        sys.setswitchinterval(self._switch)
         self._read()
         lo = self.t_start if self.t_start is not None else -1e30
         hi = self.t_end if self.t_end is not None else 1e30
@@ -549,6 +554,10 @@ def run_device(args, rank, world, dist):
     ms_per_step = elapsed_ms / args.steps
 
     # ---------- end to end through the public API, host buffers
+    # the e2e loop appends a token per sequence per step: as many steps as
+    # the pool has blocks for (the quantised workloads fill most of theirs)
+    free = pkv.pkv_pool_num_free(cache.pool)
+    e2e_steps = max(16, min(e2e_steps, (free // max(cache.B, 1) - 1) * 16))
     e2e = run_e2e(pkv, torch, cache, e2e_steps, dist, device)
     prefix = prefix_cache_timing(pkv, cache) if "prompt" in cache.w else None
     append = append_timing(pkv, torch, cache)

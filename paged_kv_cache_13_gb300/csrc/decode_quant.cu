@@ -52,8 +52,8 @@ constexpr int NW = 4;
 // registers.
 // (Measured on the 32 x 16k workload: INT4 259 -> 242 us; FP8 unchanged or
 // slower with the INT4 settings.)
-template <int QMODE, int NG = 1>
-constexpr int kCtasPerSm = QMODE == PKV_QMODE_INT4_ASYM && NG == 1 ? 5 : 4;
+template <int QMODE, int NG = 1, bool PAIR = false>
+constexpr int kCtasPerSm = PAIR ? 4 : (QMODE == PKV_QMODE_INT4_ASYM && NG == 1 ? 5 : 4);
 template <int QMODE>
 constexpr bool kQueryInShared = QMODE == PKV_QMODE_INT4_ASYM;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -163,11 +163,367 @@ __device__ __forceinline__ int pv_column(int e, int g) {
     return NG == 1 ? g * (D / 8) + e : (e >> 3) * 64 + 8 * g + (e & 7);
 }
 
+// The quantised blocks of a pass two at a time (INT4, G <= 4; the scheme is
+// described at quant_pass), the two column halves merged, then the window
+// blocks one by one with attend16.  qs: the shared query slices (two
+// copies); qs0, qs1: the group sums of the lane's query heads 2 hh, 2 hh + 1.
+template <typename T, int D, int NG, bool WIN, typename Attend16>
+__device__ __forceinline__ void quant_pairs(const QDecodeArgs& a, int b, int kvh, int ctx, int lb_first,
+                                            int lb_end, int stride, int win_lb0, uint32_t qs,
+                                            const float (&qs0)[NG], const float (&qs1)[NG],
+                                            QState<D / 16, NG>& st, Attend16& attend16) {
+    constexpr int KSTEPS = D / 16;
+    constexpr int MT = D / 16;
+    constexpr int CB = D / 2;        // code bytes per row
+    constexpr int KW = D / 32;       // 32-bit K-code words per lane per row
+    constexpr int VW = D / 64;       // 32-bit V-code words per lane per row
+    constexpr int DS = D / 8;
+    constexpr int KPG = KW / NG;
+    constexpr int VPG = VW / NG;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int sl = c >> 1;           // the lane's column half: block A (0) or B (1)
+    const int hh = c & 1;
+    float& m0 = st.m0;
+    float& m1 = st.m1;
+    float& l0 = st.l0;
+    float& l1 = st.l1;
+    auto& corr = st.corr;
+    auto& o = st.o;
+    const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
+    const int vr0 = 2 * c, vr1 = 2 * c + 1, vr2 = 8 + 2 * c, vr3 = 9 + 2 * c;
+
+    struct Codes {
+        uint32_t kw0[KW], kw1[KW], vw[4][VW];
+    };
+    struct Scales {
+        __half2 ks[NG], vs[NG], kz[NG], vz[NG];  // low: token g, high: token g + 8
+    };
+    auto load_codes = [&](int phys, Codes& C) {
+        const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;
+        const uint8_t* kc = a.k_codes + bh * (BS * CB);
+        const uint8_t* vc = a.v_codes + bh * (BS * CB);
+        if constexpr (NG == 2) {
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+                const uint2 r0 = ldg_stream8(kc + g * CB + 32 * gi + 8 * c);
+                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 32 * gi + 8 * c);
+                C.kw0[2 * gi] = r0.x; C.kw0[2 * gi + 1] = r0.y;
+                C.kw1[2 * gi] = r1.x; C.kw1[2 * gi + 1] = r1.y;
+                const int off = 32 * gi + 4 * g;
+                C.vw[0][gi] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
+                C.vw[1][gi] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
+                C.vw[2][gi] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
+                C.vw[3][gi] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+            }
+        } else {
+            if constexpr (KW == 4) {
+                const uint4 r0 = ldg_stream(kc + g * CB + 16 * c);
+                const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 16 * c);
+                C.kw0[0] = r0.x; C.kw0[1] = r0.y; C.kw0[2] = r0.z; C.kw0[3] = r0.w;
+                C.kw1[0] = r1.x; C.kw1[1] = r1.y; C.kw1[2] = r1.z; C.kw1[3] = r1.w;
+            } else {
+                const uint2 r0 = ldg_stream8(kc + g * CB + 8 * c);
+                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 8 * c);
+                C.kw0[0] = r0.x; C.kw0[1] = r0.y;
+                C.kw1[0] = r1.x; C.kw1[1] = r1.y;
+            }
+            const int off = DS / 2 * g;
+            if constexpr (VW == 2) {
+                const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
+                const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
+                C.vw[0][0] = x0.x; C.vw[0][1] = x0.y; C.vw[1][0] = x1.x; C.vw[1][1] = x1.y;
+                C.vw[2][0] = x2.x; C.vw[2][1] = x2.y; C.vw[3][0] = x3.x; C.vw[3][1] = x3.y;
+            } else {
+                C.vw[0][0] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
+                C.vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
+                C.vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
+                C.vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+            }
+        }
+    };
+    // the scales and zero points of the lane's own block (tokens g, g + 8)
+    auto load_scales = [&](int phys, Scales& S) {
+        const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;
+        const int64_t s0 = (bh * BS + g) * NG, s1 = (bh * BS + g + 8) * NG;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            S.ks[gi] = __halves2half2(a.k_scale[s0 + gi], a.k_scale[s1 + gi]);
+            S.vs[gi] = __halves2half2(a.v_scale[s0 + gi], a.v_scale[s1 + gi]);
+            S.kz[gi] = __halves2half2(a.k_zero[s0 + gi], a.k_zero[s1 + gi]);
+            S.vz[gi] = __halves2half2(a.v_zero[s0 + gi], a.v_zero[s1 + gi]);
+        }
+    };
+    // PV A fragment of element e (token pair pr) from a block's V words
+    auto pv_frag = [&](const Codes& C, int e, int pr) {
+        const uint32_t* R0 = C.vw[2 * pr];
+        const uint32_t* R1 = C.vw[2 * pr + 1];
+        const int word = e >> 3, sub = (e >> 2) & 1, nib = e & 3;
+        const uint32_t X = __byte_perm(R0[word], R1[word], sub ? 0x7632u : 0x5410u);
+        const uint32_t Y = nib >= 2 ? X >> 8 : X;
+        return (nib & 1) ? nib_odd(Y) : nib_even(Y);
+    };
+
+    auto attend_pair = [&](int lbA, bool vA, bool vB, const Codes& CA, const Codes& CB, const Scales& S) {
+        // ---- S^T = C Q^T: block A against the query in columns 0-3, block B
+        // against it in columns 4-7, one accumulator per column group
+        float sg[NG][4];
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) sg[gi][0] = sg[gi][1] = sg[gi][2] = sg[gi][3] = 0.f;
+#pragma unroll
+        for (int k = 0; k < KW; ++k) {
+            const uint4 qa = lds128(qs + k * 512);
+            const uint4 qb = lds128(qs + (KSTEPS / 2 + k) * 512);
+            float (&sk)[4] = sg[k / KPG];
+            const uint32_t a0 = CA.kw0[k] >> 8, a1 = CA.kw1[k] >> 8;
+            mma_f16(sk, nib_even(CA.kw0[k]), nib_even(CA.kw1[k]), nib_odd(CA.kw0[k]), nib_odd(CA.kw1[k]),
+                    qa.x, qa.y);
+            mma_f16(sk, nib_even(a0), nib_even(a1), nib_odd(a0), nib_odd(a1), qa.z, qa.w);
+            const uint32_t b0 = CB.kw0[k] >> 8, b1 = CB.kw1[k] >> 8;
+            mma_f16(sk, nib_even(CB.kw0[k]), nib_even(CB.kw1[k]), nib_odd(CB.kw0[k]), nib_odd(CB.kw1[k]),
+                    qb.x, qb.y);
+            mma_f16(sk, nib_even(b0), nib_even(b1), nib_odd(b0), nib_odd(b1), qb.z, qb.w);
+        }
+        // ---- the lane's block: A for c = 0, 1, B for c = 2, 3
+        const int lbm = lbA + (sl ? stride : 0);
+        const bool vm = sl ? vB : vA;
+        const int t0 = lbm * BS;
+        const bool ok0 = vm && t0 + g < ctx, ok1 = vm && t0 + g + 8 < ctx;
+        float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const float ks0 = __low2float(S.ks[gi]), ks1 = __high2float(S.ks[gi]);
+            const float kz0 = __low2float(S.kz[gi]), kz1 = __high2float(S.kz[gi]);
+            x0 += ks0 * (sg[gi][0] * kTwo24 - kz0 * qs0[gi]);
+            x1 += ks0 * (sg[gi][1] * kTwo24 - kz0 * qs1[gi]);
+            x2 += ks1 * (sg[gi][2] * kTwo24 - kz1 * qs0[gi]);
+            x3 += ks1 * (sg[gi][3] * kTwo24 - kz1 * qs1[gi]);
+        }
+        x0 *= a.scale_log2;
+        x1 *= a.scale_log2;
+        x2 *= a.scale_log2;
+        x3 *= a.scale_log2;
+        // sinks: only logical block 0, which is block A of a pass's first step
+        const bool sinks_here = lbA == 0 && a.n_sink > 0;
+        bool sk0 = false, sk1 = false;
+        if (sinks_here) {
+            sk0 = sl == 0 && g < a.n_sink;
+            sk1 = sl == 0 && g + 8 < a.n_sink;
+            const T* qbase = static_cast<const T*>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * a.G) * D;
+            const T* skb = static_cast<const T*>(a.sink_k);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int t = g + 8 * r;
+                if (sl == 0 && t < a.n_sink) {
+                    const T* krow = skb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D;
+                    float d0 = 0.f, d1 = 0.f;
+                    const int h0 = min(2 * hh, a.G - 1), h1 = min(2 * hh + 1, a.G - 1);
+                    for (int d = 0; d < D; ++d) {
+                        const float kv = tofloat(krow[d]);
+                        d0 += tofloat(qbase[h0 * D + d]) * kv;
+                        d1 += tofloat(qbase[h1 * D + d]) * kv;
+                    }
+                    if (r == 0) {
+                        x0 = d0 * a.scale_log2;
+                        x1 = d1 * a.scale_log2;
+                    } else {
+                        x2 = d0 * a.scale_log2;
+                        x3 = d1 * a.scale_log2;
+                    }
+                }
+            }
+        }
+        if (!ok0) x0 = x1 = neg_inf();
+        if (!ok1) x2 = x3 = neg_inf();
+
+        // ---- online softmax of the lane's stream (as in quant_pass)
+        const float bx0 = fmaxf(x0, x2), bx1 = fmaxf(x1, x3);
+        float vsmax = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+            vsmax = fmaxf(vsmax, fmaxf(__low2float(S.vs[gi]), __high2float(S.vs[gi])));
+        if (__any_sync(0xffffffffu, bx0 > m0 + kSlack || bx1 > m1 + kSlack || vsmax > kLazyMaxScale)) {
+            float bm0 = bx0, bm1 = bx1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            // a stream may have had no live token yet (its maxima still
+            // -inf: a pass's single block, or block B missing)
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = mn0 == neg_inf() ? 1.f : ex2(m0 - mn0);
+            const float al1 = mn1 == neg_inf() ? 1.f : ex2(m1 - mn1);
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                corr[gi][0] *= al0;
+                corr[gi][1] *= al1;
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+            m0 = mn0;
+            m1 = mn1;
+        }
+        const float r0 = m0 == neg_inf() ? 0.f : m0, r1 = m1 == neg_inf() ? 0.f : m1;
+        const float p0 = ex2(x0 - r0), p1 = ex2(x1 - r1);
+        const float p2 = ex2(x2 - r0), p3 = ex2(x3 - r1);
+        l0 += p0 + p2;
+        l1 += p1 + p3;
+        const bool w0 = ok0 && !sk0, w1 = ok1 && !sk1;
+        // PV weight fragments, split by column half: block A's MMAs take
+        // columns 0-3 (lanes g < 4 after the transpose), block B's 4-7
+        uint32_t wa0[NG], wa1[NG], wb0[NG], wb1[NG];
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const float vs0 = __low2float(S.vs[gi]), vs1 = __high2float(S.vs[gi]);
+            const float W0 = w0 ? p0 * vs0 : 0.f, W1 = w0 ? p1 * vs0 : 0.f;
+            const float W2 = w1 ? p2 * vs1 : 0.f, W3 = w1 ? p3 * vs1 : 0.f;
+            const uint32_t pk0 = f16pair(W0, W1), pk1 = f16pair(W2, W3);
+            const float vz0 = __low2float(S.vz[gi]), vz1 = __high2float(S.vz[gi]);
+            const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
+            const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
+            if (w0) {
+                corr[gi][0] += __low2float(h0) * vz0;
+                corr[gi][1] += __high2float(h0) * vz0;
+            }
+            if (w1) {
+                corr[gi][0] += __low2float(h1) * vz1;
+                corr[gi][1] += __high2float(h1) * vz1;
+            }
+            const uint32_t t0w = movmatrix_trans(pk0), t1w = movmatrix_trans(pk1);
+            wa0[gi] = g < 4 ? t0w : 0u;
+            wa1[gi] = g < 4 ? t1w : 0u;
+            wb0[gi] = g < 4 ? 0u : t0w;
+            wb1[gi] = g < 4 ? 0u : t1w;
+        }
+        // ---- O^T += C_v^T W^T for both blocks (INT4 codes decode to finite
+        // values, so rows past the context need no clearing: their W is 0)
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int el = pv_e<NG, MT>(mt, 0), eh = pv_e<NG, MT>(mt, 1);
+            const int gi = (el >> 3) / VPG;
+            mma_f16(o[mt], pv_frag(CA, el, 0), pv_frag(CA, eh, 0), pv_frag(CA, el, 1), pv_frag(CA, eh, 1),
+                    wa0[gi], wa1[gi]);
+            mma_f16(o[mt], pv_frag(CB, el, 0), pv_frag(CB, eh, 0), pv_frag(CB, el, 1), pv_frag(CB, eh, 1),
+                    wb0[gi], wb1[gi]);
+        }
+        if (sinks_here) {
+            // add P_t * sink_v[t] for the sink positions (block A's lanes)
+            const T* svb = static_cast<const T*>(a.sink_v);
+            for (int t = 0; t < a.n_sink && t < ctx; ++t) {
+                const int src = (t & 7) * 4 + c;
+                const float pa = __shfl_sync(0xffffffffu, t < 8 ? p0 : p2, src);
+                const float pb = __shfl_sync(0xffffffffu, t < 8 ? p1 : p3, src);
+                if (sl != 0) continue;
+                const T* vrow = svb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D;
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int el = pv_e<NG, MT>(mt, 0), eh = pv_e<NG, MT>(mt, 1);
+                    const float u = (el & 1) ? 16.f * kInvTwo24 : kInvTwo24;
+                    const float vl = tofloat(vrow[pv_column<NG, D>(el, g)]) * u;
+                    const float vh = tofloat(vrow[pv_column<NG, D>(eh, g)]) * u;
+                    o[mt][0] += pa * vl;
+                    o[mt][1] += pb * vl;
+                    o[mt][2] += pa * vh;
+                    o[mt][3] += pb * vh;
+                }
+            }
+        }
+    };
+
+    // ---- the quantised blocks, two per step
+    const int qlim = WIN ? min(lb_end, win_lb0) : lb_end;
+    const int nq = qlim > lb_first ? (qlim - lb_first + stride - 1) / stride : 0;
+    int tab = 0;
+    for (int i = 0; i < nq; i += 2) {
+        const int lb = lb_first + i * stride;
+        if ((i & 31) == 0) {  // i is even: a step's two entries never straddle a refill
+            const int idx = lb + stride * lane;
+            tab = idx < lb_end ? trow[idx] : -1;
+        }
+        const int physA = __shfl_sync(0xffffffffu, tab, i & 31);
+        const int physB = __shfl_sync(0xffffffffu, tab, (i + 1) & 31);
+        const bool hasB = i + 1 < nq;
+        const bool vA = static_cast<unsigned>(physA) < static_cast<unsigned>(a.num_blocks);
+        const bool vB = hasB && static_cast<unsigned>(physB) < static_cast<unsigned>(a.num_blocks);
+        if (lane == 0 && (!vA || (hasB && !vB))) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
+        if (!vA && !vB) continue;
+        // a missing or bad block reads the other one's codes (finite), masked
+        const int pA = vA ? physA : physB, pB = vB ? physB : pA;
+        Codes CA, CB;
+        Scales S;
+        load_codes(pA, CA);
+        load_codes(pB, CB);
+        load_scales(sl ? pB : pA, S);
+        attend_pair(lb, vA, vB, CA, CB, S);
+    }
+
+    // ---- merge the two column halves: lane c (< 2) and lane c + 2 hold the
+    // same query heads, token lanes and output columns for blocks A and B;
+    // after the exchange both hold the merged state (lanes c >= 2 then stand
+    // for the padding heads 4-7, as in the single-block layout)
+    {
+        const float pm0 = __shfl_xor_sync(0xffffffffu, m0, 2), pm1 = __shfl_xor_sync(0xffffffffu, m1, 2);
+        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+        const bool e0 = M0 == neg_inf(), e1 = M1 == neg_inf();
+        const float sa0 = e0 ? 0.f : ex2(m0 - M0), sb0 = e0 ? 0.f : ex2(pm0 - M0);
+        const float sa1 = e1 ? 0.f : ex2(m1 - M1), sb1 = e1 ? 0.f : ex2(pm1 - M1);
+        const float pl0 = __shfl_xor_sync(0xffffffffu, l0, 2), pl1 = __shfl_xor_sync(0xffffffffu, l1, 2);
+        l0 = l0 * sa0 + pl0 * sb0;
+        l1 = l1 * sa1 + pl1 * sb1;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            const float pc0 = __shfl_xor_sync(0xffffffffu, corr[gi][0], 2);
+            const float pc1 = __shfl_xor_sync(0xffffffffu, corr[gi][1], 2);
+            corr[gi][0] = corr[gi][0] * sa0 + pc0 * sb0;
+            corr[gi][1] = corr[gi][1] * sa1 + pc1 * sb1;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const float q0 = __shfl_xor_sync(0xffffffffu, o[mt][0], 2);
+            const float q1 = __shfl_xor_sync(0xffffffffu, o[mt][1], 2);
+            const float q2 = __shfl_xor_sync(0xffffffffu, o[mt][2], 2);
+            const float q3 = __shfl_xor_sync(0xffffffffu, o[mt][3], 2);
+            o[mt][0] = o[mt][0] * sa0 + q0 * sb0;
+            o[mt][1] = o[mt][1] * sa1 + q1 * sb1;
+            o[mt][2] = o[mt][2] * sa0 + q2 * sb0;
+            o[mt][3] = o[mt][3] * sa1 + q3 * sb1;
+        }
+        m0 = M0;
+        m1 = M1;
+    }
+    // ---- the 16-bit window blocks (the pass's last ones), one at a time
+    if constexpr (WIN) {
+        for (int lb = lb_first + nq * stride; lb < lb_end; lb += stride) attend16(lb);
+    }
+}
+
 // One warp's pass over the blocks lb_first, lb_first + stride, ... < lb_end
 // of sequence b, KV head kvh (context ctx): query fragments, then every block
 // loaded into registers and attended into st (reset first).  sq is the
 // lane's slot of the warp's shared query slice (row t at sq[t * 32]).
-template <typename T, int D, int QMODE, int NG, bool WIN>
+//
+// PAIR (INT4, G <= 4): two blocks per step, one in each half of the MMA's
+// eight query columns.  The GQA group fills at most four of them, so block A
+// takes columns 0-3 and block B columns 4-7: its QK^T MMAs see the query in
+// columns 4-7 and zeros in 0-3 (and A's the other way round), both add into
+// one accumulator, and every lane's four logits are live -- lanes c = 0, 1
+// hold block A's (tokens g, g + 8; heads 2c, 2c + 1), lanes c = 2, 3 block
+// B's.  The whole scalar part of a step (scales, zero points, softmax, PV
+// weights) then runs once for two blocks.  The two halves are two
+// independent online softmaxes (even and odd blocks of the pass), each PV
+// weight fragment is split by its column half into one MMA per block, and
+// the halves are merged (log-sum-exp) before the window blocks and at the
+// end.  The query slice holds two copies: columns 0-3 live (stream A) and
+// columns 4-7 live (stream B), row t of copy s at sq[(s KSTEPS / 2 + t) 32].
+template <typename T, int D, int QMODE, int NG, bool WIN, bool PAIR = false>
 __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh, int ctx, int lb_first,
                                            int lb_end, int stride, uint4* sq, QState<D / 16, NG>& st) {
     constexpr bool INT4 = QMODE == PKV_QMODE_INT4_ASYM;
@@ -183,8 +539,13 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     constexpr int KPG = KW / NG;
     constexpr int VPG = VW / NG;
     static_assert(NG == 1 || (INT4 && D == 128 && NG == 2), "groups: one per head, or 64 columns at D 128");
+    static_assert(!PAIR || INT4, "paired blocks: INT4 only");
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    // hh: the lane's S / O columns are query heads 2 hh, 2 hh + 1 (of its
+    // stream when PAIR); qh: the query head whose B-fragment column it feeds
+    const int hh = PAIR ? (c & 1) : c;
+    const int qh = PAIR ? (g & 3) : g;
 
     // ---- query fragments (fp16) in the permuted k order of the code layout
     // staged in this warp's shared slice (k-steps 2t, 2t + 1 of lane l at
@@ -195,8 +556,8 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     for (int gi = 0; gi < NG; ++gi) qsum[gi] = 0.f;
     {
         const T* qrow = static_cast<const T*>(a.q) +
-                        (static_cast<int64_t>(b) * a.hq + kvh * a.G + (g < a.G ? g : 0)) * D;
-        const bool valid = g < a.G;
+                        (static_cast<int64_t>(b) * a.hq + kvh * a.G + (qh < a.G ? qh : 0)) * D;
+        const bool valid = qh < a.G;
         if constexpr (INT4) {
             // K word k of lane c covers the 8 columns starting at
             // (k / KPG) GS + (GS / 4) c + 8 (k % KPG): lane c holds a quarter
@@ -241,19 +602,27 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     __syncwarp();  // the previous pass no longer reads the slice
     if constexpr (kQueryInShared<QMODE>) {
 #pragma unroll
-        for (int t = 0; t < KSTEPS / 2; ++t)
-            sq[t * 32] = make_uint4(qf[2 * t][0], qf[2 * t][1], qf[2 * t + 1][0], qf[2 * t + 1][1]);
+        for (int t = 0; t < KSTEPS / 2; ++t) {
+            const uint4 v = make_uint4(qf[2 * t][0], qf[2 * t][1], qf[2 * t + 1][0], qf[2 * t + 1][1]);
+            if constexpr (PAIR) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                sq[t * 32] = g < 4 ? v : z;
+                sq[(KSTEPS / 2 + t) * 32] = g < 4 ? z : v;
+            } else {
+                sq[t * 32] = v;
+            }
+        }
         __syncwarp();
     }
     const uint32_t qs = static_cast<uint32_t>(__cvta_generic_to_shared(sq));
-    float qs0[NG], qs1[NG];  // group sums of heads 2c, 2c + 1
+    float qs0[NG], qs1[NG];  // group sums of heads 2 hh, 2 hh + 1
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
         float x = qsum[gi];
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
-        qs0[gi] = __shfl_sync(0xffffffffu, x, (2 * c) * 4);
-        qs1[gi] = __shfl_sync(0xffffffffu, x, (2 * c + 1) * 4);
+        qs0[gi] = __shfl_sync(0xffffffffu, x, (2 * hh) * 4);
+        qs1[gi] = __shfl_sync(0xffffffffu, x, (2 * hh + 1) * 4);
     }
 
     float& m0 = st.m0;
@@ -426,7 +795,7 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
                 if (t < a.n_sink) {
                     const T* krow = skb + ((static_cast<int64_t>(b) * a.n_sink + t) * a.hkv + kvh) * D;
                     float d0 = 0.f, d1 = 0.f;
-                    const int h0 = min(2 * c, a.G - 1), h1 = min(2 * c + 1, a.G - 1);
+                    const int h0 = min(2 * hh, a.G - 1), h1 = min(2 * hh + 1, a.G - 1);
                     for (int d = 0; d < D; ++d) {
                         const float kv = tofloat(krow[d]);
                         d0 += tofloat(qbase[h0 * D + d]) * kv;
@@ -706,6 +1075,12 @@ __device__ __forceinline__ void quant_pass(const QDecodeArgs& a, int b, int kvh,
     // kernels built for calls with a window; the others carry no such code)
     const int win_lb0 = WIN ? max(ctx - a.window, 0) / BS : 0x7fffffff;
 
+    if constexpr (PAIR) {
+        quant_pairs<T, D, NG, WIN>(a, b, kvh, ctx, lb_first, lb_end, stride, win_lb0, qs, qs0, qs1, st,
+                                   attend16);
+        return;
+    }
+
     // Lane j holds the physical id of the pass's j-th upcoming block (32 at
     // a time), so a block's loads never wait behind a table load.
     int tab = 0;
@@ -775,8 +1150,8 @@ __device__ __forceinline__ void out_columns(int mt, int g, int& dl, int& dh) {
 // Partition kernel: one CTA of NW warps per (partition, KV head, sequence);
 // the warps take the partition's blocks round-robin and merge through
 // shared memory.
-template <typename T, int D, int QMODE, int NG, bool WIN, bool SPLIT>
-__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_quant_kernel(QDecodeArgs a) {
+template <typename T, int D, int QMODE, int NG, bool WIN, bool SPLIT, bool PAIR>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG, PAIR>) paged_decode_quant_kernel(QDecodeArgs a) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
     const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -795,9 +1170,10 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_q
     const int blk_begin = p * a.part_blocks;
     const int blk_end = min(blk_begin + a.part_blocks, nblk);
 
-    __shared__ uint4 sq[NW][KSTEPS / 2][32];
+    __shared__ uint4 sq[NW][PAIR ? 2 : 1][KSTEPS / 2][32];
     QState<MT, NG> st;
-    quant_pass<T, D, QMODE, NG, WIN>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][lane], st);
+    quant_pass<T, D, QMODE, NG, WIN, PAIR>(a, b, kvh, ctx, blk_begin + warp, blk_end, NW, &sq[warp][0][0][lane],
+                                           st);
     quant_finish<D, QMODE, NG>(st);
     const float m0 = st.m0, m1 = st.m1, l0 = st.l0, l1 = st.l1;
     auto& o = st.o;
@@ -852,8 +1228,8 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>) paged_decode_q
 // Balanced split for the quantised cache (the split itself: balanced.cuh):
 // warp i walks its range run by run, one pass per run segment, and writes
 // the run's partial.  No barrier.
-template <typename T, int D, int QMODE, int NG, bool WIN>
-__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
+template <typename T, int D, int QMODE, int NG, bool WIN, bool PAIR>
+__global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG, PAIR>)
     paged_decode_quant_balanced_kernel(QDecodeArgs a, int batch, int nwt_launch) {
     constexpr int KSTEPS = D / 16;
     constexpr int MT = D / 16;
@@ -861,7 +1237,7 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     const int g = lane >> 2, c = lane & 3;
     // the merge grid may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;");
-    __shared__ uint4 sq[NW][KSTEPS / 2][32];
+    __shared__ uint4 sq[NW][PAIR ? 2 : 1][KSTEPS / 2][32];
     __shared__ __align__(16) float sm_o[NW][8][D];
 
     const int i = blockIdx.x * NW + warp;
@@ -873,7 +1249,8 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     if (!any) return;
     while (sp.next()) {
         QState<MT, NG> st;
-        quant_pass<T, D, QMODE, NG, WIN>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][lane], st);
+        quant_pass<T, D, QMODE, NG, WIN, PAIR>(a, sp.b, sp.kvh, sp.ctx, sp.lb0, sp.lb1, 1, &sq[warp][0][0][lane],
+                                               st);
         quant_finish<D, QMODE, NG>(st);
         // partial (m, l, o) of this run: o staged through shared memory so
         // the G x D rows go out in 16-byte stores
@@ -906,18 +1283,40 @@ __global__ void __launch_bounds__(NW * 32, kCtasPerSm<QMODE, NG>)
     }
 }
 
+// Whether a call takes the paired-block pass (INT4 with at most 4 query
+// heads per KV head: two blocks fit the MMA's 8 query columns).
+inline bool use_pairs(int qmode, int G) { return qmode == PKV_QMODE_INT4_ASYM && G <= 4; }
+
+template <typename T, int D, int QMODE, int NG, bool PAIR>
+void launch_balanced_w(const QDecodeArgs& a, int batch, int nwt, cudaStream_t st) {
+    const dim3 grid((nwt + NW - 1) / NW);
+    if (a.window > 0)
+        paged_decode_quant_balanced_kernel<T, D, QMODE, NG, true, PAIR><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
+    else
+        paged_decode_quant_balanced_kernel<T, D, QMODE, NG, false, PAIR><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
+}
+
 template <typename T, int D, int QMODE, int NG>
 void launch_balanced(const QDecodeArgs& a, int batch, int nwt, cudaStream_t st) {
-    const dim3 grid((nwt + NW - 1) / NW);
-    if (a.window > 0) paged_decode_quant_balanced_kernel<T, D, QMODE, NG, true><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
-    else paged_decode_quant_balanced_kernel<T, D, QMODE, NG, false><<<grid, NW * 32, 0, st>>>(a, batch, nwt);
+    if constexpr (QMODE == PKV_QMODE_INT4_ASYM) {
+        if (use_pairs(QMODE, a.G)) return launch_balanced_w<T, D, QMODE, NG, true>(a, batch, nwt, st);
+    }
+    launch_balanced_w<T, D, QMODE, NG, false>(a, batch, nwt, st);
+}
+
+template <typename T, int D, int QMODE, int NG, bool SPLIT, bool PAIR>
+void launch_w(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
+    dim3 grid(SPLIT ? parts : 1, hkv, batch);
+    if (a.window > 0) paged_decode_quant_kernel<T, D, QMODE, NG, true, SPLIT, PAIR><<<grid, NW * 32, 0, st>>>(a);
+    else paged_decode_quant_kernel<T, D, QMODE, NG, false, SPLIT, PAIR><<<grid, NW * 32, 0, st>>>(a);
 }
 
 template <typename T, int D, int QMODE, int NG, bool SPLIT>
 void launch(const QDecodeArgs& a, int parts, int hkv, int batch, cudaStream_t st) {
-    dim3 grid(SPLIT ? parts : 1, hkv, batch);
-    if (a.window > 0) paged_decode_quant_kernel<T, D, QMODE, NG, true, SPLIT><<<grid, NW * 32, 0, st>>>(a);
-    else paged_decode_quant_kernel<T, D, QMODE, NG, false, SPLIT><<<grid, NW * 32, 0, st>>>(a);
+    if constexpr (QMODE == PKV_QMODE_INT4_ASYM) {
+        if (use_pairs(QMODE, a.G)) return launch_w<T, D, QMODE, NG, SPLIT, true>(a, parts, hkv, batch, st);
+    }
+    launch_w<T, D, QMODE, NG, SPLIT, false>(a, parts, hkv, batch, st);
 }
 
 // The kernel for (dtype, head dim, mode, column groups); balanced or
@@ -1023,9 +1422,11 @@ extern "C" int pkv_paged_attention_decode_quant(
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (partition_size == 0 && a.max_parts > 1 && pkv::use_balanced(batch, num_kv_heads, max_blocks)) {
         // balanced split, all CTAs resident: kCtasPerSm CTAs of NW warps per SM
-        const int per_sm = pkv::NW * (qmode != PKV_QMODE_INT4_ASYM ? pkv::kCtasPerSm<PKV_QMODE_FP8_E4M3>
-                                      : ng == 2 ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 2>
-                                                : pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 1>);
+        const int per_sm =
+            pkv::NW * (qmode != PKV_QMODE_INT4_ASYM ? pkv::kCtasPerSm<PKV_QMODE_FP8_E4M3>
+                       : pkv::use_pairs(qmode, a.G) ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 1, true>
+                       : ng == 2                    ? pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 2>
+                                                    : pkv::kCtasPerSm<PKV_QMODE_INT4_ASYM, 1>);
         const int nwt = pkv::balanced_warps(static_cast<int64_t>(batch) * num_kv_heads * max_blocks, per_sm);
         const size_t rows = static_cast<size_t>(nwt) * a.G + static_cast<size_t>(batch) * num_q_heads;
         if (!workspace || workspace_bytes < pkv::balanced_bytes(batch, num_q_heads, a.G, head_dim, nwt))
