@@ -199,59 +199,76 @@ __device__ __forceinline__ void quant_pairs(const QDecodeArgs& a, int b, int kvh
     struct Scales {
         __half2 ks[NG], vs[NG], kz[NG], vz[NG];  // low: token g, high: token g + 8
     };
+    // Per-lane base addresses for this pass's KV head; a block adds
+    // phys x (the pool's bytes per block) with one widening multiply-add,
+    // and every load of the block is an immediate offset from it.
+    const uint32_t code_stride = static_cast<uint32_t>(a.hkv) * (BS * CB);      // bytes per pool block
+    const uint32_t scale_stride = static_cast<uint32_t>(a.hkv) * (BS * NG * 2);  // bytes per pool block
+    const uint8_t* kbase = a.k_codes + static_cast<uint32_t>(kvh) * (BS * CB) + g * CB +
+                           (NG == 2 ? 8 * c : (KW == 4 ? 16 * c : 8 * c));
+    const uint8_t* vbase = a.v_codes + static_cast<uint32_t>(kvh) * (BS * CB) + vr0 * CB +
+                           (NG == 2 ? 4 * g : DS / 2 * g);
+    const uint32_t soff = (static_cast<uint32_t>(kvh) * BS + g) * (NG * 2);  // bytes, token g
+    const uint8_t* ksb = reinterpret_cast<const uint8_t*>(a.k_scale) + soff;
+    const uint8_t* vsb = reinterpret_cast<const uint8_t*>(a.v_scale) + soff;
+    const uint8_t* kzb = reinterpret_cast<const uint8_t*>(a.k_zero) + soff;
+    const uint8_t* vzb = reinterpret_cast<const uint8_t*>(a.v_zero) + soff;
+    auto at = [](const uint8_t* base, int phys, uint32_t stride) {
+        return base + static_cast<uint64_t>(static_cast<uint32_t>(phys)) * stride;
+    };
     auto load_codes = [&](int phys, Codes& C) {
-        const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;
-        const uint8_t* kc = a.k_codes + bh * (BS * CB);
-        const uint8_t* vc = a.v_codes + bh * (BS * CB);
+        const uint8_t* kc = at(kbase, phys, code_stride);  // row g, this lane's columns
+        const uint8_t* vc = at(vbase, phys, code_stride);  // row 2c, this lane's columns
+        // V rows 2c + 1, 8 + 2c, 9 + 2c are 1, 8, 9 rows further
         if constexpr (NG == 2) {
 #pragma unroll
             for (int gi = 0; gi < 2; ++gi) {
-                const uint2 r0 = ldg_stream8(kc + g * CB + 32 * gi + 8 * c);
-                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 32 * gi + 8 * c);
+                const uint2 r0 = ldg_stream8(kc + 32 * gi);
+                const uint2 r1 = ldg_stream8(kc + 8 * CB + 32 * gi);
                 C.kw0[2 * gi] = r0.x; C.kw0[2 * gi + 1] = r0.y;
                 C.kw1[2 * gi] = r1.x; C.kw1[2 * gi + 1] = r1.y;
-                const int off = 32 * gi + 4 * g;
-                C.vw[0][gi] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
-                C.vw[1][gi] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
-                C.vw[2][gi] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
-                C.vw[3][gi] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+                C.vw[0][gi] = *reinterpret_cast<const uint32_t*>(vc + 32 * gi);
+                C.vw[1][gi] = *reinterpret_cast<const uint32_t*>(vc + CB + 32 * gi);
+                C.vw[2][gi] = *reinterpret_cast<const uint32_t*>(vc + 8 * CB + 32 * gi);
+                C.vw[3][gi] = *reinterpret_cast<const uint32_t*>(vc + 9 * CB + 32 * gi);
             }
         } else {
             if constexpr (KW == 4) {
-                const uint4 r0 = ldg_stream(kc + g * CB + 16 * c);
-                const uint4 r1 = ldg_stream(kc + (g + 8) * CB + 16 * c);
+                const uint4 r0 = ldg_stream(kc);
+                const uint4 r1 = ldg_stream(kc + 8 * CB);
                 C.kw0[0] = r0.x; C.kw0[1] = r0.y; C.kw0[2] = r0.z; C.kw0[3] = r0.w;
                 C.kw1[0] = r1.x; C.kw1[1] = r1.y; C.kw1[2] = r1.z; C.kw1[3] = r1.w;
             } else {
-                const uint2 r0 = ldg_stream8(kc + g * CB + 8 * c);
-                const uint2 r1 = ldg_stream8(kc + (g + 8) * CB + 8 * c);
+                const uint2 r0 = ldg_stream8(kc);
+                const uint2 r1 = ldg_stream8(kc + 8 * CB);
                 C.kw0[0] = r0.x; C.kw0[1] = r0.y;
                 C.kw1[0] = r1.x; C.kw1[1] = r1.y;
             }
-            const int off = DS / 2 * g;
             if constexpr (VW == 2) {
-                const uint2 x0 = ldg_stream8(vc + vr0 * CB + off), x1 = ldg_stream8(vc + vr1 * CB + off);
-                const uint2 x2 = ldg_stream8(vc + vr2 * CB + off), x3 = ldg_stream8(vc + vr3 * CB + off);
+                const uint2 x0 = ldg_stream8(vc), x1 = ldg_stream8(vc + CB);
+                const uint2 x2 = ldg_stream8(vc + 8 * CB), x3 = ldg_stream8(vc + 9 * CB);
                 C.vw[0][0] = x0.x; C.vw[0][1] = x0.y; C.vw[1][0] = x1.x; C.vw[1][1] = x1.y;
                 C.vw[2][0] = x2.x; C.vw[2][1] = x2.y; C.vw[3][0] = x3.x; C.vw[3][1] = x3.y;
             } else {
-                C.vw[0][0] = *reinterpret_cast<const uint32_t*>(vc + vr0 * CB + off);
-                C.vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + vr1 * CB + off);
-                C.vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + vr2 * CB + off);
-                C.vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + vr3 * CB + off);
+                C.vw[0][0] = *reinterpret_cast<const uint32_t*>(vc);
+                C.vw[1][0] = *reinterpret_cast<const uint32_t*>(vc + CB);
+                C.vw[2][0] = *reinterpret_cast<const uint32_t*>(vc + 8 * CB);
+                C.vw[3][0] = *reinterpret_cast<const uint32_t*>(vc + 9 * CB);
             }
         }
     };
     // the scales and zero points of the lane's own block (tokens g, g + 8)
     auto load_scales = [&](int phys, Scales& S) {
-        const int64_t bh = static_cast<int64_t>(phys) * a.hkv + kvh;
-        const int64_t s0 = (bh * BS + g) * NG, s1 = (bh * BS + g + 8) * NG;
+        const __half* ks = reinterpret_cast<const __half*>(at(ksb, phys, scale_stride));
+        const __half* vs = reinterpret_cast<const __half*>(at(vsb, phys, scale_stride));
+        const __half* kz = reinterpret_cast<const __half*>(at(kzb, phys, scale_stride));
+        const __half* vz = reinterpret_cast<const __half*>(at(vzb, phys, scale_stride));
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
-            S.ks[gi] = __halves2half2(a.k_scale[s0 + gi], a.k_scale[s1 + gi]);
-            S.vs[gi] = __halves2half2(a.v_scale[s0 + gi], a.v_scale[s1 + gi]);
-            S.kz[gi] = __halves2half2(a.k_zero[s0 + gi], a.k_zero[s1 + gi]);
-            S.vz[gi] = __halves2half2(a.v_zero[s0 + gi], a.v_zero[s1 + gi]);
+            S.ks[gi] = __halves2half2(ks[gi], ks[8 * NG + gi]);
+            S.vs[gi] = __halves2half2(vs[gi], vs[8 * NG + gi]);
+            S.kz[gi] = __halves2half2(kz[gi], kz[8 * NG + gi]);
+            S.vz[gi] = __halves2half2(vz[gi], vz[8 * NG + gi]);
         }
     };
     // PV A fragment of element e (token pair pr) from a block's V words
@@ -387,16 +404,13 @@ __device__ __forceinline__ void quant_pairs(const QDecodeArgs& a, int b, int kvh
             const float W2 = w1 ? p2 * vs1 : 0.f, W3 = w1 ? p3 * vs1 : 0.f;
             const uint32_t pk0 = f16pair(W0, W1), pk1 = f16pair(W2, W3);
             const float vz0 = __low2float(S.vz[gi]), vz1 = __high2float(S.vz[gi]);
+            // masked tokens carry W = 0, but their zero point may be any
+            // bits (slots never written): it is selected away, not multiplied
+            const float zm0 = w0 ? vz0 : 0.f, zm1 = w1 ? vz1 : 0.f;
             const __half2 h0 = *reinterpret_cast<const __half2*>(&pk0);
             const __half2 h1 = *reinterpret_cast<const __half2*>(&pk1);
-            if (w0) {
-                corr[gi][0] += __low2float(h0) * vz0;
-                corr[gi][1] += __high2float(h0) * vz0;
-            }
-            if (w1) {
-                corr[gi][0] += __low2float(h1) * vz1;
-                corr[gi][1] += __high2float(h1) * vz1;
-            }
+            corr[gi][0] += __low2float(h0) * zm0 + __low2float(h1) * zm1;
+            corr[gi][1] += __high2float(h0) * zm0 + __high2float(h1) * zm1;
             const uint32_t t0w = movmatrix_trans(pk0), t1w = movmatrix_trans(pk1);
             wa0[gi] = g < 4 ? t0w : 0u;
             wa1[gi] = g < 4 ? t1w : 0u;
@@ -442,10 +456,15 @@ __device__ __forceinline__ void quant_pairs(const QDecodeArgs& a, int b, int kvh
     const int qlim = WIN ? min(lb_end, win_lb0) : lb_end;
     const int nq = qlim > lb_first ? (qlim - lb_first + stride - 1) / stride : 0;
     int tab = 0;
-    for (int i = 0; i < nq; i += 2) {
-        const int lb = lb_first + i * stride;
-        if ((i & 31) == 0) {  // i is even: a step's two entries never straddle a refill
-            const int idx = lb + stride * lane;
+    // Step k (blocks 2k, 2k + 1 of the pass): the physical ids its loads
+    // read -- a missing or bad block reads the other one's bytes, or block
+    // 0's (finite, masked) -- and its validity bits (1: A, 2: B).  The
+    // table window of 32 entries is refilled at multiples of 32 blocks; a
+    // step's two entries never straddle a refill.
+    auto step_ids = [&](int k, int& pA, int& pB) {
+        const int i = 2 * k;
+        if ((i & 31) == 0) {
+            const int idx = lb_first + stride * (i + lane);
             tab = idx < lb_end ? trow[idx] : -1;
         }
         const int physA = __shfl_sync(0xffffffffu, tab, i & 31);
@@ -454,15 +473,21 @@ __device__ __forceinline__ void quant_pairs(const QDecodeArgs& a, int b, int kvh
         const bool vA = static_cast<unsigned>(physA) < static_cast<unsigned>(a.num_blocks);
         const bool vB = hasB && static_cast<unsigned>(physB) < static_cast<unsigned>(a.num_blocks);
         if (lane == 0 && (!vA || (hasB && !vB))) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
-        if (!vA && !vB) continue;
-        // a missing or bad block reads the other one's codes (finite), masked
-        const int pA = vA ? physA : physB, pB = vB ? physB : pA;
+        pA = vA ? physA : (vB ? physB : 0);
+        pB = vB ? physB : pA;
+        return (vA ? 1 : 0) | (vB ? 2 : 0);
+    };
+    const int nsteps = (nq + 1) / 2;
+    for (int k = 0; k < nsteps; ++k) {
+        int pA, pB;
+        const int f = step_ids(k, pA, pB);
+        if (!f) continue;
         Codes CA, CB;
         Scales S;
         load_codes(pA, CA);
         load_codes(pB, CB);
         load_scales(sl ? pB : pA, S);
-        attend_pair(lb, vA, vB, CA, CB, S);
+        attend_pair(lb_first + 2 * k * stride, (f & 1) != 0, (f & 2) != 0, CA, CB, S);
     }
 
     // ---- merge the two column halves: lane c (< 2) and lane c + 2 hold the

@@ -704,16 +704,53 @@ __global__ void __launch_bounds__(kMergeThreads) multi_query_merge_kernel(
     }
     // partials are produced by the preceding grid: wait for it
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int x = tid; x < rows * D; x += kMergeThreads) {
-        const int r = x / D, d = x - r * D;
-        const int tok = r / G, h = r - tok * G;
-        float v = 0.f;
-        if (np > 0) {
-            const MergeAcc m = merge_range(ws_ml + (slot0 * R + r) * 2, 2 * R, ws_o + (slot0 * R + r) * D + d,
-                                           static_cast<int64_t>(R) * D, 0, np, 1);
-            v = m.L > 0.f ? m.acc / m.L : 0.f;
+    // 1. per row: M = max_p m_p and 1 / L, L = sum_p l_p 2^(m_p - M) (one
+    // warp per row, lanes over the partials)
+    __shared__ float rowM[R], rowInv[R];
+    const float* ml = ws_ml + slot0 * R * 2;  // partial p, row r: ml[(p R + r) 2 + {0, 1}]
+    for (int r = warp; r < rows; r += NWARP) {
+        float M = neg_inf();
+        for (int p = lane; p < np; p += 32) M = fmaxf(M, __ldcg(ml + (static_cast<int64_t>(p) * R + r) * 2));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        if (M != neg_inf()) {
+            for (int p = lane; p < np; p += 32) {
+                const float* e = ml + (static_cast<int64_t>(p) * R + r) * 2;
+                L += __ldcg(e + 1) * ex2(__ldcg(e) - M);
+            }
         }
-        out[((static_cast<int64_t>(q0) + tok) * hq + kvh * G + h) * D + d] = Half16<T>::from_float(v);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        if (lane == 0) {
+            rowM[r] = M;
+            rowInv[r] = L > 0.f ? 1.f / L : 0.f;
+        }
+    }
+    __syncthreads();
+    // 2. out[r, d..d+3] = sum_p 2^(m_p - M) o_p[r, d..d+3] / L: 16-byte
+    // partial loads (the threads of a row share each m_p load)
+    constexpr int D4 = D / 4;
+    for (int x = tid; x < rows * D4; x += kMergeThreads) {
+        const int r = x / D4, d = (x - r * D4) * 4;
+        const int tok = r / G, h = r - tok * G;
+        const float M = rowM[r], inv = rowInv[r];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (inv > 0.f) {
+            for (int p = 0; p < np; ++p) {
+                const int64_t row = (slot0 + p) * R + r;
+                const float w = ex2(__ldcg(ws_ml + row * 2) - M);
+                const float4 o = __ldcg(reinterpret_cast<const float4*>(ws_o + row * D + d));
+                acc.x += w * o.x;
+                acc.y += w * o.y;
+                acc.z += w * o.z;
+                acc.w += w * o.w;
+            }
+        }
+        uint2 v;
+        v.x = Half16<T>::pack(acc.x * inv, acc.y * inv);
+        v.y = Half16<T>::pack(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2*>(out + ((static_cast<int64_t>(q0) + tok) * hq + kvh * G + h) * D + d) = v;
     }
 }
 
