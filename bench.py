@@ -158,6 +158,7 @@ def parse_args():
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="override the pool size (blocks); 0 keeps the workload's")
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--clock-worker", nargs=3, default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
 
@@ -219,118 +220,137 @@ def recorded_traffic(workload, kv_bytes_per_launch):
     return per_kv_byte * kv_bytes_per_launch
 
 
+# clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+CLOCK_REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+                 (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+
+def clock_worker(device, period_s, out_path):
+    """Sampling process: read-only NVML queries of the SM clock, power and
+    active clock-event reasons every period_s until SIGTERM, one line each
+    ("monotonic_s mhz watts reasons") to out_path; the first line is the
+    device's maximum SM clock.  It runs in its own interpreter so the
+    launching process's GIL never delays a sample."""
+    import ctypes
+    import signal
+    stop = []
+    signal.signal(signal.SIGTERM, lambda *_: stop.append(1))
+    lib = ctypes.CDLL("libnvidia-ml.so.1")
+    if lib.nvmlInit_v2() != 0:
+        raise SystemExit("nvmlInit_v2 failed")
+    h = ctypes.c_void_p()
+    if not (device.startswith("GPU-") and lib.nvmlDeviceGetHandleByUUID(device.encode(), ctypes.byref(h)) == 0):
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(device) if device.isdigit() else 0),
+                                             ctypes.byref(h)) != 0:
+            raise SystemExit("no NVML handle")
+    reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+        lib.nvmlDeviceGetCurrentClocksThrottleReasons
+    mx, mhz, mw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+    lines = ["max %d" % mx.value]
+    for _ in range(3):  # the first queries are the slow ones: before "ready"
+        lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))
+        reasons_fn(h, ctypes.byref(rs))
+        lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+    with open(out_path + ".ready", "w") as f:
+        f.write("1")
+    n = 0
+    while not stop:
+        ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0
+        reasons_fn(h, ctypes.byref(rs))
+        if n % 8 == 0:  # power changes slowly: one read in eight
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+        n += 1
+        if ok:
+            lines.append("%.6f %d %.3f %d" % (time.monotonic(), mhz.value, mw.value / 1000.0, rs.value))
+        if period_s >= 1e-3:
+            time.sleep(period_s)
+    with open(out_path, "w") as f:
+        f.write("\n".join(lines) + "\n")
+
+
 class ClockSampler:
-    """SM clock, power and clock-event reasons, read in-process from NVML
-    (read-only queries) by a background thread every ``period_s`` seconds.
+    """SM clock, power and clock-event reasons during the timed region.
 
-    The sampler runs across the warm-up and the timed loop; ``mark_start`` /
-    ``mark_end`` bracket the timed region, and the summary is taken over the
-    samples inside it (a 20-step region lasts about 2 ms, so the period is a
-    fraction of a millisecond).  NVML is reached through ctypes on the
-    driver's ``libnvidia-ml.so.1``; when it cannot be loaded the summary says
-    so and holds no samples."""
-
-    # clock-event reason bits (nvml.h, nvmlClocksEventReason*)
-    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
-               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+    A separate sampling process (``clock_worker``) reads NVML every
+    ``period_s`` from before the warm-up until ``stop``; ``mark_start`` /
+    ``mark_end`` bracket the timed region (CLOCK_MONOTONIC, shared by both
+    processes) and the summary is taken over the samples inside it.  A
+    20-step region lasts about 2 ms, hence the sub-millisecond period.  Without
+    NVML the summary says so and holds no samples."""
 
     def __init__(self, device_index, period_s=0.0002):
-        import ctypes
-        import threading
-        self.ct, self.period, self.samples = ctypes, period_s, []
-        self.lib, self.handle, self.error = None, None, None
+        self.period = period_s
         self.t_start = self.t_end = None
-        self._stop = threading.Event()
-        self._thread = None
-        try:
-            lib = ctypes.CDLL("libnvidia-ml.so.1")
-            if lib.nvmlInit_v2() != 0:
-                raise RuntimeError("nvmlInit_v2 failed")
-            handle = ctypes.c_void_p()
-            uuid = self._uuid(device_index)
-            ok = uuid is not None and lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) == 0
-            if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index),
-                                                            ctypes.byref(handle)) != 0:
-                raise RuntimeError("no NVML handle for device %d" % device_index)
-            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                lib.nvmlDeviceGetCurrentClocksThrottleReasons
-            mx = ctypes.c_uint(0)
-            lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
-            self.sm_max = float(mx.value) or None
-            self.lib, self.handle = lib, handle
-        except Exception as e:  # no NVML: the summary records why
-            self.error = str(e)
-
-    @staticmethod
-    def _uuid(device_index):
+        self.proc, self.error = None, None
+        self.path = os.path.join("/tmp", "pkv_clocks_%d_%d.txt" % (os.getpid(), device_index))
         try:
             import torch
             u = str(torch.cuda.get_device_properties(device_index).uuid)
-            return u if u.startswith("GPU-") else "GPU-" + u
+            self.device = u if u.startswith("GPU-") else "GPU-" + u
         except Exception:
-            return None
-
-    def _read(self):
-        ct, lib, h = self.ct, self.lib, self.handle
-        mhz, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
-        ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0
-        lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
-        self.reasons_fn(h, ct.byref(rs))
-        if ok:
-            self.samples.append((time.perf_counter(), float(mhz.value), mw.value / 1000.0, rs.value))
-
-    def _loop(self):
-        while not self._stop.is_set():
-            self._read()
-            time.sleep(self.period)
+            self.device = str(device_index)
 
     def start(self):
-        if self.lib is None:
-            return
-        import threading
-        # the launch loop holds the GIL between its calls: a short switch
-        # interval lets the sampling thread in every fraction of a millisecond
-        self._switch = sys.getswitchinterval()
-        sys.setswitchinterval(self.period / 2)
-        self._thread = threading.Thread(target=self._loop, daemon=True)
-        self._thread.start()
+        try:
+            self.proc = subprocess.Popen([sys.executable, os.path.abspath(__file__), "--clock-worker",
+                                          self.device, str(self.period), self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.PIPE)
+            t0 = time.monotonic()
+            while not os.path.exists(self.path + ".ready"):  # NVML up before the warm-up
+                if self.proc.poll() is not None or time.monotonic() - t0 > 20:
+                    raise RuntimeError("clock sampler did not start")
+                time.sleep(0.005)
+        except Exception as e:
+            self.error = str(e)
+            self.proc = None
 
     def mark_start(self):
-        self.t_start = time.perf_counter()
-
-    def poll_until(self, event):
-        """Samples from the calling thread until `event` (recorded after the
-        timed launches) completes: the launches are all queued, so this reads
-        the clocks while the GPU runs them and adds nothing to its work."""
-        if self.lib is None:
-            return
-        while not event.query():
-            self._read()
+        self.t_start = time.monotonic()
 
     def mark_end(self):
-        self.t_end = time.perf_counter()
+        self.t_end = time.monotonic()
+
+    def poll_until(self, event):
+        """Kept for the launch loops' call: the sampling process samples on
+        its own, so this only waits for the timed launches to finish."""
+        event.synchronize()
 
     def stop(self):
-        if self.lib is None:
+        if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "source": "NVML unavailable: %s" % self.error}
-        self._stop.set()
-        self._thread.join(timeout=5)
-        sys.setswitchinterval(self._switch)
-        self._read()
+                    "source": "NVML sampler unavailable: %s" % self.error}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=10)
+        except Exception:
+            self.proc.kill()
+        samples, sm_max = [], None
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = line.split()
+                    if parts and parts[0] == "max":
+                        sm_max = float(parts[1]) or None
+                    elif len(parts) == 4:
+                        samples.append((float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3])))
+        except OSError as e:
+            self.error = str(e)
+        for path in (self.path, self.path + ".ready"):
+            if os.path.exists(path):
+                os.unlink(path)
         lo = self.t_start if self.t_start is not None else -1e30
         hi = self.t_end if self.t_end is not None else 1e30
-        inside = [x for x in self.samples if lo <= x[0] <= hi]
-        reasons = sorted({n for x in inside for bit, n in self.REASONS if x[3] & bit})
-        out = {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
-               "sm_max_mhz": self.sm_max, "reasons": reasons, "samples": len(inside),
-               "power_w_max": max((x[2] for x in inside), default=None),
-               "samples_whole_run": len(self.samples),
-               "sm_mhz_median_whole_run": statistics.median([x[1] for x in self.samples])
-               if self.samples else None,
-               "source": "in-process NVML reads every %.1f ms across warm-up and timed loop; "
-                         "summary over the timed region" % (self.period * 1e3)}
-        return out
+        inside = [x for x in samples if lo <= x[0] <= hi]
+        reasons = sorted({n for x in inside for bit, n in CLOCK_REASONS if x[3] & bit})
+        return {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
+                "sm_max_mhz": sm_max, "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((x[2] for x in inside), default=None),
+                "samples_whole_run": len(samples),
+                "sm_mhz_median_whole_run": statistics.median([x[1] for x in samples]) if samples else None,
+                "source": "NVML read-only queries back to back (period %.1f ms or less) by a sampling "
+                          "process, from before the warm-up to after the timed loop; summary over the "
+                          "timed region" % (self.period * 1e3)}
 
 
 # ----------------------------------------------------------- device setup
@@ -1032,6 +1052,9 @@ def config_block(name, B, kv_bytes, partition_size, split_desc):
 
 def main():
     args = parse_args()
+    if args.clock_worker is not None:
+        clock_worker(args.clock_worker[0], float(args.clock_worker[1]), args.clock_worker[2])
+        return
     if args.cpu_worker is not None:
         cpu_worker(args.workload, args.cpu_worker, CPU_SAMPLE_SEQS[args.workload])
         return
