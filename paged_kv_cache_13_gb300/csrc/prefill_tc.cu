@@ -81,6 +81,8 @@ constexpr int kSmemBytes = kOffXch + 2 * 128 * 4 + 1024;  // then alignment slac
 
 struct TcArgs {
     const void* q;
+    const void* k_pool;  // the pools (for L2 prefetches; the tiles come by TMA)
+    const void* v_pool;
     const int32_t* q_start;
     const int32_t* tables;
     const int32_t* ctx_lens;
@@ -137,6 +139,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Bring `bytes` at p into L2 ahead of their copies (no data returned).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // UMMA shared-memory descriptor: start, leading and stride byte offsets (16-
@@ -243,9 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // bars: 0-1 K full, 2-3 V full, 4-5 S ready (per S buffer), 6 O ready
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
     int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 68);
-    // set by warp 1 when it skipped its copies of an iteration (its wait for
-    // the previous O += P V ran out): the drain then expects one copy fewer
-    int* copies_skipped = reinterpret_cast<int*>(sm + kOffBar + 72);
     float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2][128]: per-half row values
     // tab[t % 4][jj]: TMA row of block jj of key tile t (past the map's end:
     // zeros), read from the table two tiles ahead of its copies
@@ -276,7 +280,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
-        *copies_skipped = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
@@ -315,7 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return y;
     };
-    if (tid < 24) tab[tid] = block_row(tid);  // tiles 0, 1, 2
+    if (tid < 24) {  // tiles 0, 1, 2 (tile 2's rows prefetched into L2)
+        const int y = block_row(tid);
+        tab[tid] = y;
+        if (tid >= 16 && y < a.total_rows) {
+            prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
+            prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
+        }
+    }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the MMA
     fence_before_sync();
     __syncthreads();
@@ -383,8 +393,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // the table entries of tile j + 3 (stored before the barrier below;
         // tile j - 1's slot was last read two iterations ago)
+        // and their K and V rows (16 x 256 contiguous bytes per block) are
+        // prefetched into L2 now, three tiles before their copies: the row
+        // tiles of one (sequence, KV head) run together and would otherwise
+        // all wait on the same DRAM fetch
         int ahead = 0;
-        if (warp == 1 && (tid & 31) < 8) ahead = block_row((j + 3) * 8 + (tid & 31));
+        if (warp == 1 && (tid & 31) < 8) {
+            ahead = block_row((j + 3) * 8 + (tid & 31));
+            if (ahead < a.total_rows) {
+                prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(ahead) * kDim, kBS * kDim * 2);
+                prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(ahead) * kDim, kBS * kDim * 2);
+            }
+        }
         // ---- this thread's half row of S(j), masked and scaled (base 2)
         if (!wait_bar(bar(4 + s), (j >> 1) & 1)) {
             atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
@@ -447,24 +467,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             o_done = false;
         }
         fence_after_sync();
-        if (warp == 1) {
+        {
             // stages freed: V of tile j - 1 (its O += P V is done), K of tile
-            // j (its S was read above).  One copy per lane: lanes 0-15 the 16
-            // of K tile j + 2, lanes 16-31 the 16 of V tile j + 1.  If any
-            // lane's wait ran out, the V stage may still be read by that MMA:
-            // the warp issues nothing this iteration (the CTA stops below).
+            // j (its S was read above).  32 copies, four per warp (lanes 0-3):
+            // copy c = 4 warp + lane, c < 16 the K boxes of tile j + 2, the
+            // rest the V boxes of tile j + 1 (spread so no warp reaches the
+            // barrier late behind a queue of copy issues).  A warp in which a
+            // wait ran out issues nothing (the CTA stops at the barrier; the
+            // drain's bounded waits outlast whatever was issued).
             const int ln = tid & 31;
-            const bool is_v = ln >= 16;
-            const int jt = is_v ? j + 1 : j + 2;
             const bool all_done = __all_sync(0xffffffffu, o_done);
-            if (!all_done && ln == 0) *copies_skipped = 1;
-            if (all_done && jt < ntiles) {
-                const int st = jt & 1;
-                const uint32_t fb = bar((is_v ? 2 : 0) + st);
-                if ((ln & 15) == 0) mbar_arrive_expect_tx(fb, kTile);
-                const int jj = (ln & 15) >> 1, h = ln & 1;
-                tma_load_2d(sbase + (is_v ? kOffV : kOffK) + st * kTile + h * 16384 + jj * 2048, is_v ? &vmap : &kmap,
-                            h * 64, tab[(jt & 3) * 8 + jj], fb);
+            if (ln < 4) {
+                const int c = warp * 4 + ln;
+                const bool is_v = c >= 16;
+                const int jt = is_v ? j + 1 : j + 2;
+                if (all_done && jt < ntiles) {
+                    const int st = jt & 1;
+                    const uint32_t fb = bar((is_v ? 2 : 0) + st);
+                    if ((c & 15) == 0) mbar_arrive_expect_tx(fb, kTile);
+                    const int jj = (c & 15) >> 1, h = c & 1;
+                    tma_load_2d(sbase + (is_v ? kOffV : kOffK) + st * kTile + h * 16384 + jj * 2048,
+                                is_v ? &vmap : &kmap, h * 64, tab[(jt & 3) * 8 + jj], fb);
+                }
             }
         }
         if (j > 0 && __any_sync(0xffffffffu, raise)) {
@@ -529,11 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the flag just after the barrier
         if (__syncthreads_or(*reinterpret_cast<volatile int*>(abort_flag))) {
             aborted = true;
-            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1,
-            // or one fewer of each when warp 1 skipped this iteration's
-            const int skipped = *reinterpret_cast<volatile int*>(copies_skipped);
-            issued_k = min(ntiles, j + (skipped ? 2 : 3));
-            issued_v = min(ntiles, j + (skipped ? 1 : 2));
+            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1
+            // (some of this iteration's may have been skipped: their phases
+            // then never complete and the drain's waits run out, bounded)
+            issued_k = min(ntiles, j + 3);
+            issued_v = min(ntiles, j + 2);
             break;
         }
         // ---- O += P V (thread 0 issues)
@@ -675,6 +699,8 @@ int launch_prefill_tc(const void* q, const int32_t* q_start, const void* k_pool,
     if (!pool_map(&km, k_pool, rows, bf16) || !pool_map(&vm, v_pool, rows, bf16)) return PKV_ERR_CUDA;
     TcArgs a;
     a.q = q;
+    a.k_pool = k_pool;
+    a.v_pool = v_pool;
     a.q_start = q_start;
     a.tables = tables;
     a.ctx_lens = ctx_lens;
