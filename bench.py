@@ -539,6 +539,21 @@ class Cache:
         return (2 if self.split else 1) + (1 if self.qmode else 0)
 
 
+def per_call_ms(torch, step, stream, steps):
+    """Mean device time of one call, each bracketed by its own CUDA events on
+    the launching stream.  A separate pass after the timed loop, which has
+    nothing on the stream between consecutive steps (the event pairs add
+    about 2 us per step on the 64-sequence layer)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
 def run_device(args, rank, world, dist):
     import torch
     import paged_kv_cache_13_gb300 as pkv
@@ -558,18 +573,16 @@ def run_device(args, rank, world, dist):
     for _ in range(args.warmup):
         cache.step()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.mark_start()
+    # the steps back to back, as a serving loop issues them (nothing between
+    # consecutive steps on the stream)
     t0.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         cache.step()
-        ev[i][1].record(stream)
     t1.record(stream)
     clocks.poll_until(t1)
     torch.cuda.synchronize()
@@ -578,7 +591,7 @@ def run_device(args, rank, world, dist):
     if dist is not None:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    call_ms = per_call_ms(torch, cache.step, stream, args.steps)
     assert pkv.pkv_device_status() == 0
     elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
     ms_per_step = elapsed_ms / args.steps
@@ -702,7 +715,6 @@ def run_mq(args, rank, world, dist):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
@@ -710,18 +722,16 @@ def run_mq(args, rank, world, dist):
     clocks.mark_start()
     t0.record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         step()
-        ev[i][1].record(stream)
     t1.record(stream)
     clocks.poll_until(t1)
     torch.cuda.synchronize()
     clocks.mark_end()
     clk = clocks.stop()
-    assert pkv.pkv_device_status() == 0
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dist, device)
     ms = elapsed_ms / args.steps
-    call_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    call_ms = per_call_ms(torch, step, stream, args.steps)
+    assert pkv.pkv_device_status() == 0
 
     # end to end: q from pinned host memory, out back to pinned host memory
     e2e_steps = max(E2E_MIN_STEPS, args.steps)

@@ -218,3 +218,106 @@ def test_quant_window_many_short_sequences(pkv, cuda_dev, qmode):
     got = _decode_quant(pkv, c)
     assert pkv.pkv_device_status() == 0
     assert_close(got, expected(c), what="%s window, 640 short sequences" % qmode)
+
+
+def _runs_pieces(lens, hkv, max_blocks, sms):
+    """How many warp ranges meet each non-empty (sequence, KV head) run of
+    a balanced call: the split restated on the host (items of the call cut
+    into nwt equal contiguous shares, 16 warps per SM at most)."""
+    units = [-(-int(L) // 16) for L in lens]
+    W = hkv * sum(units)
+    nwt_launch = max(1, min(len(lens) * hkv * -(-max_blocks * 16 // 16) // 2, sms * 16))
+    nwt = max(min(W // 2, nwt_launch), 1)
+    out, cs = [], 0
+    for nb in units:
+        for k in range(hkv):
+            if nb:
+                S = cs + k * nb
+                out.append(((S + nb) * nwt - 1) // W - ((S + 1) * nwt - 1) // W + 1)
+        cs += nb * hkv
+    return np.array(out)
+
+
+def _mixed_workload():
+    """400 short sequences and two long ones: runs met by one warp, by a
+    few, and by dozens (merged with 4 partial groups per CTA)."""
+    rng = np.random.default_rng(5)
+    lens = [int(x) for x in rng.integers(1, 321, size=400)] + [65536, 40000]
+    return syn.workload("llama3_8b_b64", lens=lens,
+                        num_blocks=sum(-(-L // 16) for L in lens) + len(lens) + 64)
+
+
+def test_runs_of_one_few_and_many_pieces_in_one_call(pkv, cuda_dev):
+    """One call whose runs are met by one warp range, by a few, and by more
+    than 32 (the merge folds each from its consecutive partial slots)."""
+    c = build(pkv, _mixed_workload(), cuda_dev)
+    assert _is_balanced(c)
+    pieces = _runs_pieces(c.lens_host, c.w["hkv"], c.max_blocks, _sms())
+    assert (pieces == 1).any() and ((pieces > 1) & (pieces <= 32)).any() and (pieces > 32).any()
+    out = _decode(pkv, c)
+    assert pkv.pkv_device_status() == 0
+    assert_close(out.float().cpu().numpy(), expected(c), what="mixed runs")
+
+
+def test_back_to_back_calls_share_the_workspace(pkv, cuda_dev):
+    """Calls of two shapes alternate on one stream and one workspace (first
+    filled with 0xFF bytes) with no synchronisation between them: each call
+    finds the other shape's partials in its slots, and gives the same bits
+    every time."""
+    c = build(pkv, _mixed_workload(), cuda_dev)
+    w = c.w
+    B, sub = len(c.decoded), 300
+    n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, 0)
+    ws = torch.empty(n, dtype=torch.uint8, device=cuda_dev)
+    ws.fill_(0xFF)
+    full, part = [], []
+    for _ in range(3):
+        o = torch.full((B, w["hq"], w["d"]), float("nan"), dtype=w["torch_dtype"], device=cuda_dev)
+        pkv.pkv_paged_attention_decode(c.q, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"], o, ws, 0)
+        full.append(o)
+        p = torch.full((sub, w["hq"], w["d"]), float("nan"), dtype=w["torch_dtype"], device=cuda_dev)
+        pkv.pkv_paged_attention_decode(c.q[:sub].contiguous(), c.k_pool, c.v_pool, c.tables[:sub].contiguous(),
+                                       c.lens[:sub].contiguous(), w["scale"], p, ws, 0)
+        part.append(p)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    want = expected(c)
+    for o in full:
+        assert torch.equal(o, full[0])  # the same bits every call
+    for p in part:
+        assert torch.equal(p, part[0])
+    assert_close(full[0].float().cpu().numpy(), want, what="full shape")
+    assert_close(part[0].float().cpu().numpy(), want[:sub], what="first 300 sequences")
+
+
+def test_graph_replay_of_the_balanced_call(pkv, cuda_dev):
+    """The balanced call (split kernel and its merge, launched with
+    programmatic dependent launch) captured in a CUDA graph: every replay
+    gives the same bits, within the bound of the oracle."""
+    c = build(pkv, syn.workload("llama3_8b_b64"), cuda_dev)
+    assert _is_balanced(c)
+    w = c.w
+    B = len(c.decoded)
+    out = torch.empty((B, w["hq"], w["d"]), dtype=w["torch_dtype"], device=cuda_dev)
+    n = pkv.pkv_decode_workspace_bytes(B, w["hq"], w["d"], c.max_blocks, 16, 0)
+    ws = torch.zeros(n, dtype=torch.uint8, device=cuda_dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        pkv.pkv_paged_attention_decode(c.q, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"], out, ws, 0)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkv.pkv_paged_attention_decode(c.q, c.k_pool, c.v_pool, c.tables, c.lens, w["scale"], out, ws, 0)
+    want = expected(c)
+    first = None
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_status() == 0
+        got = out.clone()
+        first = got if first is None else first
+        assert torch.equal(got, first)
+    assert_close(first.float().cpu().numpy(), want, what="graph replays")
