@@ -276,8 +276,12 @@ class ClockSampler:
     ``period_s`` from before the warm-up until ``stop``; ``mark_start`` /
     ``mark_end`` bracket the timed region (CLOCK_MONOTONIC, shared by both
     processes) and the summary is taken over the samples inside it.  A
-    20-step region lasts about 2 ms, hence the sub-millisecond period.  Without
-    NVML the summary says so and holds no samples."""
+    20-step region lasts about 2 ms and NVML answers every few ms on some
+    hosts: with fewer than MIN_SAMPLES inside, the summary takes the
+    MIN_SAMPLES samples nearest to the region and says so (``basis``).
+    Without NVML the summary says so and holds no samples."""
+
+    MIN_SAMPLES = 5
 
     def __init__(self, device_index, period_s=0.0002):
         self.period = period_s
@@ -342,15 +346,27 @@ class ClockSampler:
         lo = self.t_start if self.t_start is not None else -1e30
         hi = self.t_end if self.t_end is not None else 1e30
         inside = [x for x in samples if lo <= x[0] <= hi]
-        reasons = sorted({n for x in inside for bit, n in CLOCK_REASONS if x[3] & bit})
-        return {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
+        basis = "the samples inside the timed region"
+        used = inside
+        if len(inside) < self.MIN_SAMPLES and samples:
+            # a short timed region (20 steps last about 2 ms) may fall between
+            # NVML reads: take the samples nearest to it, the warm-up steps
+            # running before it and the per-call pass of the same steps after
+            near = sorted(samples, key=lambda x: max(lo - x[0], x[0] - hi, 0.0))[:self.MIN_SAMPLES]
+            gap = max(max(lo - x[0], x[0] - hi, 0.0) for x in near)
+            used = near
+            basis = ("%d samples inside the timed region; the %d nearest to it (within %.1f ms; the "
+                     "same steps ran before and after it)" % (len(inside), len(near), gap * 1e3))
+        reasons = sorted({n for x in used for bit, n in CLOCK_REASONS if x[3] & bit})
+        return {"sm_mhz": statistics.median([x[1] for x in used]) if used else None,
                 "sm_max_mhz": sm_max, "reasons": reasons, "samples": len(inside),
-                "power_w_max": max((x[2] for x in inside), default=None),
+                "power_w_max": max((x[2] for x in used), default=None),
+                "basis": basis,
                 "samples_whole_run": len(samples),
                 "sm_mhz_median_whole_run": statistics.median([x[1] for x in samples]) if samples else None,
                 "source": "NVML read-only queries back to back (period %.1f ms or less) by a sampling "
-                          "process, from before the warm-up to after the timed loop; summary over the "
-                          "timed region" % (self.period * 1e3)}
+                          "process, from before the warm-up until after the per-call pass that follows "
+                          "the timed loop" % (self.period * 1e3)}
 
 
 # ----------------------------------------------------------- device setup
@@ -587,11 +603,12 @@ def run_device(args, rank, world, dist):
     clocks.poll_until(t1)
     torch.cuda.synchronize()
     clocks.mark_end()
+    # the same steps again, each timed alone, while the sampler still runs
+    call_ms = per_call_ms(torch, cache.step, stream, args.steps)
     clk = clocks.stop()
     if dist is not None:
         dist.barrier()
     elapsed_ms = t0.elapsed_time(t1)
-    call_ms = per_call_ms(torch, cache.step, stream, args.steps)
     assert pkv.pkv_device_status() == 0
     elapsed_ms = max_over_ranks(elapsed_ms, dist, device)
     ms_per_step = elapsed_ms / args.steps
@@ -727,10 +744,10 @@ def run_mq(args, rank, world, dist):
     clocks.poll_until(t1)
     torch.cuda.synchronize()
     clocks.mark_end()
+    call_ms = per_call_ms(torch, step, stream, args.steps)
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), dist, device)
     ms = elapsed_ms / args.steps
-    call_ms = per_call_ms(torch, step, stream, args.steps)
     assert pkv.pkv_device_status() == 0
 
     # end to end: q from pinned host memory, out back to pinned host memory
