@@ -32,13 +32,15 @@
 //   rescale of O (when a row's reference max moves) is a TMEM load / store
 //   of that half row.  O / l goes out at the end.
 // * Every operand tile is a grid of 8-row x 128-byte swizzle atoms (128-byte
-//   swizzle), atom (g, h) -- rows 8g .. 8g+7, columns 64h .. 64h+63 -- at
-//   byte h * 16 KiB + g * 1 KiB of its tile.  K-major operands (Q, K, P)
-//   step 32 bytes per K-16 slice inside an atom row (and 16 KiB to the
-//   second column half); V is the MN-major B operand of O += P V (its 8-key
-//   atom groups 1 KiB apart, its two 64-dim halves 16 KiB apart).
-// * One thread of warp 4 issues the S MMAs, thread 0 the O MMAs, the lanes
-//   of warp 1 the TMA copies of a tile (one copy each); completion is
+//   swizzle).  In Q and P atom (g, h) -- rows 8g .. 8g+7, columns 64h ..
+//   64h+63 -- sits at byte h * 16 KiB + g * 1 KiB of the tile; in K and V
+//   (one TMA box per 16-row block, so its two row groups and two column
+//   halves land together) at g * 2 KiB + h * 1 KiB.  K-major operands (Q,
+//   K, P) step 32 bytes per K-16 slice inside an atom row; V is the MN-major
+//   B operand of O += P V (its 8-key groups 2 KiB apart, its two 64-dim
+//   halves 1 KiB apart).
+// * One thread of warp 4 issues the S MMAs, thread 0 the O MMAs, lanes 0-1
+//   of every warp the TMA copies of a tile (one block each); completion is
 //   tracked by mbarriers (tcgen05.commit arrives on them).  Every wait
 //   suspends in hardware (try_wait) and is bounded in time: one that runs
 //   out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together (the
@@ -133,11 +135,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// One 16-row block of the pool (4 KiB) as a 4-D box: coordinates (0, 0, 0,
+// w), w the block's first 8-row group (see pool_map).
+__device__ __forceinline__ void tma_load_block(uint32_t dst, const CUtensorMap* map, int w, uint32_t bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, "
+        "%3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
         : "memory");
 }
 
@@ -334,9 +338,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + kKeys;  // S buffers at columns 0 and 256, O at 128
     auto tS = [&](int s) { return tmem + (s ? 2 * kKeys : 0); };
 
-    // TMA of key tile j's K (or V) into stage j % 2 (thread 0): 8 blocks x 2
-    // column halves of 16 rows; blocks past the context or with a bad id read
-    // rows past the map's end (zeros)
+    // TMA of key tile j's K (or V) into stage j % 2 (thread 0): one box per
+    // block (its 8-row groups g and column halves h land at 4096 jj + 2048 g
+    // + 1024 h); blocks past the context or with a bad id read rows past the
+    // map's end (zeros)
     int issued_k = 0, issued_v = 0, s_commits[2] = {0, 0}, o_commits = 0;  // for the drain (thread 0)
     auto issue = [&](int j, bool is_v) {
         const int s = j & 1;
@@ -344,12 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(fb, kTile);
         const uint32_t dst0 = sbase + (is_v ? kOffV : kOffK) + s * kTile;
 #pragma unroll
-        for (int jj = 0; jj < kKeys / kBS; ++jj) {
-            const int y = tab[(j & 3) * 8 + jj];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                tma_load_2d(dst0 + h * 16384 + jj * 2048, is_v ? &vmap : &kmap, h * 64, y, fb);
-        }
+        for (int jj = 0; jj < kKeys / kBS; ++jj)
+            tma_load_block(dst0 + jj * 4096, is_v ? &vmap : &kmap, tab[(j & 3) * 8 + jj] >> 3, fb);
         if (is_v) ++issued_v;
         else ++issued_k;
     };
@@ -366,8 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < kDim / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_f16(tS(s), smem_desc(qa + off, 16384, 1024), smem_desc(kb + off, 16384, 1024), idesc_s, kk > 0);
+            // Q: halves at 16 KiB, 8-row groups at 1 KiB; K: halves at 1 KiB,
+            // 8-key groups at 2 KiB
+            const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 1024 + (kk & 3) * 32;
+            mma_f16(tS(s), smem_desc(qa + qoff, 16384, 1024), smem_desc(kb + koff, 1024, 2048), idesc_s, kk > 0);
         }
         mma_commit(bar(4 + s));
         ++s_commits[s];
@@ -469,25 +472,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_after_sync();
         {
             // stages freed: V of tile j - 1 (its O += P V is done), K of tile
-            // j (its S was read above).  32 copies, four per warp (lanes 0-3):
-            // copy c = 4 warp + lane, c < 16 the K boxes of tile j + 2, the
-            // rest the V boxes of tile j + 1 (spread so no warp reaches the
-            // barrier late behind a queue of copy issues).  A warp in which a
-            // wait ran out issues nothing (the CTA stops at the barrier; the
-            // drain's bounded waits outlast whatever was issued).
+            // j (its S was read above).  16 copies, one block each, two per
+            // warp (lanes 0-1): copy c = 2 warp + lane, c < 8 the K blocks of
+            // tile j + 2, the rest the V blocks of tile j + 1 (spread so no
+            // warp reaches the barrier late behind a queue of copy issues).
+            // A warp in which a wait ran out issues nothing (the CTA stops at
+            // the barrier; the drain's bounded waits outlast whatever was
+            // issued).
             const int ln = tid & 31;
             const bool all_done = __all_sync(0xffffffffu, o_done);
-            if (ln < 4) {
-                const int c = warp * 4 + ln;
-                const bool is_v = c >= 16;
+            if (ln < 2) {
+                const int c = warp * 2 + ln;
+                const bool is_v = c >= 8;
                 const int jt = is_v ? j + 1 : j + 2;
                 if (all_done && jt < ntiles) {
                     const int st = jt & 1;
                     const uint32_t fb = bar((is_v ? 2 : 0) + st);
-                    if ((c & 15) == 0) mbar_arrive_expect_tx(fb, kTile);
-                    const int jj = (c & 15) >> 1, h = c & 1;
-                    tma_load_2d(sbase + (is_v ? kOffV : kOffK) + st * kTile + h * 16384 + jj * 2048,
-                                is_v ? &vmap : &kmap, h * 64, tab[(jt & 3) * 8 + jj], fb);
+                    if ((c & 7) == 0) mbar_arrive_expect_tx(fb, kTile);
+                    const int jj = c & 7;
+                    tma_load_block(sbase + (is_v ? kOffV : kOffK) + st * kTile + jj * 4096, is_v ? &vmap : &kmap,
+                                   tab[(jt & 3) * 8 + jj] >> 3, fb);
                 }
             }
         }
@@ -540,8 +544,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
                 *abort_flag = 1;
             } else if (j * kKeys + r >= ctx) {
-                uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + hc * 16384 + (r >> 3) * 1024 +
-                                                      (r & 7) * 128);
+                uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + (r >> 4) * 4096 +
+                                                      ((r >> 3) & 1) * 2048 + hc * 1024 + (r & 7) * 128);
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
             }
@@ -571,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    const uint64_t bd = smem_desc(vb + kk * 2048, 16384, 1024);
+                    // V of block kk: halves (N) at 1 KiB, 8-key groups (K) at 2 KiB
+                    const uint64_t bd = smem_desc(vb + kk * 4096, 1024, 2048);
                     mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc_o, j > 0 || kk > 0);
                     if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc_o, true);
                 }
@@ -656,16 +661,21 @@ EncodeTiled encode_fn() {
     return fn;
 }
 
-// The pool [num_blocks * Hkv * 16 rows, 128 dims] as a 2-D tensor; boxes of
-// 16 rows x 64 dims (128 bytes: one swizzle span), 128-byte swizzle.
+// The pool [num_blocks * Hkv * 16 rows, 128 dims] as a 4-D tensor: (64
+// dims; 8 rows at 256 bytes; 2 column halves at 128 bytes; 8-row groups at
+// 2 KiB).  A box (64, 8, 2, 2) is one 16-row block, 4 KiB, landing as
+// [group][half][row][64 dims] with 128-byte swizzle: one copy per block
+// where a 2-D map takes two (one per 128-byte column half), and the copy
+// engine's cost is mostly per copy (measured on GB300: a 32 KiB tile of 8
+// blocks takes ~1,450 cycles as 8 such boxes, ~1,790 as 16 2-D boxes).
 bool pool_map(CUtensorMap* map, const void* pool, int64_t rows, bool bf16) {
     EncodeTiled enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDim) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBS)};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    const cuuint64_t dims[4] = {64, 8, 2, static_cast<cuuint64_t>(rows / 8)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kDim) * 2, 128, static_cast<cuuint64_t>(kDim) * 2 * 8};
+    const cuuint32_t box[4] = {64, 8, 2, 2};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
