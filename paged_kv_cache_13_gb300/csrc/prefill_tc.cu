@@ -9,17 +9,22 @@
 // 512-token slice of a prompt attends to the cache before it and causally
 // to itself).
 //
-// Design (one CTA of 8 warps per 128 query rows of one (sequence, KV head);
+// Design (one CTA of 12 warps per 128 query rows of one (sequence, KV head);
 // a row is a (query token, query head) pair, 128 / G tokens per tile):
 // * Q tile [128 rows x 128 dims] bf16/fp16 in shared memory; K and V tiles
-//   of 128 keys (8 pool blocks) in a 2-stage ring, each block's 16 rows
-//   fetched by TMA straight from its physical block.  The table entries of
-//   a tile are read into shared memory three tiles ahead (unused or bad
-//   blocks become rows past the map's end, which TMA fills with zeros), so
-//   the issuing lanes never wait on a table load.
+//   of 128 keys (8 pool blocks) in 2-stage rings, each block's 16 rows
+//   fetched by one TMA box straight from its physical block (unused or bad
+//   blocks become rows past the map's end, which TMA fills with zeros).
+// * Warps 0-7 (two warpgroups, 232 registers each after setmaxnreg) do the
+//   softmax; warps 8-11 (one warpgroup, 40 registers) issue: lane 0 of warp
+//   8 the S MMAs, lane 0 of warp 9 the O MMAs, warps 10 and 11 the K and V
+//   copies (a lane per block, the table entries loaded by the same lanes,
+//   the K warp also prefetching the rows two tiles ahead into L2).  An MMA
+//   issue blocks while the tensor pipe drains (16 MMAs of a tile take ~1,200
+//   cycles to issue), so no softmax warp issues any.
 // * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into one of two
-//   TMEM S buffers (columns [0, 128) and [256, 384)): the next tile's S is
-//   computed while this tile's softmax runs.  Warps w and w + 4 share the
+//   TMEM S buffers (columns [0, 128) and [256, 384)): S(j + 1) is computed
+//   while the softmax of tile j runs.  Softmax warps w and w + 4 share the
 //   TMEM lanes (rows) 32 (w % 4) .. +31, each taking 64 of the 128 columns:
 //   the thread of row r loads its half row of S, applies the causal mask
 //   (only on tiles that reach past the CTA's first query position), and the
@@ -31,6 +36,11 @@
 // * O += P V (M 128, N 128, K 128 keys) into TMEM columns [128, 256); a
 //   rescale of O (when a row's reference max moves) is a TMEM load / store
 //   of that half row.  O / l goes out at the end.
+// * Hand-offs are mbarriers: K / V landed (TMA), S done and O done
+//   (tcgen05.commit), S read and P written (one arrival per softmax warp),
+//   the V stage read (a second commit).  Each waiter is at most one phase
+//   behind its barrier by construction (a barrier's next phase needs the
+//   waiter's own later arrival).
 // * Every operand tile is a grid of 8-row x 128-byte swizzle atoms (128-byte
 //   swizzle).  In Q and P atom (g, h) -- rows 8g .. 8g+7, columns 64h ..
 //   64h+63 -- sits at byte h * 16 KiB + g * 1 KiB of the tile; in K and V
@@ -39,12 +49,11 @@
 //   K, P) step 32 bytes per K-16 slice inside an atom row; V is the MN-major
 //   B operand of O += P V (its 8-key groups 2 KiB apart, its two 64-dim
 //   halves 1 KiB apart).
-// * One thread of warp 4 issues the S MMAs, thread 0 the O MMAs, lanes 0-1
-//   of every warp the TMA copies of a tile (one block each); completion is
-//   tracked by mbarriers (tcgen05.commit arrives on them).  Every wait
-//   suspends in hardware (try_wait) and is bounded in time: one that runs
-//   out sets PKV_STATUS_COPY_TIMEOUT, and the CTA stops together (the
-//   decision is the OR the CTA barrier returns), still freeing its TMEM.
+// * Every wait suspends in hardware (try_wait) and is bounded in time: one
+//   that runs out sets PKV_STATUS_COPY_TIMEOUT and the stop flag; softmax
+//   warp pairs stop together (the OR their barrier returns), the issuers
+//   let their MMAs and copies in flight finish (bounded), and the CTA still
+//   frees its TMEM.
 
 #include <cuda.h>
 
@@ -62,8 +71,18 @@ constexpr int kKeys = 128;   // keys per tile (MMA N of S, K of O)
 constexpr int kDim = 128;    // head dim
 constexpr int kBS = 16;      // tokens per pool block
 constexpr int kTile = kRows * kDim * 2;  // bytes of one 128 x 128 16-bit tile
-constexpr int kThreads = 256;  // 8 warps: two per 32-row TMEM lane quarter
-constexpr int kSIssuer = 128;  // thread issuing S = Q K^T (warp 4); thread 0 issues O += P V
+// warps 0-7: softmax, two per 32-row TMEM lane quarter; warps 8-11: producers
+constexpr int kSoftmaxWarps = 8;
+constexpr int kWarpS = 8;   // lane 0 issues S = Q K^T
+constexpr int kWarpO = 9;   // lane 0 issues O += P V
+constexpr int kWarpK = 10;  // K copies (and L2 prefetches)
+constexpr int kWarpV = 11;  // V copies
+constexpr int kThreads = 384;
+// Registers: launched at 168 a thread (384 threads, one CTA per SM), the
+// softmax warpgroups raise theirs to 232 and the producer warpgroup lowers
+// its own to 40 (setmaxnreg): 2 x 128 x 232 + 128 x 40 = 384 x 168.
+constexpr int kLaunchRegs = 168;
+static_assert(2 * 128 * 232 + 128 * 40 <= kThreads * kLaunchRegs, "register split exceeds the launch's registers");
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.f;
@@ -76,9 +95,17 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
 constexpr int kOffP = kOffV + 2 * kTile;  // P, then its residual (bf16)
-constexpr int kOffBar = kOffP + 2 * kTile;
-constexpr int kOffTab = kOffBar + 128;                // [4][8] TMA rows of the next tiles' blocks
+constexpr int kOffBar = kOffP + 2 * kTile;           // mbarriers, then the TMEM address and stop flag
 constexpr int kOffXch = kOffBar + 256;                // [2][128] floats: row values of the two halves
+// mbarriers (index: count)
+constexpr int kBarKFull = 0;   // 2 (per stage): the K tile has landed (TMA)
+constexpr int kBarVFull = 2;   // 2: the V tile has landed
+constexpr int kBarSFull = 4;   // 2 (per S buffer): S = Q K^T done
+constexpr int kBarO = 6;       // O += P V done: P, O and the V stage may be touched
+constexpr int kBarP = 7;       // 8 (softmax warps): P written, O rescaled
+constexpr int kBarSFree = 8;   // 2 x 8: the softmax has read S out of the buffer
+constexpr int kBarVFree = 10;  // 2: O += P V done reading the V stage
+constexpr int kNumBars = 12;
 constexpr int kSmemBytes = kOffXch + 2 * 128 * 4 + 1024;  // then alignment slack
 
 struct TcArgs {
@@ -101,6 +128,11 @@ __device__ __forceinline__ uint32_t sh_addr(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// one plain arrival
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // one arrival that also expects `bytes` of copies to complete on the barrier
@@ -223,9 +255,23 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-// named barrier of the 64 threads of warps w and w + 4 (id 1 .. 4)
+// named barrier of the 64 threads of softmax warps w and w + 4 (id 1 .. 4)
 __device__ __forceinline__ void pair_sync(int id) {
     asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+
+// the same barrier, returning whether any of the 64 threads passed true
+__device__ __forceinline__ bool pair_sync_or(int id, bool pred) {
+    uint32_t any;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %2, 0;\n\t"
+        "bar.red.or.pred q, %1, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(any)
+        : "r"(id), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return any != 0;
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -246,24 +292,21 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, TcArgs a) {
     constexpr bool kSplit = std::is_same<T, __nv_bfloat16>::value;
-    constexpr int kHalf = kKeys / 2;  // columns of S (and O) per thread
+    constexpr int kHalf = kKeys / 2;  // columns of S (and O) per softmax thread
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = sh_addr(sm);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-    // bars: 0-1 K full, 2-3 V full, 4-5 S ready (per S buffer), 6 O ready
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 64);
-    int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 68);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + 112);
+    int* abort_flag = reinterpret_cast<int*>(sm + kOffBar + 116);
     float* xch = reinterpret_cast<float*>(sm + kOffXch);  // [2][128]: per-half row values
-    // tab[t % 4][jj]: TMA row of block jj of key tile t (past the map's end:
-    // zeros), read from the table two tiles ahead of its copies
-    int* tab = reinterpret_cast<int*>(sm + kOffTab);
     const uint32_t bar0 = sh_addr(bars);
     auto bar = [&](int i) { return bar0 + 8 * i; };
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    // warp w: TMEM lanes (rows) 32 (w % 4) .. +31, columns 64 (w / 4) .. +63
-    const int r = 32 * (warp & 3) + (tid & 31), hc = warp >> 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool softmax = warp < kSoftmaxWarps;
+    // softmax warp w: TMEM lanes (rows) 32 (w % 4) .. +31, columns 64 (w / 4) .. +63
+    const int r = 32 * (warp & 3) + lane, hc = (warp >> 2) & 1;
     const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int q0 = a.q_start[b], L = a.q_start[b + 1] - q0;
     const int tpt = kRows / a.G;  // query tokens per tile
@@ -282,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nblk = (ctx + kBS - 1) / kBS;  // blocks holding context tokens
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(bar(i), (i == kBarP || i == kBarSFree || i == kBarSFree + 1) ? kSoftmaxWarps : 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -294,9 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    // ---- Q tile: thread (r, hc) writes columns 64 hc .. +63 of row r
+    // ---- Q tile: softmax thread (r, hc) writes columns 64 hc .. +63 of row r
     const int my_tok = tok0 + r / a.G, my_h = r - (r / a.G) * a.G;
-    {
+    if (softmax) {
         const bool valid = my_tok < L;
         const uint4* src = valid ? reinterpret_cast<const uint4*>(
                                        static_cast<const T*>(a.q) +
@@ -308,9 +352,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint4 v = valid ? src[ch] : make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(sm + kOffQ + tile_off(r, hc * 64 + ch * 8)) = v;
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the MMA
     }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tO = tmem + kKeys;  // S buffers at columns 0 and 256, O at 128
+    auto tS = [&](int s) { return tmem + (s ? 2 * kKeys : 0); };
     const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
-    // TMA row of logical block lb (a global load of the table)
+    // TMA row of logical block lb (a global load of the table; past the
+    // context or a bad id: the map's end, which TMA fills with zeros)
     auto block_row = [&](int lb) {
         int y = a.total_rows;
         if (lb < nblk) {
@@ -322,316 +374,287 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return y;
     };
-    if (tid < 24) {  // tiles 0, 1, 2 (tile 2's rows prefetched into L2)
-        const int y = block_row(tid);
-        tab[tid] = y;
-        if (tid >= 16 && y < a.total_rows) {
-            prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
-            prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q visible to the MMA
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + kKeys;  // S buffers at columns 0 and 256, O at 128
-    auto tS = [&](int s) { return tmem + (s ? 2 * kKeys : 0); };
-
-    // TMA of key tile j's K (or V) into stage j % 2 (thread 0): one box per
-    // block (its 8-row groups g and column halves h land at 4096 jj + 2048 g
-    // + 1024 h); blocks past the context or with a bad id read rows past the
-    // map's end (zeros)
-    int issued_k = 0, issued_v = 0, s_commits[2] = {0, 0}, o_commits = 0;  // for the drain (thread 0)
-    auto issue = [&](int j, bool is_v) {
-        const int s = j & 1;
-        const uint32_t fb = bar((is_v ? 2 : 0) + s);
-        mbar_arrive_expect_tx(fb, kTile);
-        const uint32_t dst0 = sbase + (is_v ? kOffV : kOffK) + s * kTile;
-#pragma unroll
-        for (int jj = 0; jj < kKeys / kBS; ++jj)
-            tma_load_block(dst0 + jj * 4096, is_v ? &vmap : &kmap, tab[(j & 3) * 8 + jj] >> 3, fb);
-        if (is_v) ++issued_v;
-        else ++issued_k;
-    };
-    const uint32_t idesc_s = instr_desc<T>(false), idesc_o = instr_desc<T>(true);
-    // S(j) = Q K(j)^T into S buffer j % 2 (thread 0)
-    auto mma_s = [&](int j) {
-        const int s = j & 1;
-        if (!wait_bar(bar(s), (j >> 1) & 1)) {
-            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-            *abort_flag = 1;
-            return;
-        }
-        fence_after_sync();
-        const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
-#pragma unroll
-        for (int kk = 0; kk < kDim / 16; ++kk) {
-            // Q: halves at 16 KiB, 8-row groups at 1 KiB; K: halves at 1 KiB,
-            // 8-key groups at 2 KiB
-            const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 1024 + (kk & 3) * 32;
-            mma_f16(tS(s), smem_desc(qa + qoff, 16384, 1024), smem_desc(kb + koff, 1024, 2048), idesc_s, kk > 0);
-        }
-        mma_commit(bar(4 + s));
-        ++s_commits[s];
+    auto stopped = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
+    auto give_up = [&]() {
+        atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+        *reinterpret_cast<volatile int*>(abort_flag) = 1;
     };
 
-    const int my_pos = my_tok < L ? first_pos + my_tok : -1;  // padding rows: all masked
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float m = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
-    bool aborted = false;
-    if (tid == 0 && ntiles > 0) {
-        issue(0, false);
-        issue(0, true);
-        if (ntiles > 1) issue(1, false);
-    }
-    if (tid == kSIssuer && ntiles > 0) mma_s(0);
-    __syncwarp();
-
-    for (int j = 0; j < ntiles; ++j) {
-        const int s = j & 1;
-        // ---- the next tile's S = Q K^T, overlapping this tile's softmax; its
-        // S buffer was last read by the softmax of tile j - 1
-        if (tid == kSIssuer && j + 1 < ntiles) mma_s(j + 1);
-        __syncwarp();
-        // the table entries of tile j + 3 (stored before the barrier below;
-        // tile j - 1's slot was last read two iterations ago)
-        // and their K and V rows (16 x 256 contiguous bytes per block) are
-        // prefetched into L2 now, three tiles before their copies: the row
-        // tiles of one (sequence, KV head) run together and would otherwise
-        // all wait on the same DRAM fetch
-        int ahead = 0;
-        if (warp == 1 && (tid & 31) < 8) {
-            ahead = block_row((j + 3) * 8 + (tid & 31));
-            if (ahead < a.total_rows) {
-                prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(ahead) * kDim, kBS * kDim * 2);
-                prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(ahead) * kDim, kBS * kDim * 2);
-            }
-        }
-        // ---- this thread's half row of S(j), masked and scaled (base 2)
-        if (!wait_bar(bar(4 + s), (j >> 1) & 1)) {
-            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-            *abort_flag = 1;
-        }
-        fence_after_sync();
-        float x[kHalf];
-#pragma unroll
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
-            float v[32];
-            tmem_ld32(tS(s) + lane_base + hc * kHalf + cc * 32, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
-        }
-        tmem_wait_ld();
-        // A tile wholly at or below the CTA's first query position needs no
-        // causal mask (padding rows there see zero queries: finite scores,
-        // outputs never written).  With a positive scale the max is taken
-        // over raw scores and the scale enters the exponent's FMA (mul);
-        // otherwise the scores are scaled first.
-        const int key0 = j * kKeys + hc * kHalf;
-        const bool interior = j * kKeys + kKeys - 1 <= first_pos + tok0;
-        const float mul = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
-        if (a.scale_log2 > 0.f) {
-            if (!interior) {
-#pragma unroll
-                for (int i = 0; i < kHalf; ++i)
-                    if (key0 + i > my_pos) x[i] = neg_inf();
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kHalf; ++i) x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
-        }
-        // the half row's max: three-input max, four independent chains
-        float mq[4] = {x[0], x[1], x[2], x[3]};
-#pragma unroll
-        for (int i = 4; i < kHalf; i += 8) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) mq[u] = max3f(mq[u], x[i + u], x[i + 4 + u < kHalf ? i + 4 + u : i + u]);
-        }
-        float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * mul;
-        // the row max over both halves
-        xch[hc * kRows + r] = mx;
-        if (warp == 1 && (tid & 31) < 8) tab[((j + 3) & 3) * 8 + (tid & 31)] = ahead;
-        // only warps w and w + 4 (the two halves of the same rows) meet here
-        pair_sync(1 + (warp & 3));
-        mx = fmaxf(mx, xch[(1 - hc) * kRows + r]);
-        const bool raise = mx > m + kSlack;
-        float alpha = 1.f;
-        if (raise) {
-            alpha = m == neg_inf() ? 0.f : ex2(m - mx);
-            m = mx;
-            l *= alpha;
-        }
-        // the previous tile's O += P V must be done before P and O are touched
-        bool o_done = true;
-        if (j > 0 && !wait_bar(bar(6), (j - 1) & 1)) {
-            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-            *abort_flag = 1;
-            o_done = false;
-        }
-        fence_after_sync();
-        {
-            // stages freed: V of tile j - 1 (its O += P V is done), K of tile
-            // j (its S was read above).  16 copies, one block each, two per
-            // warp (lanes 0-1): copy c = 2 warp + lane, c < 8 the K blocks of
-            // tile j + 2, the rest the V blocks of tile j + 1 (spread so no
-            // warp reaches the barrier late behind a queue of copy issues).
-            // A warp in which a wait ran out issues nothing (the CTA stops at
-            // the barrier; the drain's bounded waits outlast whatever was
-            // issued).
-            const int ln = tid & 31;
-            const bool all_done = __all_sync(0xffffffffu, o_done);
-            if (ln < 2) {
-                const int c = warp * 2 + ln;
-                const bool is_v = c >= 8;
-                const int jt = is_v ? j + 1 : j + 2;
-                if (all_done && jt < ntiles) {
-                    const int st = jt & 1;
-                    const uint32_t fb = bar((is_v ? 2 : 0) + st);
-                    if ((c & 7) == 0) mbar_arrive_expect_tx(fb, kTile);
-                    const int jj = c & 7;
-                    tma_load_block(sbase + (is_v ? kOffV : kOffK) + st * kTile + jj * 4096, is_v ? &vmap : &kmap,
-                                   tab[(jt & 3) * 8 + jj] >> 3, fb);
+    if (!softmax) {
+        // ================= producers: S issuer, O issuer, K copies, V copies
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+        if (warp == kWarpS && lane == 0) {
+            // S(j) = Q K(j)^T into S buffer j % 2, once K(j) has landed and
+            // the softmax has read S(j - 2) out of that buffer
+            const uint32_t idesc = instr_desc<T>(false);
+            int last = -1;
+            for (int j = 0; j < ntiles && !stopped(); ++j) {
+                const int s = j & 1;
+                if (!wait_bar(bar(kBarKFull + s), (j >> 1) & 1) ||
+                    (j >= 2 && !wait_bar(bar(kBarSFree + s), ((j - 2) >> 1) & 1))) {
+                    give_up();
+                    break;
                 }
-            }
-        }
-        if (j > 0 && __any_sync(0xffffffffu, raise)) {
+                fence_after_sync();
+                const uint32_t qa = sbase + kOffQ, kb = sbase + kOffK + s * kTile;
 #pragma unroll
-            for (int cc = 0; cc < kHalf / 32; ++cc) {
-                float v[32];
-                tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tmem_st32(tO + lane_base + hc * kHalf + cc * 32, v);
+                for (int kk = 0; kk < kDim / 16; ++kk) {
+                    // Q: halves at 16 KiB, 8-row groups at 1 KiB; K: halves
+                    // at 1 KiB, 8-key groups at 2 KiB
+                    const uint32_t qoff = (kk >> 2) * 16384 + (kk & 3) * 32, koff = (kk >> 2) * 1024 + (kk & 3) * 32;
+                    mma_f16(tS(s), smem_desc(qa + qoff, 16384, 1024), smem_desc(kb + koff, 1024, 2048), idesc,
+                            kk > 0);
+                }
+                mma_commit(bar(kBarSFull + s));
+                last = j;
             }
-            tmem_wait_st();
-        }
-        const float mref = m == neg_inf() ? 0.f : m;
-        float sum = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < kHalf / 8; ++ch) {
-            float p[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
-                sum += p[i];
-            }
-            uint4 hi;
-            hi.x = pack2<T>(p[0], p[1]);
-            hi.y = pack2<T>(p[2], p[3]);
-            hi.z = pack2<T>(p[4], p[5]);
-            hi.w = pack2<T>(p[6], p[7]);
-            const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
-            *reinterpret_cast<uint4*>(sm + kOffP + off) = hi;
-            if constexpr (kSplit) {
-                auto res = [](uint32_t w, float a0, float a1) {
-                    return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
-                };
-                uint4 lo;
-                lo.x = res(hi.x, p[0], p[1]);
-                lo.y = res(hi.y, p[2], p[3]);
-                lo.z = res(hi.z, p[4], p[5]);
-                lo.w = res(hi.w, p[6], p[7]);
-                *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = lo;
-            }
-        }
-        l += sum;
-        // keys past the context in this tile: their V rows may hold any bits
-        // (0 x NaN would poison O); zero them once the tile has landed
-        if (j * kKeys + kKeys > ctx) {
-            if (!wait_bar(bar(2 + s), (j >> 1) & 1)) {
-                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-                *abort_flag = 1;
-            } else if (j * kKeys + r >= ctx) {
-                uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + (r >> 4) * 4096 +
-                                                      ((r >> 3) & 1) * 2048 + hc * 1024 + (r & 7) * 128);
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
-            }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
-        fence_before_sync();
-        // the stop decision is the barrier's own OR of every thread's view of
-        // the flag, so that all threads take it alike even when thread 0 sets
-        // the flag just after the barrier
-        if (__syncthreads_or(*reinterpret_cast<volatile int*>(abort_flag))) {
-            aborted = true;
-            // copies issued so far: K tiles 0 .. j + 2, V tiles 0 .. j + 1
-            // (some of this iteration's may have been skipped: their phases
-            // then never complete and the drain's waits run out, bounded)
-            issued_k = min(ntiles, j + 3);
-            issued_v = min(ntiles, j + 2);
-            break;
-        }
-        // ---- O += P V (thread 0 issues)
-        if (tid == 0) {
-            fence_after_sync();
-            if (!wait_bar(bar(2 + s), (j >> 1) & 1)) {
-                atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-                *abort_flag = 1;
-            } else {
+            // stopping early: let the S MMAs in flight finish (bounded)
+            if (stopped() && last >= 0) wait_bar(bar(kBarSFull + (last & 1)), (last >> 1) & 1);
+        } else if (warp == kWarpO && lane == 0) {
+            // O += P(j) V(j), once the softmax has written P(j) and V(j) has
+            // landed; its completion frees P, O and V stage j % 2
+            const uint32_t idesc = instr_desc<T>(true);
+            int last = -1;
+            for (int j = 0; j < ntiles && !stopped(); ++j) {
+                const int s = j & 1;
+                if (!wait_bar(bar(kBarP), j & 1) || !wait_bar(bar(kBarVFull + s), (j >> 1) & 1)) {
+                    give_up();
+                    break;
+                }
+                fence_after_sync();
                 const uint32_t pa = sbase + kOffP, vb = sbase + kOffV + s * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
                     const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
                     // V of block kk: halves (N) at 1 KiB, 8-key groups (K) at 2 KiB
                     const uint64_t bd = smem_desc(vb + kk * 4096, 1024, 2048);
-                    mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc_o, j > 0 || kk > 0);
-                    if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc_o, true);
+                    mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc, j > 0 || kk > 0);
+                    if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc, true);
                 }
-                mma_commit(bar(6));
-                ++o_commits;
+                mma_commit(bar(kBarO));
+                mma_commit(bar(kBarVFree + s));
+                last = j;
             }
+            if (stopped() && last >= 0) wait_bar(bar(kBarO), last & 1);
+        } else if (warp == kWarpK || warp == kWarpV) {
+            // TMA copies of tile t into stage t % 2, one 16-row block per lane
+            // (lanes 0-7); stage t % 2 is free for K once S(t - 2) is done,
+            // for V once O(t - 2) is done.  The K warp's lanes 8-15 also
+            // prefetch the K and V rows of tile t + 2 into L2.
+            const bool is_v = warp == kWarpV;
+            const int jj = lane & 7;
+            const uint32_t base = sbase + (is_v ? kOffV : kOffK);
+            const CUtensorMap* map = is_v ? &vmap : &kmap;
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t & 1;
+                const int y = lane < 16 ? block_row(t * 8 + jj) : 0;
+                if (!is_v && lane >= 8 && lane < 16 && t + 2 < ntiles) {
+                    const int yp = block_row((t + 2) * 8 + jj);
+                    if (yp < a.total_rows) {
+                        prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(yp) * kDim, kBS * kDim * 2);
+                        prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(yp) * kDim, kBS * kDim * 2);
+                    }
+                }
+                int go = 1;
+                if (lane == 0) {
+                    go = !stopped();
+                    if (go && t >= 2) {
+                        go = is_v ? wait_bar(bar(kBarVFree + s), ((t - 2) >> 1) & 1)
+                                  : wait_bar(bar(kBarSFull + s), ((t - 2) >> 1) & 1);
+                        if (!go) give_up();
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, go, 0)) break;
+                if (lane < 8) {
+                    const uint32_t fb = bar((is_v ? kBarVFull : kBarKFull) + s);
+                    if (lane == 0) mbar_arrive_expect_tx(fb, kTile);
+                    tma_load_block(base + s * kTile + jj * 4096, map, y >> 3, fb);
+                }
+                issued = t + 1;
+            }
+            // stopping early: let the copies in flight land (bounded) before
+            // the shared memory is given up
+            if (lane == 0 && stopped()) {
+                for (int t = issued - 1; t >= 0 && t >= issued - 2; --t)
+                    wait_bar(bar((is_v ? kBarVFull : kBarKFull) + (t & 1)), (t >> 1) & 1);
+            }
+            __syncwarp();
         }
-        __syncwarp();
-    }
-    if (aborted && tid == 0) {
-        // let the copies and MMAs still in flight finish (bounded) before the
-        // shared memory and TMEM are given up
-        for (int t = issued_k - 1; t >= 0 && t >= issued_k - 2; --t) wait_bar(bar(t & 1), (t >> 1) & 1);
-        for (int t = issued_v - 1; t >= 0 && t >= issued_v - 2; --t) wait_bar(bar(2 + (t & 1)), (t >> 1) & 1);
-        if (o_commits > 0) wait_bar(bar(6), (o_commits - 1) & 1);
-    }
-    if (aborted && tid == kSIssuer) {
-        for (int s = 0; s < 2; ++s)
-            if (s_commits[s] > 0) wait_bar(bar(4 + s), (s_commits[s] - 1) & 1);
-    }
-    __syncwarp();
+    } else {
+        // ================= softmax warps
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+        const int my_pos = my_tok < L ? first_pos + my_tok : -1;  // padding rows: all masked
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        float m = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
+        bool late = false;  // a wait after the pair exchange ran out: stop at the next one
+        for (int j = 0; j < ntiles; ++j) {
+            const int s = j & 1;
+            // ---- this thread's half row of S(j), masked and scaled (base 2)
+            const bool want = !late && !__any_sync(0xffffffffu, stopped());
+            const bool have_s = want && __all_sync(0xffffffffu, wait_bar(bar(kBarSFull + s), (j >> 1) & 1));
+            float x[kHalf];
+            if (have_s) {
+                fence_after_sync();
+#pragma unroll
+                for (int cc = 0; cc < kHalf / 32; ++cc) {
+                    float v[32];
+                    tmem_ld32(tS(s) + lane_base + hc * kHalf + cc * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
+                }
+                tmem_wait_ld();
+                fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kBarSFree + s));  // the S buffer may be refilled
+            } else {
+#pragma unroll
+                for (int i = 0; i < kHalf; ++i) x[i] = neg_inf();
+            }
+            // A tile wholly at or below the CTA's first query position needs
+            // no causal mask (padding rows there see zero queries: finite
+            // scores, outputs never written).  With a positive scale the max
+            // is taken over raw scores and the scale enters the exponent's
+            // FMA (mul); otherwise the scores are scaled first.
+            const int key0 = j * kKeys + hc * kHalf;
+            const bool interior = j * kKeys + kKeys - 1 <= first_pos + tok0;
+            const float mul = a.scale_log2 > 0.f ? a.scale_log2 : 1.f;
+            if (a.scale_log2 > 0.f) {
+                if (!interior) {
+#pragma unroll
+                    for (int i = 0; i < kHalf; ++i)
+                        if (key0 + i > my_pos) x[i] = neg_inf();
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kHalf; ++i) x[i] = key0 + i <= my_pos ? x[i] * a.scale_log2 : neg_inf();
+            }
+            // the half row's max: three-input max, four independent chains
+            float mq[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+            for (int i = 4; i < kHalf; i += 8) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    mq[u] = max3f(mq[u], x[i + u], x[i + 4 + u < kHalf ? i + 4 + u : i + u]);
+            }
+            float mx = max3f(mq[0], mq[1], fmaxf(mq[2], mq[3])) * mul;
+            // the row max over both halves; warps w and w + 4 (the two halves
+            // of the same rows) meet here and stop together if either lacks S
+            xch[hc * kRows + r] = mx;
+            if (pair_sync_or(1 + (warp & 3), !have_s)) break;
+            mx = fmaxf(mx, xch[(1 - hc) * kRows + r]);
+            const bool raise = mx > m + kSlack;
+            float alpha = 1.f;
+            if (raise) {
+                alpha = m == neg_inf() ? 0.f : ex2(m - mx);
+                m = mx;
+                l *= alpha;
+            }
+            // the previous tile's O += P V must be done before P and O are touched
+            if (j > 0 && !__all_sync(0xffffffffu, wait_bar(bar(kBarO), (j - 1) & 1))) {
+                if (lane == 0) give_up();
+                late = true;
+                continue;
+            }
+            fence_after_sync();
+            if (j > 0 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+                for (int cc = 0; cc < kHalf / 32; ++cc) {
+                    float v[32];
+                    tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                    tmem_st32(tO + lane_base + hc * kHalf + cc * 32, v);
+                }
+                tmem_wait_st();
+            }
+            const float mref = m == neg_inf() ? 0.f : m;
+            float sum = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < kHalf / 8; ++ch) {
+                float p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
+                    sum += p[i];
+                }
+                uint4 hi;
+                hi.x = pack2<T>(p[0], p[1]);
+                hi.y = pack2<T>(p[2], p[3]);
+                hi.z = pack2<T>(p[4], p[5]);
+                hi.w = pack2<T>(p[6], p[7]);
+                const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
+                *reinterpret_cast<uint4*>(sm + kOffP + off) = hi;
+                if constexpr (kSplit) {
+                    auto res = [](uint32_t w, float a0, float a1) {
+                        return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
+                    };
+                    uint4 lo;
+                    lo.x = res(hi.x, p[0], p[1]);
+                    lo.y = res(hi.y, p[2], p[3]);
+                    lo.z = res(hi.z, p[4], p[5]);
+                    lo.w = res(hi.w, p[6], p[7]);
+                    *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = lo;
+                }
+            }
+            l += sum;
+            // keys past the context in this tile: their V rows may hold any
+            // bits (0 x NaN would poison O); zero them once the tile has landed
+            if (j * kKeys + kKeys > ctx) {
+                if (!__all_sync(0xffffffffu, wait_bar(bar(kBarVFull + s), (j >> 1) & 1))) {
+                    if (lane == 0) give_up();
+                    late = true;
+                    continue;
+                }
+                if (j * kKeys + r >= ctx) {
+                    uint4* row = reinterpret_cast<uint4*>(sm + kOffV + s * kTile + (r >> 4) * 4096 +
+                                                          ((r >> 3) & 1) * 2048 + hc * 1024 + (r & 7) * 128);
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarP));  // P(j) written, O rescaled
+        }
+        // the row sum over both halves
+        xch[hc * kRows + r] = l;
+        pair_sync(1 + (warp & 3));
+        l += xch[(1 - hc) * kRows + r];
 
-    // ---- epilogue: O / l for this thread's half row (l summed over halves)
-    xch[hc * kRows + r] = l;
-    __syncthreads();
-    l += xch[(1 - hc) * kRows + r];
-    bool ok = !aborted && ntiles > 0;
-    if (ok && !wait_bar(bar(6), (ntiles - 1) & 1)) {
-        atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
-        ok = false;
-    }
-    fence_after_sync();
-    T* orow = static_cast<T*>(a.out) + ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + my_h) * kDim;
-    if (__any_sync(0xffffffffu, ok)) {  // warp-collective TMEM loads
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        // ---- epilogue: O / l for this thread's half row
+        bool ok = !stopped() && ntiles > 0;
+        if (ok && !wait_bar(bar(kBarO), (ntiles - 1) & 1)) {
+            atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
+            ok = false;
+        }
+        fence_after_sync();
+        T* orow = static_cast<T*>(a.out) + ((static_cast<int64_t>(q0) + my_tok) * a.hq + kvh * a.G + my_h) * kDim;
+        if (__any_sync(0xffffffffu, ok)) {  // warp-collective TMEM loads
+            const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < kHalf / 32; ++cc) {
-            float v[32];
-            tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
-            tmem_wait_ld();
-            if (ok && my_tok < L) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + hc * kHalf + cc * 32);
+            for (int cc = 0; cc < kHalf / 32; ++cc) {
+                float v[32];
+                tmem_ld32(tO + lane_base + hc * kHalf + cc * 32, v);
+                tmem_wait_ld();
+                if (ok && my_tok < L) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + hc * kHalf + cc * 32);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 w;
-                    w.x = pack2<T>(v[8 * q] * inv, v[8 * q + 1] * inv);
-                    w.y = pack2<T>(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
-                    w.z = pack2<T>(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
-                    w.w = pack2<T>(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
-                    dst[q] = w;
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack2<T>(v[8 * q] * inv, v[8 * q + 1] * inv);
+                        w.y = pack2<T>(v[8 * q + 2] * inv, v[8 * q + 3] * inv);
+                        w.z = pack2<T>(v[8 * q + 4] * inv, v[8 * q + 5] * inv);
+                        w.w = pack2<T>(v[8 * q + 6] * inv, v[8 * q + 7] * inv);
+                        dst[q] = w;
+                    }
                 }
             }
+        } else if (ntiles == 0 && my_tok < L) {  // every position negative: zeros
+            for (int d = hc * kHalf; d < hc * kHalf + kHalf; ++d) orow[d] = Half16<T>::from_float(0.f);
         }
-    } else if (ntiles == 0 && my_tok < L) {  // every position negative: zeros
-        for (int d = hc * kHalf; d < hc * kHalf + kHalf; ++d) orow[d] = Half16<T>::from_float(0.f);
     }
     fence_before_sync();
     __syncthreads();
@@ -685,10 +708,16 @@ template <typename T>
 int launch_t(const CUtensorMap& km, const CUtensorMap& vm, const TcArgs& a, int tiles, int batch, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
+    static int regs = 0;
     std::call_once(once, [] {
         attr = cudaFuncSetAttribute(prefill_tc_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaFuncAttributes fa;
+        if (attr == cudaSuccess && (attr = cudaFuncGetAttributes(&fa, prefill_tc_kernel<T>)) == cudaSuccess)
+            regs = fa.numRegs;
     });
     if (attr != cudaSuccess) return PKV_ERR_CUDA;
+    // the warpgroups' register split needs the launch's full allocation
+    if (regs < kLaunchRegs) return PKV_ERR_UNSUPPORTED;
     prefill_tc_kernel<T><<<dim3(tiles, a.hkv, batch), kThreads, kSmemBytes, st>>>(km, vm, a);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
