@@ -82,6 +82,7 @@ constexpr int kThreads = 384;
 // softmax warpgroups raise theirs to 232 and the producer warpgroup lowers
 // its own to 40 (setmaxnreg): 2 x 128 x 232 + 128 x 40 = 384 x 168.
 constexpr int kLaunchRegs = 168;
+constexpr int kNoBlock = -2147483647 - 1;  // a tile slot past the context
 static_assert(2 * 128 * 232 + 128 * 40 <= kThreads * kLaunchRegs, "register split exceeds the launch's registers");
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -361,19 +362,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + kKeys;  // S buffers at columns 0 and 256, O at 128
     auto tS = [&](int s) { return tmem + (s ? 2 * kKeys : 0); };
     const int32_t* trow = a.tables + static_cast<int64_t>(b) * a.max_blocks;
-    // TMA row of logical block lb (a global load of the table; past the
-    // context or a bad id: the map's end, which TMA fills with zeros)
-    auto block_row = [&](int lb) {
-        int y = a.total_rows;
-        if (lb < nblk) {
-            const int phys = trow[lb];
-            if (static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks))
-                y = (phys * a.hkv + kvh) * kBS;
-            else
-                atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
-        }
-        return y;
-    };
     auto stopped = [&]() { return *reinterpret_cast<volatile int*>(abort_flag) != 0; };
     auto give_up = [&]() {
         atomicOr(a.status, PKV_STATUS_COPY_TIMEOUT);
@@ -440,21 +428,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             // TMA copies of tile t into stage t % 2, one 16-row block per lane
             // (lanes 0-7); stage t % 2 is free for K once S(t - 2) is done,
             // for V once O(t - 2) is done.  The K warp's lanes 8-15 also
-            // prefetch the K and V rows of tile t + 2 into L2.
+            // prefetch the K and V rows of tile t + 2 into L2.  The table
+            // entries are loaded two tiles before their copies (one before
+            // their prefetch), so the warp never waits on those loads.
             const bool is_v = warp == kWarpV;
             const int jj = lane & 7;
+            const bool copier = lane < 8, prefetcher = !is_v && lane >= 8 && lane < 16;
             const uint32_t base = sbase + (is_v ? kOffV : kOffK);
             const CUtensorMap* map = is_v ? &vmap : &kmap;
+            // the physical block of block jj of tile t (kNoBlock: none), and its TMA
+            // row: the load is only consumed a tile or two later, and nothing
+            // branches on it before then (a bad id is reported once, at the end)
+            auto entry_at = [&](int t) {
+                const int lb = t * 8 + jj;
+                return t < ntiles && lb < nblk ? __ldg(trow + lb) : kNoBlock;
+            };
+            bool bad = false;
+            auto row_of = [&](int phys) {
+                const bool ok = static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
+                bad |= phys != kNoBlock && !ok;
+                return ok ? (phys * a.hkv + kvh) * kBS : a.total_rows;
+            };
+            // copier lanes: entries of tiles t and t + 1; prefetcher lanes: of tile t + 2
+            int e = copier ? entry_at(0) : (prefetcher ? entry_at(2) : kNoBlock);
+            int e_next = copier ? entry_at(1) : kNoBlock;
             int issued = 0;
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t & 1;
-                const int y = lane < 16 ? block_row(t * 8 + jj) : 0;
-                if (!is_v && lane >= 8 && lane < 16 && t + 2 < ntiles) {
-                    const int yp = block_row((t + 2) * 8 + jj);
-                    if (yp < a.total_rows) {
-                        prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(yp) * kDim, kBS * kDim * 2);
-                        prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(yp) * kDim, kBS * kDim * 2);
-                    }
+                const int e_after = copier ? entry_at(t + 2) : (prefetcher ? entry_at(t + 3) : kNoBlock);
+                const int y = row_of(e);
+                if (prefetcher && y < a.total_rows) {
+                    prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
+                    prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
                 }
                 int go = 1;
                 if (lane == 0) {
@@ -466,13 +471,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, go, 0)) break;
-                if (lane < 8) {
+                if (copier) {
                     const uint32_t fb = bar((is_v ? kBarVFull : kBarKFull) + s);
                     if (lane == 0) mbar_arrive_expect_tx(fb, kTile);
                     tma_load_block(base + s * kTile + jj * 4096, map, y >> 3, fb);
+                    e = e_next;
+                    e_next = e_after;
+                } else {
+                    e = e_after;
                 }
                 issued = t + 1;
             }
+            if (bad && !is_v) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
             // stopping early: let the copies in flight land (bounded) before
             // the shared memory is given up
             if (lane == 0 && stopped()) {
@@ -550,7 +560,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = mx;
                 l *= alpha;
             }
-            // the previous tile's O += P V must be done before P and O are touched
+            // P of this half row in chunks of 8 keys: the first kPre are
+            // computed and packed before the wait for the previous O += P V
+            // (which then overlaps their exponentials), the rest after it,
+            // each stored as it is made.  3 of the 8 measured best (per
+            // call: 419 us; 432, 424, 451, 440 us for 2, 4, 5, 6; 449 us with
+            // all after the wait, 435 us with all before).
+            const float mref = m == neg_inf() ? 0.f : m;
+            float sum = 0.f;
+            constexpr int kPre = 3;
+            uint4 phi[kPre], plo[kSplit ? kPre : 1];
+            auto res = [](uint32_t w, float a0, float a1) {
+                return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
+            };
+#pragma unroll
+            for (int ch = 0; ch < kPre; ++ch) {
+                float p[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
+                    sum += p[i];
+                }
+                phi[ch].x = pack2<T>(p[0], p[1]);
+                phi[ch].y = pack2<T>(p[2], p[3]);
+                phi[ch].z = pack2<T>(p[4], p[5]);
+                phi[ch].w = pack2<T>(p[6], p[7]);
+                if constexpr (kSplit) {
+                    plo[ch].x = res(phi[ch].x, p[0], p[1]);
+                    plo[ch].y = res(phi[ch].y, p[2], p[3]);
+                    plo[ch].z = res(phi[ch].z, p[4], p[5]);
+                    plo[ch].w = res(phi[ch].w, p[6], p[7]);
+                }
+            }
             if (j > 0 && !__all_sync(0xffffffffu, wait_bar(bar(kBarO), (j - 1) & 1))) {
                 if (lane == 0) give_up();
                 late = true;
@@ -569,10 +610,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tmem_wait_st();
             }
-            const float mref = m == neg_inf() ? 0.f : m;
-            float sum = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < kHalf / 8; ++ch) {
+            for (int ch = 0; ch < kPre; ++ch) {
+                const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
+                *reinterpret_cast<uint4*>(sm + kOffP + off) = phi[ch];
+                if constexpr (kSplit) *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = plo[ch];
+            }
+#pragma unroll
+            for (int ch = kPre; ch < kHalf / 8; ++ch) {
                 float p[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -587,9 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
                 *reinterpret_cast<uint4*>(sm + kOffP + off) = hi;
                 if constexpr (kSplit) {
-                    auto res = [](uint32_t w, float a0, float a1) {
-                        return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
-                    };
                     uint4 lo;
                     lo.x = res(hi.x, p[0], p[1]);
                     lo.y = res(hi.y, p[2], p[3]);
