@@ -95,18 +95,16 @@ constexpr uint64_t kWaitNs = 300000000ull;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;      // 2 stages
 constexpr int kOffV = kOffK + 2 * kTile;  // 2 stages
-constexpr int kOffP = kOffV + 2 * kTile;  // P, then its residual (bf16)
-constexpr int kOffBar = kOffP + 2 * kTile;           // mbarriers, then the TMEM address and stop flag
+constexpr int kOffBar = kOffV + 2 * kTile;           // mbarriers, then the TMEM address and stop flag
 constexpr int kOffXch = kOffBar + 256;                // [2][128] floats: row values of the two halves
 // mbarriers (index: count)
 constexpr int kBarKFull = 0;   // 2 (per stage): the K tile has landed (TMA)
 constexpr int kBarVFull = 2;   // 2: the V tile has landed
 constexpr int kBarSFull = 4;   // 2 (per S buffer): S = Q K^T done
-constexpr int kBarO = 6;       // O += P V done: P, O and the V stage may be touched
-constexpr int kBarP = 7;       // 8 (softmax warps): P written, O rescaled
-constexpr int kBarSFree = 8;   // 2 x 8: the softmax has read S out of the buffer
-constexpr int kBarVFree = 10;  // 2: O += P V done reading the V stage
-constexpr int kNumBars = 12;
+constexpr int kBarO = 6;       // O += P V done: O may be touched
+constexpr int kBarP = 7;       // 8 (softmax warps): P written into TMEM, O rescaled
+constexpr int kBarVFree = 8;   // 2 (per stage / buffer): O += P V done reading V and P
+constexpr int kNumBars = 10;
 constexpr int kSmemBytes = kOffXch + 2 * 128 * 4 + 1024;  // then alignment slack
 
 struct TcArgs {
@@ -208,6 +206,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         : "memory");
 }
 
+// the same with A read from TMEM (lane = row, K elements packed two per
+// 32-bit column), B from shared memory
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(static_cast<uint32_t>(acc))
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -235,10 +244,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-    uint32_t r[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
@@ -247,6 +253,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+    tmem_st32(taddr, r);
 }
 
 // max of three floats (one instruction on sm_100 and later)
@@ -327,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i)
-            mbar_init(bar(i), (i == kBarP || i == kBarSFree || i == kBarSFree + 1) ? kSoftmaxWarps : 1);
+            mbar_init(bar(i), i == kBarP ? kSoftmaxWarps : 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -373,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
         if (warp == kWarpS && lane == 0) {
             // S(j) = Q K(j)^T into S buffer j % 2, once K(j) has landed and
-            // the softmax has read S(j - 2) out of that buffer
+            // O += P(j - 2) V(j - 2) has read P(j - 2) out of that buffer
             const uint32_t idesc = instr_desc<T>(false);
             int last = -1;
             for (int j = 0; j < ntiles && !stopped(); ++j) {
                 const int s = j & 1;
                 if (!wait_bar(bar(kBarKFull + s), (j >> 1) & 1) ||
-                    (j >= 2 && !wait_bar(bar(kBarSFree + s), ((j - 2) >> 1) & 1))) {
+                    (j >= 2 && !wait_bar(bar(kBarVFree + s), ((j - 2) >> 1) & 1))) {
                     give_up();
                     break;
                 }
@@ -410,14 +423,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 fence_after_sync();
-                const uint32_t pa = sbase + kOffP, vb = sbase + kOffV + s * kTile;
+                const uint32_t vb = sbase + kOffV + s * kTile;
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    const uint32_t aoff = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    // V of block kk: halves (N) at 1 KiB, 8-key groups (K) at 2 KiB
+                    // P of keys 16 kk .. +15: TMEM columns 8 kk .. +7 of S
+                    // buffer s (its residual 64 columns further); V of block
+                    // kk: halves (N) at 1 KiB, 8-key groups (K) at 2 KiB
                     const uint64_t bd = smem_desc(vb + kk * 4096, 1024, 2048);
-                    mma_f16(tO, smem_desc(pa + aoff, 16384, 1024), bd, idesc, j > 0 || kk > 0);
-                    if constexpr (kSplit) mma_f16(tO, smem_desc(pa + kTile + aoff, 16384, 1024), bd, idesc, true);
+                    mma_f16_ts(tO, tS(s) + kk * 8, bd, idesc, j > 0 || kk > 0);
+                    if constexpr (kSplit) mma_f16_ts(tO, tS(s) + kKeys / 2 + kk * 8, bd, idesc, true);
                 }
                 mma_commit(bar(kBarO));
                 mma_commit(bar(kBarVFree + s));
@@ -514,9 +528,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) x[cc * 32 + i] = v[i];
                 }
                 tmem_wait_ld();
-                fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kBarSFree + s));  // the S buffer may be refilled
             } else {
 #pragma unroll
                 for (int i = 0; i < kHalf; ++i) x[i] = neg_inf();
@@ -560,44 +571,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = mx;
                 l *= alpha;
             }
-            // P of this half row in chunks of 8 keys: the first kPre are
-            // computed and packed before the wait for the previous O += P V
-            // (which then overlaps their exponentials), the rest after it,
-            // each stored as it is made.  3 of the 8 measured best (per
-            // call: 419 us; 432, 424, 451, 440 us for 2, 4, 5, 6; 449 us with
-            // all after the wait, 435 us with all before).
+            // P of this half row, packed (bf16: value and rounding residual),
+            // written over S(j) in TMEM: the thread's row (lane), keys
+            // 64 hc .. +63 as 32 columns from column 32 hc of the buffer,
+            // their residuals 64 columns further (the partner warp has read
+            // its half of S(j): it passed the pair barrier).  P of the
+            // previous tile sits in the other buffer; the store still waits
+            // for the previous O += P V, which has mostly finished while the
+            // exponentials ran: without that wait three of four runs of the
+            // parity tests had one CTA's row wrong (cause not found).
             const float mref = m == neg_inf() ? 0.f : m;
             float sum = 0.f;
-            constexpr int kPre = 3;
-            uint4 phi[kPre], plo[kSplit ? kPre : 1];
-            auto res = [](uint32_t w, float a0, float a1) {
-                return pack2<T>(a0 - __uint_as_float(w << 16), a1 - __uint_as_float(w & 0xffff0000u));
-            };
+            uint32_t phi[kHalf / 2], plo[kSplit ? kHalf / 2 : 1];
 #pragma unroll
-            for (int ch = 0; ch < kPre; ++ch) {
-                float p[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
-                    sum += p[i];
-                }
-                phi[ch].x = pack2<T>(p[0], p[1]);
-                phi[ch].y = pack2<T>(p[2], p[3]);
-                phi[ch].z = pack2<T>(p[4], p[5]);
-                phi[ch].w = pack2<T>(p[6], p[7]);
-                if constexpr (kSplit) {
-                    plo[ch].x = res(phi[ch].x, p[0], p[1]);
-                    plo[ch].y = res(phi[ch].y, p[2], p[3]);
-                    plo[ch].z = res(phi[ch].z, p[4], p[5]);
-                    plo[ch].w = res(phi[ch].w, p[6], p[7]);
-                }
+            for (int i = 0; i < kHalf; i += 2) {
+                const float p0 = ex2(fmaf(x[i], mul, -mref)), p1 = ex2(fmaf(x[i + 1], mul, -mref));
+                sum += p0 + p1;
+                phi[i / 2] = pack2<T>(p0, p1);
+                if constexpr (kSplit)
+                    plo[i / 2] = pack2<T>(p0 - __uint_as_float(phi[i / 2] << 16),
+                                          p1 - __uint_as_float(phi[i / 2] & 0xffff0000u));
             }
+            l += sum;
             if (j > 0 && !__all_sync(0xffffffffu, wait_bar(bar(kBarO), (j - 1) & 1))) {
                 if (lane == 0) give_up();
                 late = true;
                 continue;
             }
             fence_after_sync();
+            tmem_st32(tS(s) + lane_base + hc * (kHalf / 2), phi);
+            if constexpr (kSplit) tmem_st32(tS(s) + lane_base + kKeys / 2 + hc * (kHalf / 2), plo);
+            // a moved reference max: O is rescaled before this tile's P V
+            // adds to it
             if (j > 0 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
                 for (int cc = 0; cc < kHalf / 32; ++cc) {
@@ -608,39 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 32; ++i) v[i] *= alpha;
                     tmem_st32(tO + lane_base + hc * kHalf + cc * 32, v);
                 }
-                tmem_wait_st();
             }
-#pragma unroll
-            for (int ch = 0; ch < kPre; ++ch) {
-                const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
-                *reinterpret_cast<uint4*>(sm + kOffP + off) = phi[ch];
-                if constexpr (kSplit) *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = plo[ch];
-            }
-#pragma unroll
-            for (int ch = kPre; ch < kHalf / 8; ++ch) {
-                float p[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    p[i] = ex2(fmaf(x[ch * 8 + i], mul, -mref));
-                    sum += p[i];
-                }
-                uint4 hi;
-                hi.x = pack2<T>(p[0], p[1]);
-                hi.y = pack2<T>(p[2], p[3]);
-                hi.z = pack2<T>(p[4], p[5]);
-                hi.w = pack2<T>(p[6], p[7]);
-                const uint32_t off = tile_off(r, hc * kHalf + ch * 8);
-                *reinterpret_cast<uint4*>(sm + kOffP + off) = hi;
-                if constexpr (kSplit) {
-                    uint4 lo;
-                    lo.x = res(hi.x, p[0], p[1]);
-                    lo.y = res(hi.y, p[2], p[3]);
-                    lo.z = res(hi.z, p[4], p[5]);
-                    lo.w = res(hi.w, p[6], p[7]);
-                    *reinterpret_cast<uint4*>(sm + kOffP + kTile + off) = lo;
-                }
-            }
-            l += sum;
+            tmem_wait_st();
             // keys past the context in this tile: their V rows may hold any
             // bits (0 x NaN would poison O); zero them once the tile has landed
             if (j * kKeys + kKeys > ctx) {
@@ -656,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int ch = 0; ch < 8; ++ch) row[ch] = make_uint4(0, 0, 0, 0);
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P (and zeroed V) to the MMA
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // zeroed V rows to the MMA
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarP));  // P(j) written, O rescaled
