@@ -18,8 +18,8 @@
 // * Warps 0-7 (two warpgroups, 232 registers each after setmaxnreg) do the
 //   softmax; warps 8-11 (one warpgroup, 40 registers) issue: lane 0 of warp
 //   8 the S MMAs, lane 0 of warp 9 the O MMAs, warps 10 and 11 the K and V
-//   copies (a lane per block, the table entries loaded by the same lanes,
-//   the K warp also prefetching the rows two tiles ahead into L2).  An MMA
+//   copies (a lane per block, the table entries loaded by the same lanes
+//   two tiles ahead).  An MMA
 //   issue blocks while the tensor pipe drains (16 MMAs of a tile take ~1,200
 //   cycles to issue), so no softmax warp issues any.
 // * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into one of two
@@ -75,7 +75,7 @@ constexpr int kTile = kRows * kDim * 2;  // bytes of one 128 x 128 16-bit tile
 constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpS = 8;   // lane 0 issues S = Q K^T
 constexpr int kWarpO = 9;   // lane 0 issues O += P V
-constexpr int kWarpK = 10;  // K copies (and L2 prefetches)
+constexpr int kWarpK = 10;  // K copies
 constexpr int kWarpV = 11;  // V copies
 constexpr int kThreads = 384;
 // Registers: launched at 168 a thread (384 threads, one CTA per SM), the
@@ -109,8 +109,6 @@ constexpr int kSmemBytes = kOffXch + 2 * 128 * 4 + 1024;  // then alignment slac
 
 struct TcArgs {
     const void* q;
-    const void* k_pool;  // the pools (for L2 prefetches; the tiles come by TMA)
-    const void* v_pool;
     const int32_t* q_start;
     const int32_t* tables;
     const int32_t* ctx_lens;
@@ -174,11 +172,6 @@ __device__ __forceinline__ void tma_load_block(uint32_t dst, const CUtensorMap* 
         "%3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(w), "r"(bar)
         : "memory");
-}
-
-// Bring `bytes` at p into L2 ahead of their copies (no data returned).
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // UMMA shared-memory descriptor: start, leading and stride byte offsets (16-
@@ -441,13 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (warp == kWarpK || warp == kWarpV) {
             // TMA copies of tile t into stage t % 2, one 16-row block per lane
             // (lanes 0-7); stage t % 2 is free for K once S(t - 2) is done,
-            // for V once O(t - 2) is done.  The K warp's lanes 8-15 also
-            // prefetch the K and V rows of tile t + 2 into L2.  The table
-            // entries are loaded two tiles before their copies (one before
-            // their prefetch), so the warp never waits on those loads.
+            // for V once O(t - 2) is done.  The table entries are loaded two
+            // tiles before their copies, so the warp never waits on those
+            // loads.  (Prefetching the rows into L2 ahead of the copies, one
+            // bulk prefetch per block, cost more than it saved once the copy
+            // engine was the busiest unit: 368 -> 340 us without it.)
             const bool is_v = warp == kWarpV;
             const int jj = lane & 7;
-            const bool copier = lane < 8, prefetcher = !is_v && lane >= 8 && lane < 16;
+            const bool copier = lane < 8;
             const uint32_t base = sbase + (is_v ? kOffV : kOffK);
             const CUtensorMap* map = is_v ? &vmap : &kmap;
             // the physical block of block jj of tile t (kNoBlock: none), and its TMA
@@ -463,18 +457,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bad |= phys != kNoBlock && !ok;
                 return ok ? (phys * a.hkv + kvh) * kBS : a.total_rows;
             };
-            // copier lanes: entries of tiles t and t + 1; prefetcher lanes: of tile t + 2
-            int e = copier ? entry_at(0) : (prefetcher ? entry_at(2) : kNoBlock);
+            // entries of tiles t and t + 1
+            int e = copier ? entry_at(0) : kNoBlock;
             int e_next = copier ? entry_at(1) : kNoBlock;
             int issued = 0;
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t & 1;
-                const int e_after = copier ? entry_at(t + 2) : (prefetcher ? entry_at(t + 3) : kNoBlock);
+                const int e_after = copier ? entry_at(t + 2) : kNoBlock;
                 const int y = row_of(e);
-                if (prefetcher && y < a.total_rows) {
-                    prefetch_l2(static_cast<const T*>(a.k_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
-                    prefetch_l2(static_cast<const T*>(a.v_pool) + static_cast<int64_t>(y) * kDim, kBS * kDim * 2);
-                }
                 int go = 1;
                 if (lane == 0) {
                     go = !stopped();
@@ -491,8 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_block(base + s * kTile + jj * 4096, map, y >> 3, fb);
                     e = e_next;
                     e_next = e_after;
-                } else {
-                    e = e_after;
                 }
                 issued = t + 1;
             }
@@ -754,8 +742,6 @@ int launch_prefill_tc(const void* q, const int32_t* q_start, const void* k_pool,
     if (!pool_map(&km, k_pool, rows, bf16) || !pool_map(&vm, v_pool, rows, bf16)) return PKV_ERR_CUDA;
     TcArgs a;
     a.q = q;
-    a.k_pool = k_pool;
-    a.v_pool = v_pool;
     a.q_start = q_start;
     a.tables = tables;
     a.ctx_lens = ctx_lens;
