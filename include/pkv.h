@@ -174,6 +174,16 @@ int pkv_build_block_tables(const pkv_pool* pool, const int64_t* seqs, int32_t n,
  * n < 0 disables. */
 int pkv_debug_fail_after(pkv_pool* pool, int64_t n_allocs);
 
+/* Test hook for the bounded waits of the tensor-core prefill kernel (the
+ * multi-query path for long query spans): while tile >= 0, no CTA issues
+ * the K copy of key tile `tile`, so the wait for it runs out after its time
+ * limit (~0.3 s); the kernel then sets PKV_STATUS_COPY_TIMEOUT, lets its
+ * copies and MMAs in flight finish (each wait again bounded) and stops,
+ * leaving the context usable.  Outputs of such a call are undefined.
+ * -1 (the default) turns it off; below -1 is INVALID_ARG.  Device-wide
+ * (the current device), for tests only. */
+int pkv_debug_prefill_drop_copy(int32_t tile);
+
 /* ========================================================= prefix cache */
 
 /* Prefix cache ("Capítulo 8 — Gerenciamento de KV Cache de Próxima Geração",

@@ -65,6 +65,7 @@ _SIGS = {
     "pkv_seq_block_table": ([_vp, _i64, _vp, _i32], _int),
     "pkv_build_block_tables": ([_vp, _vp, _i32, _vp, _i32, _vp], _int),
     "pkv_debug_fail_after": ([_vp, _i64], _int),
+    "pkv_debug_prefill_drop_copy": ([_i32], _int),
     "pkv_prefix_register": ([_vp, _i64, _vp, _i32, _p_i32], _int),
     "pkv_prefix_match": ([_vp, _vp, _i32, _p_i64, _p_i32], _int),
     "pkv_prefix_evict": ([_vp, _i32, _p_i32], _int),
@@ -281,6 +282,12 @@ def pkv_build_block_tables(pool, seqs, max_blocks, tables_out=None, lens_out=Non
 
 def pkv_debug_fail_after(pool, n_allocs):
     _check(lib.pkv_debug_fail_after(pool, n_allocs), "pkv_debug_fail_after")
+
+
+def pkv_debug_prefill_drop_copy(tile):
+    """Test hook: the tensor-core prefill kernel skips the K copy of key
+    tile `tile` (-1: off), so its bounded wait for it runs out."""
+    _check(lib.pkv_debug_prefill_drop_copy(int(tile)), "pkv_debug_prefill_drop_copy")
 
 
 def pkv_prefix_register(pool, seq, tokens):

@@ -83,6 +83,10 @@ constexpr int kThreads = 384;
 // its own to 40 (setmaxnreg): 2 x 128 x 232 + 128 x 40 = 384 x 168.
 constexpr int kLaunchRegs = 168;
 constexpr int kNoBlock = -2147483647 - 1;  // a tile slot past the context
+
+// Test hook (pkv_debug_prefill_drop_copy): the K copy of this key tile is
+// never issued (-1: off), so the S issuer's bounded wait for it runs out.
+__device__ int g_drop_copy_tile = -1;
 static_assert(2 * 128 * 232 + 128 * 40 <= kThreads * kLaunchRegs, "register split exceeds the launch's registers");
 constexpr int kTmemCols = 512;  // the whole TMEM: one CTA per SM (shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -442,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool is_v = warp == kWarpV;
             const int jj = lane & 7;
             const bool copier = lane < 8;
+            const int drop = is_v ? -1 : *reinterpret_cast<volatile int*>(&g_drop_copy_tile);
             const uint32_t base = sbase + (is_v ? kOffV : kOffK);
             const CUtensorMap* map = is_v ? &vmap : &kmap;
             // the physical block of block jj of tile t (kNoBlock: none), and its TMA
@@ -475,13 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!__shfl_sync(0xffffffffu, go, 0)) break;
-                if (copier) {
+                if (copier && t != drop) {
                     const uint32_t fb = bar((is_v ? kBarVFull : kBarKFull) + s);
                     if (lane == 0) mbar_arrive_expect_tx(fb, kTile);
                     tma_load_block(base + s * kTile + jj * 4096, map, y >> 3, fb);
-                    e = e_next;
-                    e_next = e_after;
                 }
+                e = e_next;
+                e_next = e_after;
                 issued = t + 1;
             }
             if (bad && !is_v) atomicOr(a.status, PKV_STATUS_BAD_BLOCK);
@@ -760,3 +765,8 @@ int launch_prefill_tc(const void* q, const int32_t* q_start, const void* k_pool,
 }
 
 }  // namespace pkv
+
+extern "C" int pkv_debug_prefill_drop_copy(int32_t tile) {
+    if (tile < -1) return PKV_ERR_INVALID_ARG;
+    return cudaMemcpyToSymbol(pkv::g_drop_copy_tile, &tile, sizeof(tile)) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

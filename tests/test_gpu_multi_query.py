@@ -285,3 +285,24 @@ def test_prefill_tc_non_positive_scale(pkv, cuda_dev, scale):
     assert pkv.pkv_device_status() == 0
     assert not np.isnan(got).any()
     _check(c, q, q_start, got, what="tc scale %g" % scale)
+
+
+def test_prefill_tc_wait_runs_out_and_the_context_stays_usable(pkv, cuda_dev):
+    """A K copy that never comes (the test hook drops key tile 1 of every
+    CTA): the S issuer's bounded wait runs out, the kernel reports
+    PKV_STATUS_COPY_TIMEOUT and every CTA stops (no fault, no hang); the same
+    call with the hook off then gives the oracle's outputs and a clean
+    status."""
+    w = syn.workload("llama3_8b_b64", lens=[700, 500], num_blocks=128)
+    c = build(pkv, w, cuda_dev)
+    pkv.pkv_device_status()
+    try:
+        pkv.pkv_debug_prefill_drop_copy(1)
+        _run(pkv, c, [100, 80], seed=51)
+        st = pkv.pkv_device_status()
+    finally:
+        pkv.pkv_debug_prefill_drop_copy(-1)
+    assert st & pkv.PKV_STATUS_COPY_TIMEOUT
+    q, q_start, got = _run(pkv, c, [100, 80], seed=51)
+    assert pkv.pkv_device_status() == 0
+    _check(c, q, q_start, got, what="after a run-out wait")
