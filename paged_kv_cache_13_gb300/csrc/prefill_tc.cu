@@ -19,9 +19,9 @@
 //   softmax; warps 8-11 (one warpgroup, 40 registers) issue: lane 0 of warp
 //   8 the S MMAs, lane 0 of warp 9 the O MMAs, warps 10 and 11 the K and V
 //   copies (a lane per block, the table entries loaded by the same lanes
-//   two tiles ahead).  An MMA
-//   issue blocks while the tensor pipe drains (16 MMAs of a tile take ~1,200
-//   cycles to issue), so no softmax warp issues any.
+//   two tiles ahead).  An MMA issue blocks while the tensor pipe drains (16
+//   MMAs of a tile take ~1,200 cycles to issue), so no softmax warp issues
+//   any.
 // * S = Q K^T (M 128, N 128, K 128: 8 tcgen05.mma of K 16) into one of two
 //   TMEM S buffers (columns [0, 128) and [256, 384)): S(j + 1) is computed
 //   while the softmax of tile j runs.  Softmax warps w and w + 4 share the
@@ -31,24 +31,25 @@
 //   two halves exchange their maxima through shared memory under a barrier
 //   of just those two warps, for the online softmax (base 2, the reference
 //   max raised only by more than 8).
-//   P goes to shared memory (bf16: P and its rounding residual, two
-//   operands, so the products see ~16 bits of P).
-// * O += P V (M 128, N 128, K 128 keys) into TMEM columns [128, 256); a
-//   rescale of O (when a row's reference max moves) is a TMEM load / store
-//   of that half row.  O / l goes out at the end.
+// * P (bf16: P and its rounding residual, two operands, so the products see
+//   ~16 bits of P) is written into TMEM over its own S buffer, and O += P V
+//   (M 128, N 128, K 128 keys) takes A from TMEM, B (V) from shared memory,
+//   into TMEM columns [128, 256); S(j + 2) is issued once O += P(j) V(j) has
+//   read the buffer.  A rescale of O (when a row's reference max moves) is
+//   a TMEM load / store of that half row.  O / l goes out at the end.
 // * Hand-offs are mbarriers: K / V landed (TMA), S done and O done
-//   (tcgen05.commit), S read and P written (one arrival per softmax warp),
-//   the V stage read (a second commit).  Each waiter is at most one phase
+//   (tcgen05.commit), P written (one arrival per softmax warp), the V stage
+//   and P buffer read (a second commit).  Each waiter is at most one phase
 //   behind its barrier by construction (a barrier's next phase needs the
 //   waiter's own later arrival).
-// * Every operand tile is a grid of 8-row x 128-byte swizzle atoms (128-byte
-//   swizzle).  In Q and P atom (g, h) -- rows 8g .. 8g+7, columns 64h ..
-//   64h+63 -- sits at byte h * 16 KiB + g * 1 KiB of the tile; in K and V
-//   (one TMA box per 16-row block, so its two row groups and two column
-//   halves land together) at g * 2 KiB + h * 1 KiB.  K-major operands (Q,
-//   K, P) step 32 bytes per K-16 slice inside an atom row; V is the MN-major
-//   B operand of O += P V (its 8-key groups 2 KiB apart, its two 64-dim
-//   halves 1 KiB apart).
+// * Every shared-memory operand tile is a grid of 8-row x 128-byte swizzle
+//   atoms (128-byte swizzle).  In Q atom (g, h) -- rows 8g .. 8g+7, columns
+//   64h .. 64h+63 -- sits at byte h * 16 KiB + g * 1 KiB of the tile; in K
+//   and V (one TMA box per 16-row block, so its two row groups and two
+//   column halves land together) at g * 2 KiB + h * 1 KiB.  K-major
+//   operands (Q, K) step 32 bytes per K-16 slice inside an atom row; V is
+//   the MN-major B operand of O += P V (its 8-key groups 2 KiB apart, its
+//   two 64-dim halves 1 KiB apart).
 // * Every wait suspends in hardware (try_wait) and is bounded in time: one
 //   that runs out sets PKV_STATUS_COPY_TIMEOUT and the stop flag; softmax
 //   warp pairs stop together (the OR their barrier returns), the issuers
