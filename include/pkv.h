@@ -364,7 +364,10 @@ int pkv_paged_attention_decode_merge(const int32_t* context_lens, int32_t batch,
  *     block) items to fill the GPU): a balanced split.  Every warp streams
  *     an equal share of the call's (sequence, KV head, block) items, holding
  *     all L_b * G rows of its runs, so each K/V byte is read once.  A merge
- *     kernel follows behind it with programmatic dependent launch.  L_b >
+ *     kernel follows behind it with programmatic dependent launch; the split
+ *     kernel is itself launched that way and reads nothing before the
+ *     stream's previous grid has completed (behind pkv_kv_append, its CTAs
+ *     are made resident while the append runs).  L_b >
  *     max_q_len there sets PKV_STATUS_BAD_CONTEXT and only the first
  *     max_q_len * G rows are computed.  A workspace that is too small
  *     returns PKV_ERR_WORKSPACE.

@@ -23,6 +23,9 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
                                  int cpr, int block_size, int64_t num_slots,
                                  uint4* __restrict__ kp, uint4* __restrict__ vp,
                                  int* __restrict__ status) {
+    // a grid launched behind this one with programmatic serialization may be
+    // scheduled now (it waits for this grid to complete before reading)
+    asm volatile("griddepcontrol.launch_dependents;");
     const int64_t per_tok = static_cast<int64_t>(hkv) * cpr;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {

@@ -503,6 +503,9 @@ __global__ void __launch_bounds__(kMQWarps * 32, kMQCtas<NT>)
     constexpr int R = 8 * NT;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, c = lane & 3;
+    // launched behind the previous grid of the stream with programmatic
+    // serialization: nothing is read before that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the merge grid may be scheduled now; it waits for this grid to finish
     asm volatile("griddepcontrol.launch_dependents;");
     // per warp: the run's query fragments ([NT][KC][32] uint4) while it
@@ -778,9 +781,19 @@ size_t mq_balanced_bytes(int64_t batch, int64_t hkv, int D, int nt, int nwt) {
 
 template <typename T, int D, int NT>
 int run_mq_balanced(const MQArgs& a, int batch, int nwt, float* ws_o, float* ws_ml, cudaStream_t st) {
-    multi_query_balanced_kernel<T, D, NT>
-        <<<(nwt + kMQWarps - 1) / kMQWarps, kMQWarps * 32, 0, st>>>(a, batch, nwt, ws_o, ws_ml);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    {
+        cudaLaunchConfig_t c0 = {};
+        c0.gridDim = dim3((nwt + kMQWarps - 1) / kMQWarps);
+        c0.blockDim = dim3(kMQWarps * 32);
+        c0.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        c0.attrs = at;
+        c0.numAttrs = 1;
+        if (cudaLaunchKernelEx(&c0, multi_query_balanced_kernel<T, D, NT>, a, batch, nwt, ws_o, ws_ml) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.hkv, batch);
     cfg.blockDim = dim3(kMergeThreads);
