@@ -79,6 +79,8 @@ def test_host_validation_rejects_before_launch(pkv):
     assert L.pkv_kv_append(16, 16, 16, 0, 16, 16, 4, 2, 128, 16, 1, None) == 0
     # copy_blocks pool count limits
     assert L.pkv_copy_blocks(None, None, 0, None, 1, 4, None) == -1
+    # the prefill test hook takes a key tile or -1 (off)
+    assert L.pkv_debug_prefill_drop_copy(-2) == -1
 
 
 def test_workspace_bytes(pkv):
